@@ -1,0 +1,460 @@
+"""Benchmark of the GB300 hyper-connection read.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {gb300,reference}]
+
+One step = the verify-window sweep: 16 reads, T = 1..8 tokens each with and
+without a pending write, every read on a different weight set out of a rotation
+of 48 sets (630 MB of bf16 weights, larger than the 129 MB L2), so every read
+streams its 13 MB of weights from HBM. ``value`` = microseconds per read, device
+time from CUDA events around K steps (each step replayed as one CUDA graph;
+inputs resident in HBM). ``e2e`` = the same reads through the public call with
+the inputs copied from pinned host memory and the outputs copied back inside
+the timed region. Extra keys carry the 96-read cold round, per-T times and the
+8K / 32K-token prefill chunks.
+
+``--impl reference`` times the CPU oracle (float64, single thread) on a bounded
+sample of the same sweep: it is the reference arm, not a GPU implementation.
+
+Multi-GPU: the read does not shard (replicas only); with N ranks every rank runs
+its own sweep and ``value`` = max-over-ranks time / all reads of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per hc read at 1-8 tokens and ms at 8K/32K; % of GB300 HBM roofline"
+WEIGHT_BYTES = 320 * 10240 * 2 + 10240 * 320 * 2 + 4 * 2560 * 2   # 13,127,680
+SWEEP = [(T, p) for T in range(1, 9) for p in (False, True)]      # 16 reads per step
+N_SETS = 48
+EPS = float(np.float32(1e-6))
+
+# DRAM bytes per read measured by ncu for the decode kernels (sum of both kernels,
+# one 4-token read with a pending write); None until a capture of the current
+# kernels exists.
+NCU_TRAFFIC_PER_READ = None
+
+
+def read_bytes(T: int, with_P: bool) -> int:
+    """Algorithmic bytes of one read: weights once, activations in, outputs out."""
+    per_tok = 40960 + (40960 if with_P else 0) + 64 + 81920
+    return WEIGHT_BYTES + T * per_tok
+
+
+def prefill_upmix_bytes(T: int) -> int:
+    """Algorithmic bytes of the fused up + gate + mix over T tokens (lo, R', Rmix in,
+    the three outputs out, W_up once)."""
+    return 10240 * 320 * 2 + T * (1280 + 40960 + 64 + 81920)
+
+
+def prefill_read_bytes(T: int) -> int:
+    """Algorithmic bytes of the whole prefill read (down + fused up/mix)."""
+    return WEIGHT_BYTES + T * (40960 + 64 + 81920)
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"hc_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle, single-threaded
+# ---------------------------------------------------------------------------
+
+_CPU_SNIPPET = r"""
+import json, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+from hyper_connection_residual_read_gb300 import synth
+from oracle import hc_oracle as O
+budget = float(sys.argv[1]); min_sweeps = int(sys.argv[2])
+w = synth.make_weights(0)
+cases = [(T, p) for T in range(1, 9) for p in (False, True)]
+acts = [synth.make_activations(1 + i, T, p) for i, (T, p) in enumerate(cases)]
+sweeps = []; t0 = time.perf_counter()
+while len(sweeps) < min_sweeps or time.perf_counter() - t0 < budget:
+    t1 = time.perf_counter()
+    for a in acts:
+        O.hc_read(a["R"], a["P"], w["w_norm"], w["W_down"], w["W_up"], a["Rmix"], {eps!r})
+    sweeps.append(time.perf_counter() - t1)
+print(json.dumps({{"sweep_seconds": sweeps, "reads_per_sweep": len(cases)}}))
+"""
+
+
+def run_oracle_sample(budget_s: float, min_sweeps: int) -> dict:
+    """Runs the oracle, single-threaded, in a fresh process over whole sweeps until
+    both ``min_sweeps`` sweeps and ``budget_s`` seconds are done."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = _CPU_SNIPPET.format(root=ROOT, eps=EPS)
+    r = subprocess.run([sys.executable, "-c", code, str(budget_s), str(min_sweeps)],
+                       capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle sample failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def reference_arm(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    d = run_oracle_sample(0.0, args.warmup + args.steps)
+    per_step = d["sweep_seconds"][args.warmup:]
+    us = 1e6 * statistics.mean(per_step) / len(SWEEP)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us/read",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(per_step), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config("CPU oracle, float64 numpy, one thread"),
+        "cpu_baseline": {"value": us, "unit": "us/read", "cores": 1, "kind": "oracle",
+                         "sample": "one verify-window sweep (16 reads, T=1..8 x {no P, P}) "
+                                   "per step, one weight set, float64 numpy, 1 thread",
+                         "cpu": cpu_model()},
+        "e2e": {"value": us, "unit": "us/read", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def workload_config(launch: str = "one CUDA graph per step") -> dict:
+    return {"workload": "verify-window sweep: T=1..8 tokens x {no pending write, pending "
+                        "write}, 16 reads per step, 4x2560 fp32 residual, 10240->320->10240 "
+                        "bf16 weights",
+            "weight_sets": N_SETS, "l2": "weights rotated over 48 sets (630 MB > 129 MB L2)",
+            "launch": launch}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def gpu_arm(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import hyper_connection_residual_read_gb300 as hc
+    from hyper_connection_residual_read_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hc.hc_read_init(local, 32768, EPS)
+
+    def to_dev(x, dtype=None):
+        if x is None:
+            return None
+        t = torch.from_numpy(np.ascontiguousarray(x.view(np.int16) if x.dtype == np.uint16 else x))
+        return t.to(dev)
+
+    # weights: 48 sets; activations: one set per sweep case and rotation slot
+    sets = []
+    for k in range(N_SETS):
+        w = synth.make_weights(7000 + 97 * rank + k)
+        sets.append({n: to_dev(v) for n, v in w.items()})
+    acts = []
+    for i in range(N_SETS):
+        T, p = SWEEP[i % len(SWEEP)]
+        a = synth.make_activations(9000 + 97 * rank + i, T, p)
+        acts.append({"T": T, "P": p, "host": a,
+                     "R": to_dev(a["R"]), "Pd": to_dev(a["P"]), "M": to_dev(a["Rmix"])})
+    outs = [tuple(torch.empty((T, 4, 2560), dtype=dt, device=dev)
+                  for dt in (torch.float32, torch.int16, torch.int16))
+            for (T, _p) in [(x["T"], x["P"]) for x in acts]]
+
+    stream = torch.cuda.Stream(device=dev)
+    n_groups = N_SETS // len(SWEEP)   # 3 steps cover the 48 rotation slots
+
+    def enqueue_step(g: int):
+        for j in range(len(SWEEP)):
+            i = g * len(SWEEP) + j
+            a, W = acts[i], sets[i]
+            hc.hc_read(a["T"], a["R"], a["Pd"], W["w_norm"], W["W_down"], W["W_up"], a["M"],
+                       *outs[i], stream=stream)
+
+    # one graph per rotation group
+    graphs = []
+    with torch.cuda.stream(stream):
+        for g in range(n_groups):
+            enqueue_step(g)
+        stream.synchronize()
+        for g in range(n_groups):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                enqueue_step(g)
+            graphs.append(gr)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def timed(fn, steps, warmup):
+        """Device time of `steps` calls of fn on `stream`, after `warmup` calls."""
+        with torch.cuda.stream(stream):
+            for k in range(warmup):
+                fn(k)
+            barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for k in range(steps):
+                fn(k)
+            e1.record(stream)
+            barrier()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    # --- main number: graph replays of the sweep ---
+    with ClockSampler(local) as clk:
+        ms = timed(lambda k: graphs[k % n_groups].replay(), args.steps, args.warmup)
+    clocks = clk.summary()
+    reads_per_step = len(SWEEP)
+    us_per_read = 1e3 * ms / (args.steps * reads_per_step * world)
+    step_bytes = sum(read_bytes(T, p) for T, p in SWEEP)
+
+    # --- per-T times (graph of 96 reads of one T, rotated sets) ---
+    per_t = {}
+    for T in (1, 4, 8):
+        for p in (False, True):
+            a0 = synth.make_activations(500 + T, T, p)
+            R, Pd, M = to_dev(a0["R"]), to_dev(a0["P"]), to_dev(a0["Rmix"])
+            o = tuple(torch.empty((T, 4, 2560), dtype=dt, device=dev)
+                      for dt in (torch.float32, torch.int16, torch.int16))
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                for i in range(N_SETS):
+                    W = sets[i]
+                    hc.hc_read(T, R, Pd, W["w_norm"], W["W_down"], W["W_up"], M, *o,
+                               stream=stream)
+                stream.synchronize()
+                with torch.cuda.graph(gr, stream=stream):
+                    for i in range(N_SETS):
+                        W = sets[i]
+                        hc.hc_read(T, R, Pd, W["w_norm"], W["W_down"], W["W_up"], M, *o,
+                                   stream=stream)
+            ms_t = timed(lambda k: gr.replay(), 40, 3)
+            us = 1e3 * ms_t / (40 * N_SETS)
+            per_t[f"T{T}{'_P' if p else ''}"] = {
+                "us": us, "gbps": read_bytes(T, p) / (us * 1e-6) / 1e9}
+
+    # --- cold round: 96 reads of T=4 with P over the 48 sets ---
+    a4 = synth.make_activations(600, 4, True)
+    R4, P4, M4 = to_dev(a4["R"]), to_dev(a4["P"]), to_dev(a4["Rmix"])
+    o4 = [tuple(torch.empty((4, 4, 2560), dtype=dt, device=dev)
+                for dt in (torch.float32, torch.int16, torch.int16)) for _ in range(2)]
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        def round96():
+            for i in range(96):
+                W = sets[i % N_SETS]
+                hc.hc_read(4, R4, P4, W["w_norm"], W["W_down"], W["W_up"], M4, *o4[i % 2],
+                           stream=stream)
+        round96()
+        stream.synchronize()
+        with torch.cuda.graph(gr, stream=stream):
+            round96()
+    ms_r = timed(lambda k: gr.replay(), 20, 3)
+    cold_round = {"us_per_round": 1e3 * ms_r / 20, "us_per_read": 1e3 * ms_r / 20 / 96,
+                  "gbps": 96 * read_bytes(4, True) / (ms_r / 20 * 1e-3) / 1e9}
+
+    # --- e2e: pinned host inputs -> device, 16 reads via the public call, outputs back ---
+    pin_in, pin_out, dev_in = [], [], []
+    h2d = d2h = 0
+    for j, (T, p) in enumerate(SWEEP):
+        a = acts[j]["host"]
+        hin = {k: torch.from_numpy(a[k]).pin_memory() if a[k] is not None else None
+               for k in ("R", "P", "Rmix")}
+        din = {k: (torch.empty_like(v, device=dev) if v is not None else None)
+               for k, v in hin.items()}
+        hout = tuple(torch.empty((T, 4, 2560), dtype=dt).pin_memory()
+                     for dt in (torch.float32, torch.int16, torch.int16))
+        pin_in.append(hin)
+        dev_in.append(din)
+        pin_out.append(hout)
+        h2d += sum(v.numel() * v.element_size() for v in hin.values() if v is not None)
+        d2h += sum(v.numel() * v.element_size() for v in hout)
+
+    def e2e_step(k):
+        g = k % n_groups
+        with torch.cuda.stream(stream):
+            for j in range(len(SWEEP)):
+                i = g * len(SWEEP) + j
+                hin, din, hout = pin_in[j], dev_in[j], pin_out[j]
+                for key in ("R", "P", "Rmix"):
+                    if hin[key] is not None:
+                        din[key].copy_(hin[key], non_blocking=True)
+                W = sets[i]
+                hc.hc_read(SWEEP[j][0], din["R"], din["P"], W["w_norm"], W["W_down"],
+                           W["W_up"], din["Rmix"], *outs[i], stream=stream)
+                for o, ho in zip(outs[i], hout):
+                    ho.copy_(o, non_blocking=True)
+
+    e2e_steps = max(10, min(args.steps, 500))
+    ms_e = timed(e2e_step, e2e_steps, min(args.warmup, 5) + 3)
+    e2e_us = 1e3 * ms_e / (e2e_steps * reads_per_step * world)
+
+    # --- prefill chunks (one call per chunk) ---
+    prefill = {}
+    W0 = sets[0]
+    for T in (8192, 32768):
+        c = synth.make_prefill_chunk(104 if T == 32768 else 100, T)
+        R, M = to_dev(c["R"]), to_dev(c["Rmix"])
+        o = tuple(torch.empty((T, 4, 2560), dtype=dt, device=dev)
+                  for dt in (torch.float32, torch.int16, torch.int16))
+
+        def chunk(k):
+            hc.hc_read(T, R, None, W0["w_norm"], W0["W_down"], W0["W_up"], M, *o,
+                       stream=stream)
+        reps = 5 if T == 8192 else 3
+        ms_p = timed(chunk, reps, 2)
+        ms1 = ms_p / reps
+        prefill[f"T{T}"] = {"ms": ms1, "tokens_per_s": T / (ms1 * 1e-3),
+                            "gbps": prefill_read_bytes(T) / (ms1 * 1e-3) / 1e9}
+        del R, M, o
+
+    peaks = measured_peaks()
+    achieved = step_bytes / (ms / args.steps * 1e-3) / 1e9
+    traffic = NCU_TRAFFIC_PER_READ
+    kernel_launches_per_step = sum(2 * ((T + 7) // 8) for T, _ in SWEEP)
+
+    line = {
+        "metric": METRIC, "value": us_per_read, "unit": "us/read", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(),
+        "roofline": {"bound": "hbm", "kernel": "decode read (down_slice + up_mix kernels)",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "peak_source": peaks["source"],
+                     "bytes_per_step": step_bytes},
+        "clocks": clocks,
+        "e2e": {"value": e2e_us, "unit": "us/read", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": kernel_launches_per_step * args.steps,
+        "decode_by_T": per_t,
+        "cold_round_96x_T4_P": cold_round,
+        "prefill": prefill,
+    }
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            d = run_oracle_sample(args.cpu_seconds, 1)
+            n = len(d["sweep_seconds"]) * d["reads_per_sweep"]
+            line["cpu_baseline"] = {
+                "value": 1e6 * sum(d["sweep_seconds"]) / n, "unit": "us/read", "cores": 1,
+                "kind": "oracle", "cpu": cpu_model(),
+                "sample": f"{n} reads ({len(d['sweep_seconds'])} sweeps of T=1..8 x "
+                          "{no P, P}, one weight set), float64 numpy, 1 thread"}
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        # each reference step is a whole 16-read oracle sweep (about a second)
+        args.steps = max(1, min(args.steps, 20))
+        args.warmup = max(1, min(args.warmup, 3))
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,19 @@
+"""GB300 hyper-connection residual read: a C-ABI CUDA library and its Python binding.
+
+``synth`` (seeded inputs) imports without the library. The read itself
+(``hc_read`` and friends) loads ``libhcread.so`` on first use and raises if it is
+missing: there is no fallback implementation.
+"""
+from . import synth  # noqa: F401
+
+_BINDING = ("hc_read_init", "hc_read", "hc_read_path", "hc_read_check", "hc_read_status",
+            "hc_read_shutdown", "hc_read_version", "strerror", "HcReadError", "load",
+            "HC_PATH_AUTO", "HC_PATH_DECODE", "HC_PATH_PREFILL", "HC_PATH_PREFILL_UNFUSED",
+            "EXPORTS", "LIB_PATH")
+
+
+def __getattr__(name):
+    if name in _BINDING:
+        from . import _lib
+        return getattr(_lib, name)
+    raise AttributeError(name)

@@ -1,0 +1,46 @@
+// Device helpers shared by the kernels of the library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace hc {
+
+// 16-byte streaming load that skips L1 (each weight byte is read once per call).
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Low and high bf16 of a packed pair, widened exactly to fp32.
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+// The two 16-bit images of an fp32 value, round to nearest even.
+__device__ __forceinline__ uint16_t to_bf16_bits(float x) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+__device__ __forceinline__ uint16_t to_fp16_bits(float x) {
+    return __half_as_ushort(__float2half_rn(x));
+}
+
+// The gate: logistic sigmoid of the up projection times the residual value.
+__device__ __forceinline__ float gate_value(float u, float rp) {
+    return rp * (1.0f / (1.0f + expf(-u)));
+}
+
+// Row s of the token's 4x4 mix applied to the 4 gated values (q = 0..3 in order).
+__device__ __forceinline__ float mix_row(const float* m_row, float g0, float g1, float g2,
+                                         float g3) {
+    float v = m_row[0] * g0;
+    v = fmaf(m_row[1], g1, v);
+    v = fmaf(m_row[2], g2, v);
+    v = fmaf(m_row[3], g3, v);
+    return v;
+}
+
+}  // namespace hc

@@ -1,0 +1,159 @@
+/*
+ * hc_read.h - C ABI of the GB300 hyper-connection residual read.
+ *
+ * One call reads T tokens. Per token it takes 4 residual streams of width 2560
+ * and computes, in this order:
+ *
+ *   1. R' = R + P                   (optional pending write, one fp32 add)
+ *   2. per-stream RMS norm of R', times w_norm
+ *   3. lo = W_down . xn             (10240 -> 320, bf16 weights, fp32 sums)
+ *   4. gated = sigmoid(W_up . lo) * R'   (320 -> 10240, the gate)
+ *   5. mixed[s] = sum_q Rmix[s][q] * gated[q]   (per-token 4x4 mix), written as
+ *      fp32 together with its bf16 and fp16 images.
+ *
+ * Sources (pages by title and section):
+ *   "#315 hc: the multi-token hyper-connection read split finer" - "What changes"
+ *       (norm per token and stream; down projection), "Exactness" (reads with and
+ *       without the pending write; the once-per-card bitwise check).
+ *   "#1370 prefill: opt-in STRATA_HC_UPMIX=1 on CUDA - the hyper-connection up
+ *       projection with gr_mix_r as its epilogue (sm_80+)" - "Why" (the up GEMM
+ *       writes gated, gr_mix_r reads it back with R), "What it does" (the fused
+ *       up projection + mix writing mixed with its BF16 / FP16 images).
+ *   "#2488 sycl/A770: faster hyper-connection read on Arc A-series" - "Summary"
+ *       changes 1 (last slice reduces the slice partials in a fixed order) and 4
+ *       (norm folded into the down projection).
+ *   "#2226 STRATA_HC_PERSIST=1 (opt-in, HIP): the verifier's hyper-connection read
+ *       as one persistent kernel" - "Summary" (the read at 1-8 tokens).
+ *
+ * Shapes are fixed: n = 4 streams, C = 2560, N = n*C = 10240, r = 320.
+ *
+ * Layouts (all row-major, contiguous, caller-owned DEVICE memory on the device
+ * given to hc_read_init, 16-byte aligned):
+ *   R, P      float    [T][4][2560]   residual and pending write (P may be NULL)
+ *   w_norm    uint16_t [4][2560]      bf16 bits
+ *   W_down    uint16_t [320][10240]   bf16 bits, [out][in], in index k = s*2560 + c
+ *   W_up      uint16_t [10240][320]   bf16 bits, [out][in], out index i = s*2560 + c
+ *   Rmix      float    [T][4][4]      row s mixes the 4 gated streams into stream s
+ *   out_f32   float    [T][4][2560]   mixed
+ *   out_bf16  uint16_t [T][4][2560]   bf16 bits, round-to-nearest-even of out_f32
+ *   out_fp16  uint16_t [T][4][2560]   IEEE half bits, round-to-nearest-even of out_f32
+ *
+ * Ownership: the caller owns every tensor; they must stay valid until the work
+ * enqueued on `stream` has completed. Outputs must not overlap each other or any
+ * input. R and P are only read (R is not updated with P). The library owns its
+ * scratch (slice partials, counters, lo, a device status word), allocated by
+ * hc_read_init for up to max_tokens tokens.
+ *
+ * Ordering: the weights (w_norm, W_down, W_up) are layer parameters. The library
+ * may start reading them before the kernel that precedes the call on `stream`
+ * has finished (programmatic dependent launch), so they must not be produced by
+ * that preceding kernel. R, P and Rmix are read only after it has finished.
+ * Calls that share one device context must be issued on one stream at a time
+ * (they share scratch).
+ *
+ * Errors: every function returns HC_OK (0) or a negative code. Argument errors
+ * are detected on the host before anything is enqueued. Kernel-side faults that
+ * the kernels can detect themselves (a bounded wait that ran out) set a device
+ * status word, reported by hc_read_status(). hc_read never synchronises and
+ * never falls back to another implementation.
+ */
+#ifndef HC_READ_H
+#define HC_READ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HC_READ_STREAMS 4
+#define HC_READ_WIDTH 2560
+#define HC_READ_RANK 320
+
+enum hc_status {
+    HC_OK = 0,
+    HC_ERR_ARG = -1,       /* null pointer, bad size, misalignment, overlap, host pointer */
+    HC_ERR_NOT_INIT = -2,  /* hc_read_init was not called for the current device */
+    HC_ERR_ARCH = -3,      /* the device is not compute capability 10.3 */
+    HC_ERR_CUDA = -4,      /* a CUDA runtime call or a launch failed */
+    HC_ERR_TIMEOUT = -5,   /* a bounded device-side wait gave up (status word) */
+    HC_ERR_CHECK = -6,     /* hc_read_check found a mismatch */
+    HC_ERR_NOMEM = -7      /* scratch allocation failed */
+};
+
+/* Which kernels run. HC_PATH_AUTO picks the decode kernels for small T and the
+ * tensor-core tile path above that; the others force one path (tests, bench). */
+enum hc_path {
+    HC_PATH_AUTO = 0,
+    HC_PATH_DECODE = 1,          /* sliced down + up/gate/mix kernels (any T) */
+    HC_PATH_PREFILL = 2,         /* tile down, fused up + gate + mix epilogue */
+    HC_PATH_PREFILL_UNFUSED = 3  /* tile down, up GEMM writing gated, then the mix */
+};
+
+/* Creates the context of `device` (makes it current), checks that it is sm_103,
+ * and allocates scratch for up to `max_tokens` tokens per call. eps <= 0 selects
+ * 1e-6. Calling it again on the same device re-sizes the context. Returns
+ * HC_ERR_ARG for max_tokens < 1, HC_ERR_ARCH, HC_ERR_NOMEM or HC_ERR_CUDA. */
+int hc_read_init(int device, int max_tokens, float eps);
+
+/* The read of `tokens` tokens (0 <= tokens <= max_tokens; 0 enqueues nothing),
+ * asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ * Output is bitwise deterministic for a given path and T. */
+int hc_read(int tokens,
+            const float* R, const float* P,
+            const uint16_t* w_norm, const uint16_t* W_down, const uint16_t* W_up,
+            const float* Rmix,
+            float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
+            void* stream);
+
+/* hc_read with an explicit path (enum hc_path). Same arguments and errors. The
+ * unfused prefill path keeps gated [T][10240] fp32 in library scratch, which it
+ * allocates on its first use (the only call that may allocate after init). */
+int hc_read_path(int path, int tokens,
+                 const float* R, const float* P,
+                 const uint16_t* w_norm, const uint16_t* W_down, const uint16_t* W_up,
+                 const float* Rmix,
+                 float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
+                 void* stream);
+
+/* Result of the once-per-device self check. */
+typedef struct hc_check_report {
+    int device;
+    int sm_count;
+    int tokens_checked;          /* 1..tokens_checked, each with and without P */
+    int repeat_bitwise;          /* 1 if two runs of every case gave the same bits */
+    int pending_write_bitwise;   /* 1 if read(R, P) == read(R + P, NULL) bit for bit */
+    int images_bitwise;          /* 1 if the bf16/fp16 outputs are the RNE images of out_f32 */
+    int paths_agree;             /* 1 if decode and prefill agree within max_rel_tol */
+    double max_rel_diff;         /* max |decode - prefill| / max |decode| over all cases */
+    double max_rel_tol;          /* the tolerance used for paths_agree */
+    char device_name[64];
+} hc_check_report;
+
+/* Runs both paths on device-generated pseudo-random inputs (seeded) for
+ * 1..max_tokens tokens (at most 8), with and without a pending write, and checks
+ * run-to-run bitwise repeat, the pending-write identity, the image rounding and
+ * the agreement of the two paths. Synchronises the device. Allocates and frees
+ * its own buffers. Returns HC_OK or HC_ERR_CHECK (report filled either way if
+ * rep is not NULL). */
+int hc_read_check(int max_tokens, uint64_t seed, hc_check_report* rep);
+
+/* Waits for `stream`, then reads and clears the device status word of the current
+ * device's context: HC_OK, or HC_ERR_TIMEOUT if a bounded wait gave up since the
+ * last call. HC_ERR_CUDA if the stream itself reports an error. */
+int hc_read_status(void* stream);
+
+/* Static description of a status code. */
+const char* hc_read_strerror(int code);
+
+/* Frees the scratch of every device context. */
+void hc_read_shutdown(void);
+
+/* ABI version (major * 100 + minor). */
+int hc_read_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HC_READ_H */

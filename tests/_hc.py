@@ -1,0 +1,76 @@
+"""Helpers shared by the GPU tests: device copies of seeded inputs, one read
+through the C ABI, and the comparisons with the oracle's outputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import hyper_connection_residual_read_gb300 as hc
+from hyper_connection_residual_read_gb300 import synth
+
+# spec tolerance for fp32 `mixed`: max |gpu - oracle| / max |oracle|
+TOL_F32 = 2e-6
+EPS = float(np.float32(1e-6))   # the fp32 eps the library uses by default
+MAX_TOKENS = 32768
+
+
+def dev_u16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def dev_f32(a: np.ndarray | None) -> torch.Tensor | None:
+    if a is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def dev_weights(w: dict) -> dict:
+    return {k: dev_u16(v) for k, v in w.items()}
+
+
+def alloc_out(T: int) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    shape = (T, synth.N_STREAMS, synth.WIDTH)
+    return (torch.empty(shape, dtype=torch.float32, device="cuda"),
+            torch.empty(shape, dtype=torch.int16, device="cuda"),
+            torch.empty(shape, dtype=torch.int16, device="cuda"))
+
+
+def gpu_read(T, R, P, W, Rmix, path=None, out=None):
+    """One read through the C ABI; returns host copies (f32, bf16 bits, fp16 bits)."""
+    o = out if out is not None else alloc_out(T)
+    if path is None:
+        hc.hc_read(T, R, P, W["w_norm"], W["W_down"], W["W_up"], Rmix, *o)
+    else:
+        hc.hc_read_path(path, T, R, P, W["w_norm"], W["W_down"], W["W_up"], Rmix, *o)
+    torch.cuda.synchronize()
+    return (o[0].cpu().numpy(), o[1].cpu().numpy().view(np.uint16),
+            o[2].cpu().numpy().view(np.uint16))
+
+
+def ordered16(bits: np.ndarray) -> np.ndarray:
+    """Sign-magnitude 16-bit patterns -> integers in value order (+0 == -0)."""
+    b = bits.astype(np.int32)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def rel_diff(got: np.ndarray, want: np.ndarray) -> float:
+    d = np.max(np.abs(got.astype(np.float64) - want.astype(np.float64)))
+    m = np.max(np.abs(want.astype(np.float64)))
+    return float(d / m) if m > 0 else float(d)
+
+
+def assert_matches_oracle(got, want, tol=TOL_F32):
+    """fp32 within the relative tolerance; images within 1 ulp of the oracle's
+    images; and the GPU's own images are exactly the RNE images of its fp32."""
+    from oracle import hc_oracle as O
+    f32, b16, h16 = got
+    wf, wb, wh = want
+    assert np.all(np.isfinite(f32))
+    r = rel_diff(f32, wf)
+    assert r <= tol, f"max|diff|/max|value| = {r:.3g} > {tol}"
+    assert np.max(np.abs(ordered16(b16) - ordered16(wb))) <= 1
+    assert np.max(np.abs(ordered16(h16) - ordered16(wh))) <= 1
+    assert np.array_equal(b16, O.f32_to_bf16_bits(f32))
+    assert np.array_equal(h16, O.f32_to_f16_bits(f32))
+    return r

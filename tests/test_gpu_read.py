@@ -1,0 +1,209 @@
+"""GPU parity of the hyper-connection read against the CPU oracle, through the C ABI.
+
+Cases follow the workloads of the decode verify window and prefill chunks:
+one token without a pending write (seed 0), the verify-window sweep T = 1..8 with
+and without the pending write (seeds 1..16, one per case), ragged token counts
+that cross the 8-token launch chunks, a cold round of 48 weight sets, and long
+prefill chunks checked on sampled tokens. Plus determinism, the pending-write
+identity, argument errors and output guard bytes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import hyper_connection_residual_read_gb300 as hc
+from hyper_connection_residual_read_gb300 import synth
+from oracle import hc_oracle as O
+
+from _hc import (EPS, MAX_TOKENS, TOL_F32, alloc_out, assert_matches_oracle, dev_f32,
+                 dev_weights, gpu_read)
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [None, hc.HC_PATH_DECODE]
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    hc.hc_read_init(0, MAX_TOKENS, EPS)
+    yield
+    torch.cuda.synchronize()
+
+
+@pytest.fixture(scope="module")
+def weights(ctx):
+    w = synth.make_weights(0)
+    return w, dev_weights(w)
+
+
+def run_case(weights, T, with_P, seed, path=None):
+    w, W = weights
+    a = synth.make_activations(seed, T, with_P)
+    got = gpu_read(T, dev_f32(a["R"]), dev_f32(a["P"]), W, dev_f32(a["Rmix"]), path)
+    want = O.hc_read(a["R"], a["P"], w["w_norm"], w["W_down"], w["W_up"], a["Rmix"], EPS)
+    return got, want
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_single_token_no_pending_write(weights, path):
+    got, want = run_case(weights, 1, False, 0, path)
+    assert_matches_oracle(got, want)
+
+
+@pytest.mark.parametrize("T", range(1, 9))
+@pytest.mark.parametrize("with_P", [False, True])
+def test_verify_window_sweep(weights, T, with_P):
+    seed = 1 + 2 * (T - 1) + int(with_P)          # seeds 1..16, one per case
+    got, want = run_case(weights, T, with_P, seed)
+    assert_matches_oracle(got, want)
+
+
+@pytest.mark.parametrize("T", [9, 13, 16, 17, 31])
+def test_ragged_token_counts(weights, T):
+    got, want = run_case(weights, T, True, 100 + T, hc.HC_PATH_DECODE)
+    assert_matches_oracle(got, want)
+
+
+def test_bitwise_repeatable(weights):
+    w, W = weights
+    a = synth.make_activations(7, 8, True)
+    R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+    first = gpu_read(8, R, P, W, M)
+    for _ in range(5):
+        again = gpu_read(8, R, P, W, M)
+        for x, y in zip(first, again):
+            assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_pending_write_equals_preadded(weights):
+    w, W = weights
+    a = synth.make_activations(8, 5, True)
+    pre = (a["R"] + a["P"]).astype(np.float32)
+    x = gpu_read(5, dev_f32(a["R"]), dev_f32(a["P"]), W, dev_f32(a["Rmix"]))
+    y = gpu_read(5, dev_f32(pre), None, W, dev_f32(a["Rmix"]))
+    for p, q in zip(x, y):
+        assert np.array_equal(p.view(np.uint8), q.view(np.uint8))
+
+
+def test_token_batch_invariance_decode(weights):
+    """Token t's bits do not depend on the other tokens of the call."""
+    w, W = weights
+    a = synth.make_activations(9, 8, True)
+    R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+    full = gpu_read(8, R, P, W, M, hc.HC_PATH_DECODE)
+    for t in (0, 5, 7):
+        one = gpu_read(1, R[t:t + 1].contiguous(), P[t:t + 1].contiguous(), W,
+                       M[t:t + 1].contiguous(), hc.HC_PATH_DECODE)
+        assert np.array_equal(one[0][0].view(np.uint32), full[0][t].view(np.uint32))
+
+
+def test_zero_tokens_is_a_no_op(weights):
+    w, W = weights
+    o = alloc_out(1)
+    o[0].fill_(3.0)
+    a = synth.make_activations(1, 1, False)
+    hc.hc_read(0, dev_f32(a["R"]), None, W["w_norm"], W["W_down"], W["W_up"],
+               dev_f32(a["Rmix"]), *o)
+    torch.cuda.synchronize()
+    assert bool((o[0] == 3.0).all())
+
+
+def test_output_guard_bytes_untouched(weights):
+    w, W = weights
+    T, G = 3, 4096
+    a = synth.make_activations(10, T, True)
+    n = T * 4 * 2560
+    big = torch.full((n + 2 * G,), 7.0, dtype=torch.float32, device="cuda")
+    b16 = torch.full((n + 2 * G,), 0x1234, dtype=torch.int16, device="cuda")
+    h16 = torch.full((n + 2 * G,), 0x4321, dtype=torch.int16, device="cuda")
+    hc.hc_read(T, dev_f32(a["R"]), dev_f32(a["P"]), W["w_norm"], W["W_down"], W["W_up"],
+               dev_f32(a["Rmix"]), big[G:G + n], b16[G:G + n], h16[G:G + n])
+    torch.cuda.synchronize()
+    for buf, v in ((big, 7.0), (b16, 0x1234), (h16, 0x4321)):
+        assert bool((buf[:G] == v).all()) and bool((buf[G + n:] == v).all())
+
+
+def test_argument_errors_are_refused(weights):
+    w, W = weights
+    a = synth.make_activations(1, 2, True)
+    R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+    o = alloc_out(2)
+    args = dict(R=R, P=P, w_norm=W["w_norm"], W_down=W["W_down"], W_up=W["W_up"], Rmix=M,
+                out_f32=o[0], out_bf16=o[1], out_fp16=o[2])
+
+    def call(T=2, **kw):
+        d = dict(args)
+        d.update(kw)
+        hc.hc_read(T, d["R"], d["P"], d["w_norm"], d["W_down"], d["W_up"], d["Rmix"],
+                   d["out_f32"], d["out_bf16"], d["out_fp16"])
+
+    bad = [
+        dict(R=0),                                   # null
+        dict(W_up=0),
+        dict(out_fp16=0),
+        dict(R=R.data_ptr() + 4),                    # misaligned
+        dict(out_bf16=o[0]),                         # outputs overlap
+        dict(out_f32=R),                             # output overlaps an input
+        dict(R=torch.zeros(2, 4, 2560).data_ptr()),  # host memory
+    ]
+    for kw in bad:
+        with pytest.raises(hc.HcReadError) as e:
+            call(**kw)
+        assert e.value.code == -1, kw
+    with pytest.raises(hc.HcReadError):
+        call(T=-1)
+    with pytest.raises(hc.HcReadError):
+        call(T=MAX_TOKENS + 1)
+    with pytest.raises(hc.HcReadError):
+        hc.hc_read_path(17, 2, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o)
+    assert hc.hc_read_status() == 0
+
+
+def test_cold_round_sampled(ctx):
+    """48 weight sets (larger than L2) rotated over 96 reads of 4 tokens with a
+    pending write; reads 0, 47 and 95 are checked against the oracle."""
+    T = 4
+    sets = [synth.make_weights(1000 + k) for k in range(48)]
+    Wdev = [dev_weights(s) for s in sets]
+    acts = [synth.make_activations(2000 + i, T, True) for i in range(96)]
+    outs = [alloc_out(T) for _ in range(96)]
+    for i in range(96):
+        a, W = acts[i], Wdev[i % 48]
+        hc.hc_read(T, dev_f32(a["R"]), dev_f32(a["P"]), W["w_norm"], W["W_down"], W["W_up"],
+                   dev_f32(a["Rmix"]), *outs[i])
+    torch.cuda.synchronize()
+    for i in (0, 47, 95):
+        w, a = sets[i % 48], acts[i]
+        got = (outs[i][0].cpu().numpy(), outs[i][1].cpu().numpy().view(np.uint16),
+               outs[i][2].cpu().numpy().view(np.uint16))
+        want = O.hc_read(a["R"], a["P"], w["w_norm"], w["W_down"], w["W_up"], a["Rmix"], EPS)
+        assert_matches_oracle(got, want)
+
+
+@pytest.mark.parametrize("T,seed", [(8192, 100), (32768, 104)])
+def test_prefill_chunk_sampled_tokens(weights, T, seed):
+    """A long chunk in one call; the first and last 128 tokens and 256 random ones
+    are checked against the oracle, plus NaN/Inf-free output everywhere."""
+    w, W = weights
+    a = synth.make_prefill_chunk(seed, T)
+    R, M = dev_f32(a["R"]), dev_f32(a["Rmix"])
+    o = alloc_out(T)
+    hc.hc_read(T, R, None, W["w_norm"], W["W_down"], W["W_up"], M, *o)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(o[0]).all())
+    rng = np.random.default_rng(seed)
+    idx = np.unique(np.concatenate([np.arange(128), np.arange(T - 128, T),
+                                    rng.choice(T, 256, replace=False)]))
+    want = O.hc_read_tokens(idx, a["R"], None, w["w_norm"], w["W_down"], w["W_up"],
+                            a["Rmix"], EPS)
+    ti = torch.from_numpy(idx).cuda()
+    got = (o[0][ti].cpu().numpy(), o[1][ti].cpu().numpy().view(np.uint16),
+           o[2][ti].cpu().numpy().view(np.uint16))
+    assert_matches_oracle(got, want)
+
+
+def test_self_check_passes(ctx):
+    code, rep = hc.hc_read_check(8, 1234)
+    assert code == 0, rep
+    assert rep["repeat_bitwise"] and rep["pending_write_bitwise"] and rep["images_bitwise"]
+    assert rep["sm_count"] > 0
