@@ -438,6 +438,28 @@ def gpu_arm(args) -> None:
         dist.destroy_process_group()
 
 
+def profile_decode(args) -> None:
+    """A small fixed decode workload for ncu: 48 rotated weight sets (larger than
+    L2), ``--steps`` reads of T=4 tokens with a pending write. No timing."""
+    import torch
+    import hyper_connection_residual_read_gb300 as hc
+    from hyper_connection_residual_read_gb300 import synth
+    hc.hc_read_init(0, 64, EPS)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(  # noqa: E731
+        x.view(np.int16) if x.dtype == np.uint16 else x)).cuda()
+    sets = [{k: dev(v) for k, v in synth.make_weights(7000 + k).items()} for k in range(N_SETS)]
+    a = synth.make_activations(600, 4, True)
+    R, P, M = dev(a["R"]), dev(a["P"]), dev(a["Rmix"])
+    o = [torch.empty((4, 4, 2560), dtype=dt, device="cuda")
+         for dt in (torch.float32, torch.int16, torch.int16)]
+    for i in range(args.steps):
+        W = sets[i % N_SETS]
+        hc.hc_read(4, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o)
+    torch.cuda.synchronize()
+    rc = hc.hc_read_status()
+    print(json.dumps({"profile": "decode", "reads": args.steps, "status": rc}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -446,8 +468,12 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["decode"], default=None,
+                    help="run a small fixed workload for an ncu capture instead of timing")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.profile == "decode":
+        profile_decode(args)
+    elif args.impl == "reference":
         # each reference step is a whole 16-read oracle sweep (about a second)
         args.steps = max(1, min(args.steps, 20))
         args.warmup = max(1, min(args.warmup, 3))
