@@ -35,9 +35,6 @@ Ctx* current_ctx(int* err) {
 
 void free_ctx(Ctx& c) {
     if (c.device >= 0) cudaSetDevice(c.device);
-    cudaFree(c.s.partials);
-    cudaFree(c.s.ssq);
-    cudaFree(c.s.counters);
     cudaFree(c.s.lo);
     cudaFree(c.s.status);
     cudaFree(c.gated);
@@ -224,9 +221,6 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     c.sm_count = prop.multiProcessorCount;
     strncpy(c.name, prop.name, sizeof(c.name) - 1);
     bool ok = true;
-    ok &= cudaMalloc(&c.s.partials, sizeof(float) * kDownSlices * kDecodeMaxT * kRank) == cudaSuccess;
-    ok &= cudaMalloc(&c.s.ssq, sizeof(float) * kDownRowBlocks * kDownSlices * kDecodeMaxT) == cudaSuccess;
-    ok &= cudaMalloc(&c.s.counters, sizeof(unsigned) * kDownRowBlocks) == cudaSuccess;
     ok &= cudaMalloc(&c.s.lo, sizeof(float) * (size_t)max_tokens * kRank) == cudaSuccess;
     ok &= cudaMalloc(&c.s.status, sizeof(int)) == cudaSuccess;
     if (!ok) {
@@ -234,8 +228,7 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
         free_ctx(c);
         return HC_ERR_NOMEM;
     }
-    if (cudaMemset(c.s.counters, 0, sizeof(unsigned) * kDownRowBlocks) != cudaSuccess ||
-        cudaMemset(c.s.status, 0, sizeof(int)) != cudaSuccess ||
+    if (cudaMemset(c.s.status, 0, sizeof(int)) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         free_ctx(c);
         return HC_ERR_CUDA;

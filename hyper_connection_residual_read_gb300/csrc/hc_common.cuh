@@ -16,6 +16,16 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
     return v;
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialisation may start while the previous kernel on the stream is still
+// running; `pdl_wait` blocks until that kernel has completed and its writes are
+// visible, and `pdl_launch_dependents` lets the next kernel start early. Only
+// layer parameters (weights) may be read before `pdl_wait`.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Low and high bf16 of a packed pair, widened exactly to fp32.
 __device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }

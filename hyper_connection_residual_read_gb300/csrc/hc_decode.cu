@@ -1,26 +1,30 @@
 // Decode path of the hyper-connection read: 1-8 tokens per launch, bound by the
 // 13 MB of bf16 weights every read streams.
 //
-// Two kernels per chunk of up to 8 tokens:
+// Two kernels per chunk of up to 8 tokens, chained by programmatic dependent
+// launch so that each kernel's weight stream starts while the previous kernel on
+// the stream is still running:
 //
-//  down_slice_kernel  - the down projection split into K slices (half a stream,
-//      1280 columns) x row blocks (16 of the 320 rows). The norm is folded in
+//  down_slice_kernel - the down projection split into 8 K slices (half a stream,
+//      1280 columns) x 20 row blocks (16 of the 320 rows). The norm is folded in
 //      ("#2488 sycl/A770: faster hyper-connection read on Arc A-series",
 //      Summary, change 4): a slice stages R' * w_norm unscaled together with its
 //      per-token sum of squares, and the reduce applies each stream's rs to that
-//      stream's partial dots. The last slice of a row block to finish sums the
-//      slice partials in a fixed order (same page, change 1), so the result is
-//      bitwise repeatable and there is no separate reduce launch.
+//      stream's partial dots. The 8 slices of a row block form one thread-block
+//      cluster and reduce through distributed shared memory in a fixed order
+//      (the page's change 1 does it with the last slice to finish; a cluster
+//      needs no global counter), so the result is bitwise repeatable.
 //
-//  up_mix_kernel - one warp per output column c: 8 lanes per up row
-//      i = s*2560 + c (one row per stream), lane sums over 40 of the 320 inputs,
-//      an xor tree in the 8-lane group, then the gate and the 4x4 mix in
-//      registers ("#1370 prefill: opt-in STRATA_HC_UPMIX=1 on CUDA ...", "What
-//      it does": the mix runs in registers and writes mixed with its BF16 / FP16
-//      images).
+//  up_mix_kernel - a warp owns 4 output columns; 8 lanes per column each sum 40
+//      of the 320 inputs for all 4 up rows i = s*2560 + c of that column, an xor
+//      tree finishes the dots, then the gate and the 4x4 mix run in registers
+//      ("#1370 prefill: opt-in STRATA_HC_UPMIX=1 on CUDA ...", "What it does":
+//      the mix in registers, writing mixed with its BF16 / FP16 images).
 //
-// Weights are loaded straight into registers with 16-byte streaming loads that
-// are issued before anything else, so the whole matrix is in flight at once.
+// Weights are loaded straight into registers with 16-byte streaming loads issued
+// before anything else, so a kernel's whole weight matrix is in flight at once.
+#include <cooperative_groups.h>
+
 #include "hc_common.cuh"
 #include "hc_internal.h"
 
@@ -30,8 +34,8 @@ namespace {
 
 constexpr int kDownThreads = 320;   // 10 warps: 2 row groups x 5 column groups
 constexpr int kDownColGroups = 5;   // 5 x 256 columns = 1280
-constexpr int kUpColsPerCta = 8;    // one warp per column
-constexpr int kUpThreads = 32 * kUpColsPerCta;
+constexpr int kUpWarps = 4;         // 4 columns per warp, 16 per CTA
+constexpr int kUpThreads = 32 * kUpWarps;
 
 // Sum over the 32 lanes of eight per-lane values, one per row. On return the
 // lanes whose bits (4,3,2) equal the row's index hold that row's full sum:
@@ -61,59 +65,76 @@ __device__ __forceinline__ float warp_reduce_8rows(const float (&v)[8], int lane
 }
 
 template <int T>
-__global__ void __launch_bounds__(kDownThreads)
+__global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kDownThreads)
 down_slice_kernel(const float* __restrict__ R, const float* __restrict__ P,
                   const uint16_t* __restrict__ w_norm, const uint16_t* __restrict__ W_down,
-                  float* __restrict__ partials, float* __restrict__ ssq,
-                  unsigned* __restrict__ counters, float* __restrict__ lo, float eps) {
-    const int sl = blockIdx.x;                 // K slice 0..7
-    const int rb = blockIdx.y;                 // row block 0..19
+                  float* __restrict__ lo, float eps) {
+    namespace cg = cooperative_groups;
+    const int sl = blockIdx.x;                 // K slice 0..7 == rank in the cluster
+    const int rb = blockIdx.y;                 // row block 0..19 == the cluster
     const int s = sl >> 1;                     // stream of the slice
     const int c0 = (sl & 1) * kDownSliceCols;  // first column of the slice in the stream
     const int k0 = s * kWidth + c0;            // first column on the 10240 axis
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int rg = warp / kDownColGroups, cg = warp % kDownColGroups;
+    const int rg = warp / kDownColGroups, cgp = warp % kDownColGroups;
     const int j0 = rb * kDownRowsPerCta + rg * 8;
-    const int col = cg * 256 + lane * 8;       // this lane's 8 columns within the slice
+    const int col = cgp * 256 + lane * 8;      // this lane's 8 columns within the slice
 
-    // 1. weights first: 8 rows x 8 columns, one 16-byte load per row
+    // 1. weights first (layer parameters may be read before the previous kernel
+    //    on the stream has finished): 8 rows x 8 columns, one 16-byte load per row
     uint4 wv[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r)
         wv[r] = ldg_stream_v4(W_down + (size_t)(j0 + r) * kCols + k0 + col);
+    const uint2 wn = *reinterpret_cast<const uint2*>(w_norm + k0 + 4 * tid);
+    pdl_launch_dependents();
+    pdl_wait();
 
-    // 2. activations a = R' * w_norm (fp32) and per-token sums of squares of R'
+    // 2. activations a = R' * w_norm (fp32) and per-token sums of squares of R'.
+    //    Smem layout: a lane's 8 columns are stored as two float4 runs, 128 floats
+    //    apart, so that consecutive lanes read consecutive 16-byte words.
     __shared__ float4 a_s[T][kDownSliceCols / 4];
     __shared__ float red_ss[kDownThreads / 32][T];
     __shared__ float red[T][kDownColGroups][kDownRowsPerCta];
-    __shared__ int s_last;
+    __shared__ float part_s[T][kDownRowsPerCta];   // this slice's partial dots
+    __shared__ float ss_s[T];                      // this slice's sums of squares
 
-    const uint2 wn = *reinterpret_cast<const uint2*>(w_norm + k0 + 4 * tid);
-    const float w0 = bf16_lo(wn.x), w1 = bf16_hi(wn.x), w2 = bf16_lo(wn.y), w3 = bf16_hi(wn.y);
+    float4 xs[T];
 #pragma unroll
-    for (int t = 0; t < T; ++t) {
-        const size_t off = (size_t)t * kCols + k0 + 4 * tid;
-        float4 x = *reinterpret_cast<const float4*>(R + off);
-        if (P != nullptr) {
-            const float4 p = *reinterpret_cast<const float4*>(P + off);
-            x.x += p.x; x.y += p.y; x.z += p.z; x.w += p.w;
+    for (int t = 0; t < T; ++t)
+        xs[t] = *reinterpret_cast<const float4*>(R + (size_t)t * kCols + k0 + 4 * tid);
+    if (P != nullptr) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+            const float4 p = *reinterpret_cast<const float4*>(P + (size_t)t * kCols + k0 + 4 * tid);
+            xs[t].x += p.x; xs[t].y += p.y; xs[t].z += p.z; xs[t].w += p.w;
         }
-        float ss = x.x * x.x;
-        ss = fmaf(x.y, x.y, ss);
-        ss = fmaf(x.z, x.z, ss);
-        ss = fmaf(x.w, x.w, ss);
-        a_s[t][tid] = make_float4(x.x * w0, x.y * w1, x.z * w2, x.w * w3);
+    }
+    const float w0 = bf16_lo(wn.x), w1 = bf16_hi(wn.x), w2 = bf16_lo(wn.y), w3 = bf16_hi(wn.y);
+    {
+        const int c = 4 * tid;                       // first of this thread's 4 columns
+        const int scg = c >> 8, slane = (c & 255) >> 3, half = (c & 7) >> 2;
+        const int slot = scg * 64 + half * 32 + slane;   // float4 index
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) red_ss[warp][t] = ss;
+        for (int t = 0; t < T; ++t) {
+            const float4 x = xs[t];
+            float ss = x.x * x.x;
+            ss = fmaf(x.y, x.y, ss);
+            ss = fmaf(x.z, x.z, ss);
+            ss = fmaf(x.w, x.w, ss);
+            a_s[t][slot] = make_float4(x.x * w0, x.y * w1, x.z * w2, x.w * w3);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            if (lane == 0) red_ss[warp][t] = ss;
+        }
     }
     __syncthreads();
     if (tid < T) {
         float ss = 0.f;
 #pragma unroll
         for (int w = 0; w < kDownThreads / 32; ++w) ss += red_ss[w][tid];
-        ssq[(rb * kDownSlices + sl) * kDecodeMaxT + tid] = ss;
+        ss_s[tid] = ss;
     }
 
     // 3. partial dots of 8 rows over this lane's 8 columns, reduced over the warp
@@ -127,8 +148,8 @@ down_slice_kernel(const float* __restrict__ R, const float* __restrict__ P,
     }
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-        const float4 x0 = a_s[t][col / 4];
-        const float4 x1 = a_s[t][col / 4 + 1];
+        const float4 x0 = a_s[t][cgp * 64 + lane];
+        const float4 x1 = a_s[t][cgp * 64 + 32 + lane];
         float acc[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
@@ -143,7 +164,7 @@ down_slice_kernel(const float* __restrict__ R, const float* __restrict__ P,
             acc[r] = v;
         }
         const float sum = warp_reduce_8rows(acc, lane);
-        if ((lane & 3) == 0) red[t][cg][rg * 8 + ((lane >> 2) & 7)] = sum;
+        if ((lane & 3) == 0) red[t][cgp][rg * 8 + ((lane >> 2) & 7)] = sum;
     }
     __syncthreads();
 
@@ -153,34 +174,36 @@ down_slice_kernel(const float* __restrict__ R, const float* __restrict__ P,
         float v = red[t][0][j];
 #pragma unroll
         for (int g = 1; g < kDownColGroups; ++g) v += red[t][g][j];
-        partials[(sl * kDecodeMaxT + t) * kRank + rb * kDownRowsPerCta + j] = v;
+        part_s[t][j] = v;
     }
 
-    // 5. the last slice of this row block to arrive reduces (no waiting)
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = (atomicAdd(&counters[rb], 1u) == (unsigned)(kDownSlices - 1));
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (tid < T * kDownRowsPerCta) {
-        const int t = tid / kDownRowsPerCta, j = tid % kDownRowsPerCta;
-        const int row = rb * kDownRowsPerCta + j;
+    // 5. reduce over the 8 slices of the row block through distributed shared
+    //    memory: CTA `sl` finishes rows 2*sl and 2*sl+1 of the block, summing the
+    //    slices of each stream in order and applying that stream's rs.
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (tid < T * 2) {
+        const int t = tid >> 1, j = 2 * sl + (tid & 1);
         float v = 0.f;
 #pragma unroll
         for (int st = 0; st < kStreams; ++st) {
-            const int sa = 2 * st, sb = 2 * st + 1;
-            const float ss = __ldcg(&ssq[(rb * kDownSlices + sa) * kDecodeMaxT + t]) +
-                             __ldcg(&ssq[(rb * kDownSlices + sb) * kDecodeMaxT + t]);
+            const float* ssa = cluster.map_shared_rank(&ss_s[0], 2 * st);
+            const float* ssb = cluster.map_shared_rank(&ss_s[0], 2 * st + 1);
+            const float* pa = cluster.map_shared_rank(&part_s[0][0], 2 * st);
+            const float* pb = cluster.map_shared_rank(&part_s[0][0], 2 * st + 1);
+            const float ss = ssa[t] + ssb[t];
             const float rs = 1.0f / sqrtf(ss / (float)kWidth + eps);
-            const float d = __ldcg(&partials[(sa * kDecodeMaxT + t) * kRank + row]) +
-                            __ldcg(&partials[(sb * kDecodeMaxT + t) * kRank + row]);
+            const float d = pa[t * kDownRowsPerCta + j] + pb[t * kDownRowsPerCta + j];
             v = fmaf(rs, d, v);
         }
-        lo[t * kRank + row] = v;
+        lo[t * kRank + rb * kDownRowsPerCta + j] = v;
     }
-    if (tid == 0) counters[rb] = 0u;
+    cluster.sync();   // keep this CTA's shared memory alive until every reader is done
 }
+
+// lo in shared memory: each token's 320 values as 8 parts of 40, padded to 44
+// floats so that the 8 parts a warp reads at once fall in distinct banks.
+constexpr int kLoPart = 44;
 
 template <int T>
 __global__ void __launch_bounds__(kUpThreads)
@@ -190,60 +213,105 @@ up_mix_kernel(const float* __restrict__ R, const float* __restrict__ P,
               uint16_t* __restrict__ out_bf16, uint16_t* __restrict__ out_fp16) {
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x * kUpColsPerCta + warp;   // output column 0..2559
-    const int s = lane >> 3;                             // stream of this lane's row
-    const int part = lane & 7;                           // which 40 of the 320 inputs
-    const int i = s * kWidth + c;                        // up row
+    const int cc = lane >> 3;                  // which of the warp's 4 columns
+    const int part = lane & 7;                 // which 40 of the 320 inputs
+    const int c = (blockIdx.x * kUpWarps + warp) * 4 + cc;   // output column 0..2559
+    const int sp = part & 3;                   // stream gated by this lane (lanes 0..3)
 
-    uint4 wv[5];
-    const uint16_t* wrow = W_up + (size_t)i * kRank + part * 40;
+    // 1. the 4 up rows of column c (one per stream), this lane's 40 inputs each
+    uint4 wv[kStreams][5];
 #pragma unroll
-    for (int q = 0; q < 5; ++q) wv[q] = ldg_stream_v4(wrow + 8 * q);
+    for (int st = 0; st < kStreams; ++st) {
+        const uint16_t* wrow = W_up + (size_t)(st * kWidth + c) * kRank + part * 40;
+#pragma unroll
+        for (int q = 0; q < 5; ++q) wv[st][q] = ldg_stream_v4(wrow + 8 * q);
+    }
+    pdl_launch_dependents();
+    pdl_wait();
 
-    __shared__ __align__(16) float lo_s[T][kRank];
-    for (int e = tid; e < T * kRank; e += kUpThreads) lo_s[e / kRank][e % kRank] = lo[e];
+    // 2. everything the token loop needs, requested at once: lo, R' and the mix
+    __shared__ __align__(16) float lo_s[T][8][kLoPart];
+    __shared__ __align__(16) float m_s[T][16];
+    float rp[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+        const size_t off = (size_t)t * kCols + sp * kWidth + c;
+        rp[t] = R[off];
+    }
+    if (P != nullptr) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) rp[t] += P[(size_t)t * kCols + sp * kWidth + c];
+    }
+    for (int e = tid; e < T * kRank / 4; e += kUpThreads) {
+        const int t = e / (kRank / 4), j = 4 * (e % (kRank / 4));
+        const float4 v = *reinterpret_cast<const float4*>(lo + (size_t)t * kRank + j);
+        *reinterpret_cast<float4*>(&lo_s[t][j / 40][j % 40]) = v;
+    }
+    if (tid < T * 4) reinterpret_cast<float4*>(&m_s[0][0])[tid] =
+        reinterpret_cast<const float4*>(Rmix)[tid];
     __syncthreads();
 
-    float wf[40];
 #pragma unroll
-    for (int q = 0; q < 5; ++q) {
-        wf[8 * q + 0] = bf16_lo(wv[q].x); wf[8 * q + 1] = bf16_hi(wv[q].x);
-        wf[8 * q + 2] = bf16_lo(wv[q].y); wf[8 * q + 3] = bf16_hi(wv[q].y);
-        wf[8 * q + 4] = bf16_lo(wv[q].z); wf[8 * q + 5] = bf16_hi(wv[q].z);
-        wf[8 * q + 6] = bf16_lo(wv[q].w); wf[8 * q + 7] = bf16_hi(wv[q].w);
-    }
-
-#pragma unroll 1
     for (int t = 0; t < T; ++t) {
-        const float4* l4 = reinterpret_cast<const float4*>(&lo_s[t][part * 40]);
-        float acc = 0.f;
+        const float4* l4 = reinterpret_cast<const float4*>(&lo_s[t][part][0]);
+        float acc[kStreams] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int q = 0; q < 10; ++q) {
-            const float4 x = l4[q];
-            acc = fmaf(wf[4 * q + 0], x.x, acc);
-            acc = fmaf(wf[4 * q + 1], x.y, acc);
-            acc = fmaf(wf[4 * q + 2], x.z, acc);
-            acc = fmaf(wf[4 * q + 3], x.w, acc);
+        for (int q = 0; q < 5; ++q) {
+            const float4 xa = l4[2 * q], xb = l4[2 * q + 1];
+#pragma unroll
+            for (int st = 0; st < kStreams; ++st) {
+                const uint4 w = wv[st][q];
+                float v = acc[st];
+                v = fmaf(bf16_lo(w.x), xa.x, v);
+                v = fmaf(bf16_hi(w.x), xa.y, v);
+                v = fmaf(bf16_lo(w.y), xa.z, v);
+                v = fmaf(bf16_hi(w.y), xa.w, v);
+                v = fmaf(bf16_lo(w.z), xb.x, v);
+                v = fmaf(bf16_hi(w.z), xb.y, v);
+                v = fmaf(bf16_lo(w.w), xb.z, v);
+                v = fmaf(bf16_hi(w.w), xb.w, v);
+                acc[st] = v;
+            }
         }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-
-        const size_t off = (size_t)t * kCols + i;
-        float rp = R[off];
-        if (P != nullptr) rp += P[off];
-        const float g = gate_value(acc, rp);
-        const float g0 = __shfl_sync(0xffffffffu, g, 0);
-        const float g1 = __shfl_sync(0xffffffffu, g, 8);
-        const float g2 = __shfl_sync(0xffffffffu, g, 16);
-        const float g3 = __shfl_sync(0xffffffffu, g, 24);
-        if (part == 0) {
-            const float m = mix_row(Rmix + (size_t)t * 16 + s * 4, g0, g1, g2, g3);
+#pragma unroll
+        for (int st = 0; st < kStreams; ++st) {
+            acc[st] += __shfl_xor_sync(0xffffffffu, acc[st], 4);
+            acc[st] += __shfl_xor_sync(0xffffffffu, acc[st], 2);
+            acc[st] += __shfl_xor_sync(0xffffffffu, acc[st], 1);
+        }
+        // lane `part` (0..3) of the column group gates stream `part`
+        const float u = sp == 0 ? acc[0] : sp == 1 ? acc[1] : sp == 2 ? acc[2] : acc[3];
+        const float g = gate_value(u, rp[t]);
+        const int base = lane & ~7;
+        const float g0 = __shfl_sync(0xffffffffu, g, base + 0);
+        const float g1 = __shfl_sync(0xffffffffu, g, base + 1);
+        const float g2 = __shfl_sync(0xffffffffu, g, base + 2);
+        const float g3 = __shfl_sync(0xffffffffu, g, base + 3);
+        if (part < 4) {
+            const float m = mix_row(&m_s[t][part * 4], g0, g1, g2, g3);
+            const size_t off = (size_t)t * kCols + part * kWidth + c;
             out_f32[off] = m;
             out_bf16[off] = to_bf16_bits(m);
             out_fp16[off] = to_fp16_bits(m);
         }
     }
+}
+
+// Launch with programmatic stream serialisation (see pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 template <int T>
@@ -252,12 +320,12 @@ cudaError_t launch_chunk(const Ctx& ctx, const ReadArgs& a, int t0, cudaStream_t
     const float* R = a.R + off;
     const float* P = a.P ? a.P + off : nullptr;
     float* lo = ctx.s.lo + (size_t)t0 * kRank;
-    down_slice_kernel<T><<<dim3(kDownSlices, kDownRowBlocks), kDownThreads, 0, st>>>(
-        R, P, a.w_norm, a.W_down, ctx.s.partials, ctx.s.ssq, ctx.s.counters, lo, ctx.eps);
-    up_mix_kernel<T><<<kWidth / kUpColsPerCta, kUpThreads, 0, st>>>(
-        R, P, a.W_up, lo, a.Rmix + (size_t)t0 * 16, a.out_f32 + off, a.out_bf16 + off,
-        a.out_fp16 + off);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(down_slice_kernel<T>, dim3(kDownSlices, kDownRowBlocks),
+                               dim3(kDownThreads), st, R, P, a.w_norm, a.W_down, lo, ctx.eps);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(up_mix_kernel<T>, dim3(kWidth / (4 * kUpWarps)), dim3(kUpThreads), st,
+                      R, P, a.W_up, (const float*)lo, a.Rmix + (size_t)t0 * 16,
+                      a.out_f32 + off, a.out_bf16 + off, a.out_fp16 + off);
 }
 
 }  // namespace

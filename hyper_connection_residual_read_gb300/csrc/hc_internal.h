@@ -27,10 +27,7 @@ constexpr int kAutoDecodeMaxT = 8;
 constexpr int kStatusTimeout = 1;
 
 struct Scratch {
-    float* partials = nullptr;       // [kDownSlices][kDecodeMaxT][kRank]
-    float* ssq = nullptr;            // [kDownRowBlocks][kDownSlices][kDecodeMaxT]
-    unsigned* counters = nullptr;    // [kDownRowBlocks], self-resetting
-    float* lo = nullptr;             // [max_tokens][kRank]
+    float* lo = nullptr;             // [max_tokens][kRank], the down projection's output
     int* status = nullptr;           // device status word
 };
 
