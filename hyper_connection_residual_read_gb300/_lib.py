@@ -32,7 +32,7 @@ STREAMS, WIDTH, RANK = 4, 2560, 320
 
 # every symbol include/hc_read.h declares
 EXPORTS = ("hc_read_init", "hc_read", "hc_read_path", "hc_read_check", "hc_read_status",
-           "hc_read_strerror", "hc_read_shutdown", "hc_read_version")
+           "hc_read_strerror", "hc_read_shutdown", "hc_read_version", "hc_read_noalloc")
 
 
 class HcReadError(RuntimeError):
@@ -90,6 +90,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_read_shutdown.restype = None
     lib.hc_read_version.argtypes = []
     lib.hc_read_version.restype = i32
+    lib.hc_read_noalloc.argtypes = [i32] + [vp] * 9 + [ctypes.c_float, vp]
+    lib.hc_read_noalloc.restype = i32
     _lib = lib
     return lib
 
@@ -144,6 +146,15 @@ def hc_read_path(path, tokens, R, P, w_norm, W_down, W_up, Rmix, out_f32, out_bf
     _check("hc_read_path", load().hc_read_path(
         path, tokens, _ptr(R), _ptr(P), _ptr(w_norm), _ptr(W_down), _ptr(W_up), _ptr(Rmix),
         _ptr(out_f32), _ptr(out_bf16), _ptr(out_fp16), _stream(stream)))
+
+
+def hc_read_noalloc(tokens, R, P, w_norm, W_down, W_up, Rmix, out_f32, out_bf16, out_fp16,
+                    eps: float = 1e-6, stream=None) -> None:
+    """The decode read with no allocation by the library (at most 64 tokens; the
+    scratch is a fixed device array shared by every call on the device)."""
+    _check("hc_read_noalloc", load().hc_read_noalloc(
+        tokens, _ptr(R), _ptr(P), _ptr(w_norm), _ptr(W_down), _ptr(W_up), _ptr(Rmix),
+        _ptr(out_f32), _ptr(out_bf16), _ptr(out_fp16), eps, _stream(stream)))
 
 
 def hc_read_check(max_tokens: int = 8, seed: int = 0) -> tuple[int, dict]:

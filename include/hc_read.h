@@ -149,6 +149,31 @@ const char* hc_read_strerror(int code);
 /* Frees the scratch of every device context. */
 void hc_read_shutdown(void);
 
+/* The decode read for callers that cannot allocate device memory: plug-ins that
+ * run inside a host engine which owns all device memory and hands out fixed
+ * workspaces, latency-critical loops where cudaMalloc/cudaFree could synchronise
+ * the device, and callers that never call hc_read_init (which allocates). The
+ * pages have no counterpart of this entry point.
+ *
+ * Same arguments and layouts as hc_read, plus eps (<= 0 selects 1e-6); no
+ * hc_read_init is needed. It runs the decode kernels for 0 <= tokens <= 64 and
+ * keeps their scratch (the down projection's output, 64 x 320 floats = 80 KB) in
+ * a fixed array in device memory that the CUDA runtime reserves on every device
+ * that loads the library, until the process exits. It calls no cudaMalloc,
+ * cudaFree or other allocating routine. Returns HC_ERR_ARG for tokens > 64 or the
+ * pointer errors hc_read refuses, HC_ERR_ARCH off sm_103, HC_ERR_CUDA otherwise.
+ *
+ * The first call on a device (with that device current) looks up the array's
+ * device address; make that first call before any stream capture. Every call
+ * on a device shares the one array: calls that may overlap on the GPU (on
+ * different streams without ordering between them) race and must not be made. */
+int hc_read_noalloc(int tokens,
+                    const float* R, const float* P,
+                    const uint16_t* w_norm, const uint16_t* W_down, const uint16_t* W_up,
+                    const float* Rmix,
+                    float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
+                    float eps, void* stream);
+
 /* ABI version (major * 100 + minor). */
 int hc_read_version(void);
 
