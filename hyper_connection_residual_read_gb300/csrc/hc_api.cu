@@ -37,6 +37,10 @@ void free_ctx(Ctx& c) {
     if (c.device >= 0) cudaSetDevice(c.device);
     cudaFree(c.s.lo);
     cudaFree(c.s.status);
+    cudaFree(c.wd16);
+    cudaFree(c.wu16);
+    cudaFree(c.partials);
+    cudaFree(c.lo16);
     cudaFree(c.gated);
     c = Ctx();
 }
@@ -99,14 +103,27 @@ int run(int path, const ReadArgs& a, cudaStream_t st) {
     if (path < HC_PATH_AUTO || path > HC_PATH_PREFILL_UNFUSED) return HC_ERR_ARG;
     if (int e = validate(*c, a)) return e;
     if (a.T == 0) return HC_OK;
+    if (path == HC_PATH_AUTO) path = a.T <= kAutoDecodeMaxT ? HC_PATH_DECODE : HC_PATH_PREFILL;
     cudaError_t ce;
     switch (path) {
-        case HC_PATH_AUTO:
         case HC_PATH_DECODE:
             ce = launch_decode(*c, a, st);
             break;
+        case HC_PATH_PREFILL:
+            ce = launch_prefill(*c, a, true, st);
+            break;
         default:
-            return HC_ERR_ARG;  // tile paths are not built in this library version
+            if (c->gated == nullptr) {
+                // the unfused pair keeps gated in scratch: allocated on first use
+                if (cudaMalloc(&c->gated, sizeof(float) * (size_t)c->max_tokens * kCols) !=
+                    cudaSuccess) {
+                    cudaGetLastError();
+                    c->gated = nullptr;
+                    return HC_ERR_NOMEM;
+                }
+            }
+            ce = launch_prefill(*c, a, false, st);
+            break;
     }
     return ce == cudaSuccess ? HC_OK : HC_ERR_CUDA;
 }
@@ -203,6 +220,7 @@ extern "C" const char* hc_read_strerror(int code) {
         case HC_ERR_TIMEOUT: return "a bounded device-side wait gave up";
         case HC_ERR_CHECK: return "self check found a mismatch";
         case HC_ERR_NOMEM: return "scratch allocation failed";
+        case HC_ERR_RANGE: return "a prefill activation did not fit fp16 (|R' * w_norm| or |lo| >= 65504)";
         default: return "unknown status";
     }
 }
@@ -223,12 +241,18 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     bool ok = true;
     ok &= cudaMalloc(&c.s.lo, sizeof(float) * (size_t)max_tokens * kRank) == cudaSuccess;
     ok &= cudaMalloc(&c.s.status, sizeof(int)) == cudaSuccess;
+    ok &= cudaMalloc(&c.wd16, sizeof(__half) * (size_t)kRank * kCols) == cudaSuccess;
+    ok &= cudaMalloc(&c.wu16, sizeof(__half) * (size_t)kCols * kRank) == cudaSuccess;
+    ok &= cudaMalloc(&c.partials, sizeof(float) * (size_t)max_tokens * kStreams * kRank) == cudaSuccess;
+    ok &= cudaMalloc(&c.lo16, sizeof(__half) * 2 * (size_t)max_tokens * kRank) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
         free_ctx(c);
         return HC_ERR_NOMEM;
     }
     if (cudaMemset(c.s.status, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(c.lo16, 0, sizeof(__half) * 2 * (size_t)max_tokens * kRank) != cudaSuccess ||
+        prefill_setup(c) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         free_ctx(c);
         return HC_ERR_CUDA;
@@ -261,7 +285,8 @@ extern "C" int hc_read_status(void* stream) {
     if (cudaMemcpy(&word, c->s.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
         cudaMemset(c->s.status, 0, sizeof(int)) != cudaSuccess)
         return HC_ERR_CUDA;
-    return (word & kStatusTimeout) ? HC_ERR_TIMEOUT : HC_OK;
+    if (word & kStatusTimeout) return HC_ERR_TIMEOUT;
+    return (word & kStatusRangeBit) ? HC_ERR_RANGE : HC_OK;
 }
 
 extern "C" int hc_read_check(int max_tokens, uint64_t seed, hc_check_report* rep) {

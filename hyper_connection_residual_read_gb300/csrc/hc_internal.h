@@ -1,6 +1,8 @@
 // Internal declarations shared by the translation units of the library.
 #pragma once
 
+#include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,6 +27,7 @@ constexpr int kAutoDecodeMaxT = 8;
 
 // Device status word bits.
 constexpr int kStatusTimeout = 1;
+constexpr int kStatusRangeBit = 2;   // a prefill activation did not fit fp16
 
 struct Scratch {
     float* lo = nullptr;             // [max_tokens][kRank], the down projection's output
@@ -39,7 +42,15 @@ struct Ctx {
     int sm_count = 0;
     char name[64] = {0};
     Scratch s;
-    float* gated = nullptr;          // [max_tokens][kCols], unfused prefill only
+    // prefill scratch
+    __half* wd16 = nullptr;          // W_down as fp16 [kRank][kCols]
+    __half* wu16 = nullptr;          // W_up as fp16 [kCols][kRank]
+    float* partials = nullptr;       // per-stream down partials [max_tokens][kStreams][kRank]
+    __half* lo16 = nullptr;          // lo as two fp16 terms [2][max_tokens][kRank]
+    float* gated = nullptr;          // [max_tokens][kCols], unfused prefill only (lazy)
+    CUtensorMap tm_wd;               // TMA maps over wd16, wu16, lo16
+    CUtensorMap tm_wu;
+    CUtensorMap tm_lo;
 };
 
 struct ReadArgs {
@@ -57,5 +68,9 @@ struct ReadArgs {
 
 // Decode kernels for any T: launched in chunks of kDecodeMaxT tokens.
 cudaError_t launch_decode(const Ctx& ctx, const ReadArgs& a, cudaStream_t st);
+
+// Prefill (tensor-core tile) path: TMA maps and kernel attributes, then the launch.
+cudaError_t prefill_setup(Ctx& ctx);
+cudaError_t launch_prefill(const Ctx& ctx, const ReadArgs& a, bool fused, cudaStream_t st);
 
 }  // namespace hc

@@ -1,0 +1,622 @@
+// Prefill path of the hyper-connection read: thousands of tokens per call, on the
+// tcgen05 tensor cores with accumulators in tensor memory and operands fed by TMA.
+//
+//   convert_weights  W_down and W_up, bf16 -> fp16 (exact for |w| >= 2^-17; below
+//                    that the fp16 grid of 2^-24 rounds them by at most 3e-8).
+//   down_tile        the down projection per (128-token tile, stream): A = R' * w_norm
+//                    split on the fly into two fp16 terms (hi + residual), B = the
+//                    stream's 2560 columns of W_down, D = 128 x 320 fp32 in TMEM.
+//                    The epilogue applies the stream's rs (its sum of squares is
+//                    accumulated while A is produced), the norm fold of
+//                    "#2488 sycl/A770: faster hyper-connection read on Arc A-series",
+//                    Summary, change 4, and writes one partial per stream.
+//   lo_split         lo = the 4 stream partials summed in a fixed order, stored as
+//                    two fp16 terms for the up projection's A operand.
+//   upmix_tile       the up projection per (128-token tile, 64 columns x 4 streams),
+//                    D = 128 x 256 fp32, double-buffered in TMEM; the epilogue applies
+//                    the gate and the 4x4 mix and writes mixed with its bf16 and fp16
+//                    images, so `gated` never reaches memory ("#1370 prefill: opt-in
+//                    STRATA_HC_UPMIX=1 on CUDA - the hyper-connection up projection with
+//                    gr_mix_r as its epilogue (sm_80+)", "Why" and "What it does").
+//                    The unfused variant stores `gated` instead, and mix_gated applies
+//                    the same mix afterwards (bitwise the same result).
+//
+// Two fp16 terms per activation reproduce fp32 accuracy: the residual term carries
+// the next 11 bits, and the weights are exact in fp16, so each product of the MMA
+// is exact and the sums are fp32 in TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include "hc_common.cuh"
+#include "hc_internal.h"
+#include "hc_tc.cuh"
+
+namespace hc {
+namespace {
+
+using namespace tc;
+
+constexpr int kTileM = 128;            // tokens per tile (TMEM lanes)
+constexpr int kBK = 64;                // K per pipeline stage: one 128-byte swizzle row
+constexpr int kTileBytes16 = kTileM * kBK * 2;    // 16 KB: one 128 x 64 fp16 operand tile
+
+// down_tile
+constexpr int kDownN = kRank;          // 320 accumulator columns (two MMAs of N = 160)
+constexpr int kDownStages = 3;
+constexpr int kDownBBytes = kDownN * kBK * 2;     // 40 KB
+constexpr int kDownStageBytes = 2 * kTileBytes16 + kDownBBytes;
+constexpr int kDownKBlocks = kWidth / kBK;        // 40 per stream
+constexpr int kDownThreads = 320;                  // TMA, MMA, 8 converter/epilogue warps
+constexpr int kDownSmem = kDownStages * kDownStageBytes + 1024;
+
+// upmix_tile
+constexpr int kUpCols = 64;            // output columns per tile (x 4 streams = N 256)
+constexpr int kUpN = kStreams * kUpCols;
+constexpr int kUpStages = 3;
+constexpr int kUpBBytes = kUpN * kBK * 2;         // 32 KB
+constexpr int kUpStageBytes = 2 * kTileBytes16 + kUpBBytes;
+constexpr int kUpKBlocks = kRank / kBK;           // 5
+constexpr int kUpColTiles = kWidth / kUpCols;     // 40
+constexpr int kUpThreads = 320;                    // TMA, MMA, 8 epilogue warps
+constexpr int kUpSmem = kUpStages * kUpStageBytes + 1024;
+
+constexpr int kStatusRange = kStatusRangeBit;
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// hi = fp16(x), lo = fp16(x - hi): two fp16 terms whose sum carries 22 bits of x.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// ---------------------------------------------------------------------------
+// weights bf16 -> fp16
+// ---------------------------------------------------------------------------
+__global__ void convert_weights_kernel(const uint16_t* __restrict__ wd, const uint16_t* __restrict__ wu,
+                                       __half* __restrict__ wd16, __half* __restrict__ wu16,
+                                       int n8_each) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n8_each;
+         i += gridDim.x * blockDim.x) {
+        const bool up = i >= n8_each;
+        const int j = up ? i - n8_each : i;
+        const uint4 v = *reinterpret_cast<const uint4*>((up ? wu : wd) + 8 * (size_t)j);
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const __half2 h = __floats2half2_rn(bf16_lo(in[q]), bf16_hi(in[q]));
+            out[q] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>((up ? wu16 : wd16) + 8 * (size_t)j) =
+            make_uint4(out[0], out[1], out[2], out[3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// down projection, one (128-token tile, stream) per tile, persistent CTAs
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kDownThreads, 1)
+down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
+                 const uint16_t* __restrict__ w_norm, const __grid_constant__ CUtensorMap tm_wd,
+                 float* __restrict__ partials, int T, float eps, int* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    __shared__ __align__(8) uint64_t full_bar[kDownStages], empty_bar[kDownStages];
+    __shared__ __align__(8) uint64_t acc_full, acc_empty, ss_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+    __shared__ float ss_s[2][kTileM];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles = ((T + kTileM - 1) / kTileM) * kStreams;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kDownStages; ++i) {
+            mbar_init(&full_bar[i], 256 + 1);
+            mbar_init(&empty_bar[i], 1);
+        }
+        mbar_init(&acc_full, 1);
+        mbar_init(&acc_empty, 256);
+        mbar_init(&ss_bar, 256);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    auto sA = [&](int slot, int term) { return smem + slot * kDownStageBytes + term * kTileBytes16; };
+    auto sB = [&](int slot) { return smem + slot * kDownStageBytes + 2 * kTileBytes16; };
+
+    if (warp == 0) {
+        // B producer: the stream's W_down columns, 320 rows as two boxes of 160
+        if (lane == 0) {
+            int it = 0;
+            for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
+                const int s = tile % kStreams;
+                for (int kb = 0; kb < kDownKBlocks; ++kb, ++it) {
+                    const int slot = it % kDownStages;
+                    const uint32_t ph = (it / kDownStages) & 1;
+                    if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
+                    mbar_arrive_expect_tx(&full_bar[slot], kDownBBytes);
+                    const int x = s * kWidth + kb * kBK;
+                    tma_load_2d(sB(slot), &tm_wd, x, 0, &full_bar[slot]);
+                    tma_load_2d(sB(slot) + kDownBBytes / 2, &tm_wd, x, kDownN / 2, &full_bar[slot]);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(kTileM, kDownN / 2);
+            int it = 0, lt = 0;
+            for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
+                if (!mbar_wait(&acc_empty, (lt & 1) ^ 1, &abort_flag, status)) break;
+                tc_fence_after();
+                bool ok = true;
+                for (int kb = 0; kb < kDownKBlocks; ++kb, ++it) {
+                    const int slot = it % kDownStages;
+                    const uint32_t ph = (it / kDownStages) & 1;
+                    if (!mbar_wait(&full_bar[slot], ph, &abort_flag, status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t b0 = smem_u32(sB(slot));
+#pragma unroll
+                    for (int term = 0; term < 2; ++term) {
+                        const uint32_t a0 = smem_u32(sA(slot, term));
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)
+                                mma_f16(tmem + h * (kDownN / 2), desc_sw128(a0 + kk * 32),
+                                        desc_sw128(b0 + h * (kDownBBytes / 2) + kk * 32), idesc,
+                                        (kb | term | kk) != 0);
+                        }
+                    }
+                    mma_commit(&empty_bar[slot]);
+                }
+                if (!ok) break;
+                mma_commit(&acc_full);
+            }
+        }
+    } else {
+        // 8 converter warps: produce A for their (row quarter, K half); then epilogue
+        const int q = warp & 3, half = (warp - 2) >> 2;
+        const int m = q * 32 + lane;
+        int it = 0, lt = 0;
+        for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
+            const int tt = tile / kStreams, s = tile % kStreams;
+            const int t = tt * kTileM + m;
+            const bool valid = t < T;
+            float ss = 0.f, amax = 0.f;
+            for (int kb = 0; kb < kDownKBlocks; ++kb, ++it) {
+                const int slot = it % kDownStages;
+                const uint32_t ph = (it / kDownStages) & 1;
+                const int k = s * kWidth + kb * kBK + half * 32;
+                float x[32];
+                if (valid) {
+                    const float4* r4 = reinterpret_cast<const float4*>(R + (size_t)t * kCols + k);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 v = r4[i];
+                        x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+                    }
+                    if (P != nullptr) {
+                        const float4* p4 = reinterpret_cast<const float4*>(P + (size_t)t * kCols + k);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 v = p4[i];
+                            x[4 * i] += v.x; x[4 * i + 1] += v.y; x[4 * i + 2] += v.z; x[4 * i + 3] += v.w;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] = 0.f;
+                }
+                uint4 wv[4];
+                const uint4* w4 = reinterpret_cast<const uint4*>(w_norm + k);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) wv[i] = w4[i];
+                if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
+                uint8_t* ahi = sA(slot, 0);
+                uint8_t* alo = sA(slot, 1);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {          // 4 chunks of 8 elements
+                    const uint32_t wq[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float r0 = x[8 * j + 2 * e], r1 = x[8 * j + 2 * e + 1];
+                        ss = fmaf(r0, r0, ss);
+                        ss = fmaf(r1, r1, ss);
+                        const float a0 = r0 * bf16_lo(wq[e]), a1 = r1 * bf16_hi(wq[e]);
+                        amax = fmaxf(amax, fmaxf(fabsf(a0), fabsf(a1)));
+                        split2(a0, a1, hi[e], lo[e]);
+                    }
+                    const uint32_t off = sw128_offset(m, half * 32 + 8 * j);
+                    *reinterpret_cast<uint4*>(ahi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(alo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&full_bar[slot]);
+            }
+            if (abort_flag) break;
+            if (amax >= 65504.f) atomicOr(status, kStatusRange);
+            // both K halves of a row must have their sums of squares in place
+            ss_s[half][m] = ss;
+            mbar_arrive(&ss_bar);
+            if (!mbar_wait(&ss_bar, lt & 1, &abort_flag, status)) break;
+            // epilogue: scale this stream's partial dots by its rs and store them
+            if (!mbar_wait(&acc_full, lt & 1, &abort_flag, status)) break;
+            tc_fence_after();
+            const float rs = 1.0f / sqrtf((ss_s[0][m] + ss_s[1][m]) / (float)kWidth + eps);
+            float* dst = partials + ((size_t)t * kStreams + s) * kRank + half * (kDownN / 2);
+#pragma unroll 1
+            for (int c0 = 0; c0 < kDownN / 2; c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + half * (kDownN / 2) + c0, v);
+                if (valid) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        *reinterpret_cast<float4*>(dst + c0 + 4 * i) =
+                            make_float4(v[4 * i] * rs, v[4 * i + 1] * rs, v[4 * i + 2] * rs,
+                                        v[4 * i + 3] * rs);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// lo = sum of the 4 stream partials (in stream order), split into two fp16 terms
+// ---------------------------------------------------------------------------
+__global__ void lo_split_kernel(const float* __restrict__ partials, __half* __restrict__ lo16,
+                                int T, int max_tokens, int* __restrict__ status) {
+    const int n4 = T * (kRank / 4);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += gridDim.x * blockDim.x) {
+        const int t = i / (kRank / 4), j = 4 * (i % (kRank / 4));
+        const float* p = partials + (size_t)t * kStreams * kRank + j;
+        float4 v = *reinterpret_cast<const float4*>(p);
+#pragma unroll
+        for (int s = 1; s < kStreams; ++s) {
+            const float4 w = *reinterpret_cast<const float4*>(p + s * kRank);
+            v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+        }
+        if (fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) >= 65504.f)
+            atomicOr(status, kStatusRange);
+        uint32_t h0, l0, h1, l1;
+        split2(v.x, v.y, h0, l0);
+        split2(v.z, v.w, h1, l1);
+        *reinterpret_cast<uint2*>(lo16 + (size_t)t * kRank + j) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2*>(lo16 + ((size_t)max_tokens + t) * kRank + j) = make_uint2(l0, l1);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// up projection + gate (+ mix), one (128-token tile, 64 columns x 4 streams) per
+// tile, persistent CTAs, two TMEM accumulators so the epilogue of one tile runs
+// under the MMAs of the next.
+// ---------------------------------------------------------------------------
+template <bool kFused>
+__global__ void __launch_bounds__(kUpThreads, 1)
+upmix_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
+                  const float* __restrict__ Rmix, const __grid_constant__ CUtensorMap tm_lo,
+                  const __grid_constant__ CUtensorMap tm_wu, float* __restrict__ out_f32,
+                  uint16_t* __restrict__ out_bf16, uint16_t* __restrict__ out_fp16,
+                  float* __restrict__ gated, int T, int* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    __shared__ __align__(8) uint64_t full_bar[kUpStages], empty_bar[kUpStages];
+    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles = ((T + kTileM - 1) / kTileM) * kUpColTiles;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kUpStages; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 256);
+        }
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_slot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    auto sA = [&](int slot, int term) { return smem + slot * kUpStageBytes + term * kTileBytes16; };
+    auto sB = [&](int slot) { return smem + slot * kUpStageBytes + 2 * kTileBytes16; };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int it = 0;
+            for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
+                const int tt = tile / kUpColTiles, ct = tile % kUpColTiles;
+                for (int kb = 0; kb < kUpKBlocks; ++kb, ++it) {
+                    const int slot = it % kUpStages;
+                    const uint32_t ph = (it / kUpStages) & 1;
+                    if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
+                    mbar_arrive_expect_tx(&full_bar[slot], kUpStageBytes);
+                    tma_load_3d(sA(slot, 0), &tm_lo, kb * kBK, tt * kTileM, 0, &full_bar[slot]);
+                    tma_load_3d(sA(slot, 1), &tm_lo, kb * kBK, tt * kTileM, 1, &full_bar[slot]);
+#pragma unroll
+                    for (int s = 0; s < kStreams; ++s)
+                        tma_load_2d(sB(slot) + s * (kUpBBytes / kStreams), &tm_wu, kb * kBK,
+                                    s * kWidth + ct * kUpCols, &full_bar[slot]);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(kTileM, kUpN);
+            int it = 0, lt = 0;
+            for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
+                const int b = lt & 1;
+                if (!mbar_wait(&acc_empty[b], ((lt >> 1) & 1) ^ 1, &abort_flag, status)) break;
+                tc_fence_after();
+                bool ok = true;
+                for (int kb = 0; kb < kUpKBlocks; ++kb, ++it) {
+                    const int slot = it % kUpStages;
+                    const uint32_t ph = (it / kUpStages) & 1;
+                    if (!mbar_wait(&full_bar[slot], ph, &abort_flag, status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t b0 = smem_u32(sB(slot));
+#pragma unroll
+                    for (int term = 0; term < 2; ++term) {
+                        const uint32_t a0 = smem_u32(sA(slot, term));
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_f16(tmem + b * kUpN, desc_sw128(a0 + kk * 32),
+                                    desc_sw128(b0 + kk * 32), idesc, (kb | term | kk) != 0);
+                    }
+                    mma_commit(&empty_bar[slot]);
+                }
+                if (!ok) break;
+                mma_commit(&acc_full[b]);
+            }
+        }
+    } else {
+        // epilogue: lane quarter q of TMEM = tokens q*32..q*32+31 of the tile; the
+        // two warps of a quarter take 32 of the 64 columns each
+        const int q = warp & 3, half = (warp - 2) >> 2;
+        const int m = q * kTileM / 4 + lane;
+        int lt = 0;
+        for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
+            const int tt = tile / kUpColTiles, ct = tile % kUpColTiles;
+            const int b = lt & 1;
+            const int t = tt * kTileM + m;
+            const bool valid = t < T;
+            float mx[16];
+            if (kFused && valid) {
+                const float4* m4 = reinterpret_cast<const float4*>(Rmix + (size_t)t * 16);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 v = m4[i];
+                    mx[4 * i] = v.x; mx[4 * i + 1] = v.y; mx[4 * i + 2] = v.z; mx[4 * i + 3] = v.w;
+                }
+            }
+            if (!mbar_wait(&acc_full[b], (lt >> 1) & 1, &abort_flag, status)) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+                const int cl = half * 32 + cc * 16;            // first of 16 columns in the tile
+                const int c = ct * kUpCols + cl;
+                float g[kStreams][16];
+#pragma unroll
+                for (int s = 0; s < kStreams; ++s)
+                    tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + b * kUpN + s * kUpCols + cl,
+                              g[s]);
+                if (!valid) continue;
+#pragma unroll
+                for (int s = 0; s < kStreams; ++s) {
+                    const size_t off = (size_t)t * kCols + s * kWidth + c;
+                    const float4* r4 = reinterpret_cast<const float4*>(R + off);
+                    float rp[16];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 v = r4[i];
+                        rp[4 * i] = v.x; rp[4 * i + 1] = v.y; rp[4 * i + 2] = v.z; rp[4 * i + 3] = v.w;
+                    }
+                    if (P != nullptr) {
+                        const float4* p4 = reinterpret_cast<const float4*>(P + off);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 v = p4[i];
+                            rp[4 * i] += v.x; rp[4 * i + 1] += v.y; rp[4 * i + 2] += v.z; rp[4 * i + 3] += v.w;
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) g[s][e] = gate_value(g[s][e], rp[e]);
+                    if (!kFused) {
+                        float4* d4 = reinterpret_cast<float4*>(gated + off);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            d4[i] = make_float4(g[s][4 * i], g[s][4 * i + 1], g[s][4 * i + 2], g[s][4 * i + 3]);
+                    }
+                }
+                if (kFused) {
+#pragma unroll
+                    for (int so = 0; so < kStreams; ++so) {
+                        float o[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            o[e] = mix_row(&mx[so * 4], g[0][e], g[1][e], g[2][e], g[3][e]);
+                        const size_t off = (size_t)t * kCols + so * kWidth + c;
+                        float4* f4 = reinterpret_cast<float4*>(out_f32 + off);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            f4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                        uint32_t bb[8], hh[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            bb[i] = (uint32_t)to_bf16_bits(o[2 * i]) | ((uint32_t)to_bf16_bits(o[2 * i + 1]) << 16);
+                            hh[i] = (uint32_t)to_fp16_bits(o[2 * i]) | ((uint32_t)to_fp16_bits(o[2 * i + 1]) << 16);
+                        }
+                        uint4* b4 = reinterpret_cast<uint4*>(out_bf16 + off);
+                        uint4* h4 = reinterpret_cast<uint4*>(out_fp16 + off);
+                        b4[0] = make_uint4(bb[0], bb[1], bb[2], bb[3]);
+                        b4[1] = make_uint4(bb[4], bb[5], bb[6], bb[7]);
+                        h4[0] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                        h4[1] = make_uint4(hh[4], hh[5], hh[6], hh[7]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[b]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// The mix of the unfused pair: reads gated back and applies the same 4x4 mix.
+__global__ void mix_gated_kernel(const float* __restrict__ gated, const float* __restrict__ Rmix,
+                                 float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16,
+                                 uint16_t* __restrict__ out_fp16, int T) {
+    const int per_tok = kWidth / 4;
+    const int n = T * per_tok;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int t = i / per_tok, c = 4 * (i % per_tok);
+        float mx[16];
+        const float4* m4 = reinterpret_cast<const float4*>(Rmix + (size_t)t * 16);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 v = m4[k];
+            mx[4 * k] = v.x; mx[4 * k + 1] = v.y; mx[4 * k + 2] = v.z; mx[4 * k + 3] = v.w;
+        }
+        float g[kStreams][4];
+#pragma unroll
+        for (int s = 0; s < kStreams; ++s) {
+            const float4 v = *reinterpret_cast<const float4*>(gated + (size_t)t * kCols + s * kWidth + c);
+            g[s][0] = v.x; g[s][1] = v.y; g[s][2] = v.z; g[s][3] = v.w;
+        }
+#pragma unroll
+        for (int so = 0; so < kStreams; ++so) {
+            float o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = mix_row(&mx[so * 4], g[0][e], g[1][e], g[2][e], g[3][e]);
+            const size_t off = (size_t)t * kCols + so * kWidth + c;
+            *reinterpret_cast<float4*>(out_f32 + off) = make_float4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint2*>(out_bf16 + off) =
+                make_uint2((uint32_t)to_bf16_bits(o[0]) | ((uint32_t)to_bf16_bits(o[1]) << 16),
+                           (uint32_t)to_bf16_bits(o[2]) | ((uint32_t)to_bf16_bits(o[3]) << 16));
+            *reinterpret_cast<uint2*>(out_fp16 + off) =
+                make_uint2((uint32_t)to_fp16_bits(o[0]) | ((uint32_t)to_fp16_bits(o[1]) << 16),
+                           (uint32_t)to_fp16_bits(o[2]) | ((uint32_t)to_fp16_bits(o[3]) << 16));
+        }
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool encode_fp16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                 const cuuint64_t* strides, const cuuint32_t* box) {
+    auto enc = get_encoder();
+    if (enc == nullptr) return false;
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, const_cast<void*>(base), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t prefill_setup(Ctx& c) {
+    // tensor maps over the library's own scratch: fixed for the context's lifetime
+    {
+        const cuuint64_t dims[2] = {kCols, kRank};
+        const cuuint64_t strides[1] = {kCols * 2};
+        const cuuint32_t box[2] = {kBK, kDownN / 2};
+        if (!encode_fp16(&c.tm_wd, c.wd16, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {kRank, kCols};
+        const cuuint64_t strides[1] = {kRank * 2};
+        const cuuint32_t box[2] = {kBK, kUpCols};
+        if (!encode_fp16(&c.tm_wu, c.wu16, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {kRank, (cuuint64_t)c.max_tokens, 2};
+        const cuuint64_t strides[2] = {kRank * 2, (cuuint64_t)c.max_tokens * kRank * 2};
+        const cuuint32_t box[3] = {kBK, kTileM, 1};
+        if (!encode_fp16(&c.tm_lo, c.lo16, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(down_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kDownSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(upmix_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kUpSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(upmix_tile_kernel<false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kUpSmem);
+}
+
+cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, bool fused, cudaStream_t st) {
+    const int n8 = kRank * kCols / 8;
+    convert_weights_kernel<<<2 * c.sm_count, 512, 0, st>>>(a.W_down, a.W_up, c.wd16, c.wu16, n8);
+    const int n_tt = (a.T + kTileM - 1) / kTileM;
+    const int down_grid = n_tt * kStreams < c.sm_count ? n_tt * kStreams : c.sm_count;
+    down_tile_kernel<<<down_grid, kDownThreads, kDownSmem, st>>>(a.R, a.P, a.w_norm, c.tm_wd,
+                                                                 c.partials, a.T, c.eps, c.s.status);
+    const int n4 = a.T * (kRank / 4);
+    const int rgrid = (n4 + 255) / 256 < 8 * c.sm_count ? (n4 + 255) / 256 : 8 * c.sm_count;
+    lo_split_kernel<<<rgrid, 256, 0, st>>>(c.partials, c.lo16, a.T, c.max_tokens, c.s.status);
+    const int up_tiles = n_tt * kUpColTiles;
+    const int up_grid = up_tiles < c.sm_count ? up_tiles : c.sm_count;
+    if (fused) {
+        upmix_tile_kernel<true><<<up_grid, kUpThreads, kUpSmem, st>>>(
+            a.R, a.P, a.Rmix, c.tm_lo, c.tm_wu, a.out_f32, a.out_bf16, a.out_fp16, nullptr, a.T,
+            c.s.status);
+    } else {
+        upmix_tile_kernel<false><<<up_grid, kUpThreads, kUpSmem, st>>>(
+            a.R, a.P, a.Rmix, c.tm_lo, c.tm_wu, nullptr, nullptr, nullptr, c.gated, a.T,
+            c.s.status);
+        const int n = a.T * (kWidth / 4);
+        const int mgrid = (n + 255) / 256 < 8 * c.sm_count ? (n + 255) / 256 : 8 * c.sm_count;
+        mix_gated_kernel<<<mgrid, 256, 0, st>>>(c.gated, a.Rmix, a.out_f32, a.out_bf16, a.out_fp16,
+                                                a.T);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace hc

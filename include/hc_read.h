@@ -78,7 +78,8 @@ enum hc_status {
     HC_ERR_CUDA = -4,      /* a CUDA runtime call or a launch failed */
     HC_ERR_TIMEOUT = -5,   /* a bounded device-side wait gave up (status word) */
     HC_ERR_CHECK = -6,     /* hc_read_check found a mismatch */
-    HC_ERR_NOMEM = -7      /* scratch allocation failed */
+    HC_ERR_NOMEM = -7,     /* scratch allocation failed */
+    HC_ERR_RANGE = -8      /* a tile-path activation did not fit fp16 (status word) */
 };
 
 /* Which kernels run. HC_PATH_AUTO picks the decode kernels for small T and the
@@ -139,8 +140,11 @@ typedef struct hc_check_report {
 int hc_read_check(int max_tokens, uint64_t seed, hc_check_report* rep);
 
 /* Waits for `stream`, then reads and clears the device status word of the current
- * device's context: HC_OK, or HC_ERR_TIMEOUT if a bounded wait gave up since the
- * last call. HC_ERR_CUDA if the stream itself reports an error. */
+ * device's context: HC_OK; HC_ERR_TIMEOUT if a bounded wait gave up since the last
+ * call; HC_ERR_RANGE if the tile path met an activation it cannot represent (its
+ * tensor-core operands carry R' * w_norm and lo as two fp16 terms, so they need
+ * |R' * w_norm| < 65504 and |lo| < 65504). HC_ERR_CUDA if the stream itself
+ * reports an error. */
 int hc_read_status(void* stream);
 
 /* Static description of a status code. */

@@ -200,6 +200,15 @@ def test_prefill_chunk_sampled_tokens(weights, T, seed):
     got = (o[0][ti].cpu().numpy(), o[1][ti].cpu().numpy().view(np.uint16),
            o[2][ti].cpu().numpy().view(np.uint16))
     assert_matches_oracle(got, want)
+    if T == 8192:
+        # the unfused pair (up GEMM writing gated, then the mix) gives the same bits
+        o2 = alloc_out(T)
+        hc.hc_read_path(hc.HC_PATH_PREFILL_UNFUSED, T, R, None, W["w_norm"], W["W_down"],
+                        W["W_up"], M, *o2)
+        torch.cuda.synchronize()
+        for x, y in zip(o, o2):
+            assert bool(torch.equal(x, y))
+    assert hc.hc_read_status() == 0
 
 
 def test_self_check_passes(ctx):
@@ -207,3 +216,53 @@ def test_self_check_passes(ctx):
     assert code == 0, rep
     assert rep["repeat_bitwise"] and rep["pending_write_bitwise"] and rep["images_bitwise"]
     assert rep["sm_count"] > 0
+
+
+# ---------------------------------------------------------------------------
+# the tensor-core tile path
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,with_P", [(1, False), (8, True), (9, True), (127, False),
+                                      (128, True), (129, False), (300, True)])
+def test_prefill_path_against_oracle(weights, T, with_P):
+    got, want = run_case(weights, T, with_P, 200 + T, hc.HC_PATH_PREFILL)
+    assert_matches_oracle(got, want)
+
+
+def test_prefill_fused_equals_unfused_bitwise(weights):
+    w, W = weights
+    T = 300
+    a = synth.make_activations(11, T, True)
+    R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+    fused = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL)
+    unfused = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL_UNFUSED)
+    for x, y in zip(fused, unfused):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+def test_prefill_bitwise_repeatable_and_pending_write(weights):
+    w, W = weights
+    T = 260
+    a = synth.make_activations(12, T, True)
+    R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+    first = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL)
+    for _ in range(3):
+        again = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL)
+        for x, y in zip(first, again):
+            assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    pre = gpu_read(T, dev_f32((a["R"] + a["P"]).astype(np.float32)), None, W, M,
+                   hc.HC_PATH_PREFILL)
+    for x, y in zip(first, pre):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    assert hc.hc_read_status() == 0
+
+
+def test_decode_and_prefill_paths_agree(weights):
+    w, W = weights
+    for T in (1, 5, 8):
+        a = synth.make_activations(13 + T, T, True)
+        R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+        d = gpu_read(T, R, P, W, M, hc.HC_PATH_DECODE)
+        p = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL)
+        from _hc import rel_diff
+        assert rel_diff(d[0], p[0]) <= 2 * TOL_F32
