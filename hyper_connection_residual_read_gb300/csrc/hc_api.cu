@@ -40,6 +40,7 @@ void free_ctx(Ctx& c) {
     cudaFree(c.wd16);
     cudaFree(c.wu16);
     cudaFree(c.partials);
+    cudaFree(c.ssq);
     cudaFree(c.lo16);
     cudaFree(c.gated);
     c = Ctx();
@@ -243,7 +244,8 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     ok &= cudaMalloc(&c.s.status, sizeof(int)) == cudaSuccess;
     ok &= cudaMalloc(&c.wd16, sizeof(__half) * (size_t)kRank * kCols) == cudaSuccess;
     ok &= cudaMalloc(&c.wu16, sizeof(__half) * (size_t)kCols * kRank) == cudaSuccess;
-    ok &= cudaMalloc(&c.partials, sizeof(float) * (size_t)max_tokens * kStreams * kRank) == cudaSuccess;
+    ok &= cudaMalloc(&c.partials, sizeof(float) * (size_t)max_tokens * kStreams * 4 * kRank) == cudaSuccess;
+    ok &= cudaMalloc(&c.ssq, sizeof(float) * (size_t)max_tokens * kStreams * 4) == cudaSuccess;
     ok &= cudaMalloc(&c.lo16, sizeof(__half) * 2 * (size_t)max_tokens * kRank) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();

@@ -45,7 +45,8 @@ struct Ctx {
     // prefill scratch
     __half* wd16 = nullptr;          // W_down as fp16 [kRank][kCols]
     __half* wu16 = nullptr;          // W_up as fp16 [kCols][kRank]
-    float* partials = nullptr;       // per-stream down partials [max_tokens][kStreams][kRank]
+    float* partials = nullptr;       // down partials [max_tokens][kStreams][4 K quarters][kRank]
+    float* ssq = nullptr;            // sums of squares of R' [max_tokens][kStreams][4 K quarters]
     __half* lo16 = nullptr;          // lo as two fp16 terms [2][max_tokens][kRank]
     float* gated = nullptr;          // [max_tokens][kCols], unfused prefill only (lazy)
     CUtensorMap tm_wd;               // TMA maps over wd16, wu16, lo16

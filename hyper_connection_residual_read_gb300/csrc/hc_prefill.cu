@@ -3,15 +3,15 @@
 //
 //   convert_weights  W_down and W_up, bf16 -> fp16 (exact for |w| >= 2^-17; below
 //                    that the fp16 grid of 2^-24 rounds them by at most 3e-8).
-//   down_tile        the down projection per (128-token tile, stream): A = R' * w_norm
-//                    split on the fly into two fp16 terms (hi + residual), B = the
-//                    stream's 2560 columns of W_down, D = 128 x 320 fp32 in TMEM.
-//                    The epilogue applies the stream's rs (its sum of squares is
-//                    accumulated while A is produced), the norm fold of
-//                    "#2488 sycl/A770: faster hyper-connection read on Arc A-series",
-//                    Summary, change 4, and writes one partial per stream.
-//   lo_split         lo = the 4 stream partials summed in a fixed order, stored as
-//                    two fp16 terms for the up projection's A operand.
+//   down_tile        the down projection per (128-token tile, stream, quarter of the
+//                    stream's 2560 columns): A = R' * w_norm split on the fly into two
+//                    fp16 terms (hi + residual), B = those columns of W_down, D = 128 x
+//                    320 fp32 in TMEM. The epilogue stores the unscaled partial dots
+//                    and the quarter's sums of squares of R'.
+//   lo_split         the norm fold of "#2488 sycl/A770: faster hyper-connection read
+//                    on Arc A-series", Summary, change 4: each stream's rs applied to
+//                    that stream's partial dots, summed in a fixed order; lo is stored
+//                    as two fp16 terms for the up projection's A operand.
 //   upmix_tile       the up projection per (128-token tile, 64 columns x 4 streams),
 //                    D = 128 x 256 fp32, double-buffered in TMEM; the epilogue applies
 //                    the gate and the 4x4 mix and writes mixed with its bf16 and fp16
@@ -47,6 +47,12 @@ constexpr int kDownStages = 3;
 constexpr int kDownBBytes = kDownN * kBK * 2;     // 40 KB
 constexpr int kDownStageBytes = 2 * kTileBytes16 + kDownBBytes;
 constexpr int kDownKBlocks = kWidth / kBK;        // 40 per stream
+// Each stream's K is split into quarters with an accumulator (and a partial) each:
+// the tensor cores' fp32 accumulation rounds toward zero at every MMA, so the depth
+// of one accumulation (here 10 K blocks x 4 steps x 2 terms = 80 MMAs) bounds the
+// relative shrink of the result.
+constexpr int kDownKSplit = 4;
+constexpr int kDownKBlocksPerTile = kDownKBlocks / kDownKSplit;   // 10
 constexpr int kDownThreads = 320;                  // TMA, MMA, 8 converter/epilogue warps
 constexpr int kDownSmem = kDownStages * kDownStageBytes + 1024;
 
@@ -105,7 +111,8 @@ __global__ void convert_weights_kernel(const uint16_t* __restrict__ wd, const ui
 __global__ void __launch_bounds__(kDownThreads, 1)
 down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                  const uint16_t* __restrict__ w_norm, const __grid_constant__ CUtensorMap tm_wd,
-                 float* __restrict__ partials, int T, float eps, int* __restrict__ status) {
+                 float* __restrict__ partials, float* __restrict__ ssq, int T,
+                 int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[kDownStages], empty_bar[kDownStages];
@@ -115,7 +122,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
     __shared__ float ss_s[2][kTileM];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles = ((T + kTileM - 1) / kTileM) * kStreams;
+    const int n_tiles = ((T + kTileM - 1) / kTileM) * kStreams * kDownKSplit;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kDownStages; ++i) {
@@ -142,8 +149,8 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         if (lane == 0) {
             int it = 0;
             for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
-                const int s = tile % kStreams;
-                for (int kb = 0; kb < kDownKBlocks; ++kb, ++it) {
+                const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
+                for (int kb = kq * kDownKBlocksPerTile; kb < (kq + 1) * kDownKBlocksPerTile; ++kb, ++it) {
                     const int slot = it % kDownStages;
                     const uint32_t ph = (it / kDownStages) & 1;
                     if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
@@ -163,7 +170,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                 if (!mbar_wait(&acc_empty, (lt & 1) ^ 1, &abort_flag, status)) break;
                 tc_fence_after();
                 bool ok = true;
-                for (int kb = 0; kb < kDownKBlocks; ++kb, ++it) {
+                for (int kl = 0; kl < kDownKBlocksPerTile; ++kl, ++it) {
                     const int slot = it % kDownStages;
                     const uint32_t ph = (it / kDownStages) & 1;
                     if (!mbar_wait(&full_bar[slot], ph, &abort_flag, status)) { ok = false; break; }
@@ -178,7 +185,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                             for (int h = 0; h < 2; ++h)
                                 mma_f16(tmem + h * (kDownN / 2), desc_sw128(a0 + kk * 32),
                                         desc_sw128(b0 + h * (kDownBBytes / 2) + kk * 32), idesc,
-                                        (kb | term | kk) != 0);
+                                        (kl | term | kk) != 0);
                         }
                     }
                     mma_commit(&empty_bar[slot]);
@@ -193,11 +200,12 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         const int m = q * 32 + lane;
         int it = 0, lt = 0;
         for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
-            const int tt = tile / kStreams, s = tile % kStreams;
+            const int tt = tile / (kStreams * kDownKSplit);
+            const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
             const int t = tt * kTileM + m;
             const bool valid = t < T;
             float ss = 0.f, amax = 0.f;
-            for (int kb = 0; kb < kDownKBlocks; ++kb, ++it) {
+            for (int kb = kq * kDownKBlocksPerTile; kb < (kq + 1) * kDownKBlocksPerTile; ++kb, ++it) {
                 const int slot = it % kDownStages;
                 const uint32_t ph = (it / kDownStages) & 1;
                 const int k = s * kWidth + kb * kBK + half * 32;
@@ -254,11 +262,12 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             ss_s[half][m] = ss;
             mbar_arrive(&ss_bar);
             if (!mbar_wait(&ss_bar, lt & 1, &abort_flag, status)) break;
-            // epilogue: scale this stream's partial dots by its rs and store them
+            // epilogue: store this quarter's partial dots and its sums of squares
             if (!mbar_wait(&acc_full, lt & 1, &abort_flag, status)) break;
             tc_fence_after();
-            const float rs = 1.0f / sqrtf((ss_s[0][m] + ss_s[1][m]) / (float)kWidth + eps);
-            float* dst = partials + ((size_t)t * kStreams + s) * kRank + half * (kDownN / 2);
+            const size_t prow = ((size_t)t * kStreams + s) * kDownKSplit + kq;
+            if (valid && half == 0) ssq[prow] = ss_s[0][m] + ss_s[1][m];
+            float* dst = partials + prow * kRank + half * (kDownN / 2);
 #pragma unroll 1
             for (int c0 = 0; c0 < kDownN / 2; c0 += 16) {
                 float v[16];
@@ -267,8 +276,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         *reinterpret_cast<float4*>(dst + c0 + 4 * i) =
-                            make_float4(v[4 * i] * rs, v[4 * i + 1] * rs, v[4 * i + 2] * rs,
-                                        v[4 * i + 3] * rs);
+                            make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                 }
             }
             tc_fence_before();
@@ -286,17 +294,27 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
 // ---------------------------------------------------------------------------
 // lo = sum of the 4 stream partials (in stream order), split into two fp16 terms
 // ---------------------------------------------------------------------------
-__global__ void lo_split_kernel(const float* __restrict__ partials, __half* __restrict__ lo16,
-                                int T, int max_tokens, int* __restrict__ status) {
+__global__ void lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ssq,
+                                __half* __restrict__ lo16, int T, int max_tokens, float eps,
+                                int* __restrict__ status) {
     const int n4 = T * (kRank / 4);
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += gridDim.x * blockDim.x) {
         const int t = i / (kRank / 4), j = 4 * (i % (kRank / 4));
-        const float* p = partials + (size_t)t * kStreams * kRank + j;
-        float4 v = *reinterpret_cast<const float4*>(p);
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int s = 1; s < kStreams; ++s) {
-            const float4 w = *reinterpret_cast<const float4*>(p + s * kRank);
-            v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+        for (int s = 0; s < kStreams; ++s) {
+            const size_t row = ((size_t)t * kStreams + s) * kDownKSplit;
+            float ss = ssq[row];
+            float4 d = *reinterpret_cast<const float4*>(partials + row * kRank + j);
+#pragma unroll
+            for (int q = 1; q < kDownKSplit; ++q) {
+                ss += ssq[row + q];
+                const float4 w = *reinterpret_cast<const float4*>(partials + (row + q) * kRank + j);
+                d.x += w.x; d.y += w.y; d.z += w.z; d.w += w.w;
+            }
+            const float rs = 1.0f / sqrtf(ss / (float)kWidth + eps);
+            v.x = fmaf(rs, d.x, v.x); v.y = fmaf(rs, d.y, v.y);
+            v.z = fmaf(rs, d.z, v.z); v.w = fmaf(rs, d.w, v.w);
         }
         if (fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) >= 65504.f)
             atomicOr(status, kStatusRange);
@@ -595,12 +613,14 @@ cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, bool fused, cudaStre
     const int n8 = kRank * kCols / 8;
     convert_weights_kernel<<<2 * c.sm_count, 512, 0, st>>>(a.W_down, a.W_up, c.wd16, c.wu16, n8);
     const int n_tt = (a.T + kTileM - 1) / kTileM;
-    const int down_grid = n_tt * kStreams < c.sm_count ? n_tt * kStreams : c.sm_count;
+    const int down_tiles = n_tt * kStreams * kDownKSplit;
+    const int down_grid = down_tiles < c.sm_count ? down_tiles : c.sm_count;
     down_tile_kernel<<<down_grid, kDownThreads, kDownSmem, st>>>(a.R, a.P, a.w_norm, c.tm_wd,
-                                                                 c.partials, a.T, c.eps, c.s.status);
+                                                                 c.partials, c.ssq, a.T, c.s.status);
     const int n4 = a.T * (kRank / 4);
     const int rgrid = (n4 + 255) / 256 < 8 * c.sm_count ? (n4 + 255) / 256 : 8 * c.sm_count;
-    lo_split_kernel<<<rgrid, 256, 0, st>>>(c.partials, c.lo16, a.T, c.max_tokens, c.s.status);
+    lo_split_kernel<<<rgrid, 256, 0, st>>>(c.partials, c.ssq, c.lo16, a.T, c.max_tokens, c.eps,
+                                           c.s.status);
     const int up_tiles = n_tt * kUpColTiles;
     const int up_grid = up_tiles < c.sm_count ? up_tiles : c.sm_count;
     if (fused) {
