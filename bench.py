@@ -460,6 +460,29 @@ def profile_decode(args) -> None:
     print(json.dumps({"profile": "decode", "reads": args.steps, "status": rc}))
 
 
+def profile_prefill(args) -> None:
+    """A fixed prefill workload for ncu: ``--steps`` reads of one 8,192-token chunk
+    (fused path), then one read through the unfused pair. No timing."""
+    import torch
+    import hyper_connection_residual_read_gb300 as hc
+    from hyper_connection_residual_read_gb300 import synth
+    T = 8192
+    hc.hc_read_init(0, T, EPS)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(  # noqa: E731
+        x.view(np.int16) if x.dtype == np.uint16 else x)).cuda()
+    W = {k: dev(v) for k, v in synth.make_weights(0).items()}
+    c = synth.make_prefill_chunk(100, T)
+    R, M = dev(c["R"]), dev(c["Rmix"])
+    o = [torch.empty((T, 4, 2560), dtype=dt, device="cuda")
+         for dt in (torch.float32, torch.int16, torch.int16)]
+    for _ in range(args.steps):
+        hc.hc_read_path(hc.HC_PATH_PREFILL, T, R, None, W["w_norm"], W["W_down"], W["W_up"], M, *o)
+    hc.hc_read_path(hc.HC_PATH_PREFILL_UNFUSED, T, R, None, W["w_norm"], W["W_down"], W["W_up"],
+                    M, *o)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": "prefill", "reads": args.steps, "status": hc.hc_read_status()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -468,11 +491,13 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode"], default=None,
+    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
                     help="run a small fixed workload for an ncu capture instead of timing")
     args = ap.parse_args()
     if args.profile == "decode":
         profile_decode(args)
+    elif args.profile == "prefill":
+        profile_prefill(args)
     elif args.impl == "reference":
         # each reference step is a whole 16-read oracle sweep (about a second)
         args.steps = max(1, min(args.steps, 20))
