@@ -59,13 +59,22 @@ constexpr int kDownSmem = kDownStages * kDownStageBytes + 1024;
 // upmix_tile
 constexpr int kUpCols = 64;            // output columns per tile (x 4 streams = N 256)
 constexpr int kUpN = kStreams * kUpCols;
-constexpr int kUpStages = 3;
+constexpr int kUpStages = 2;
 constexpr int kUpBBytes = kUpN * kBK * 2;         // 32 KB
 constexpr int kUpStageBytes = 2 * kTileBytes16 + kUpBBytes;
 constexpr int kUpKBlocks = kRank / kBK;           // 5
 constexpr int kUpColTiles = kWidth / kUpCols;     // 40
-constexpr int kUpThreads = 320;                    // TMA, MMA, 8 epilogue warps
-constexpr int kUpSmem = kUpStages * kUpStageBytes + 1024;
+constexpr int kUpEpiWarps = 4;                    // one per TMEM lane quarter (32 tokens)
+constexpr int kUpThreads = 64 + 32 * kUpEpiWarps; // TMA, MMA, epilogue warps
+// The epilogue moves its 32 tokens x 8 columns x 4 streams per step through shared
+// memory with TMA: R (and P) tiles in, double-buffered; the fp32 result and its two
+// 16-bit images out.
+constexpr int kEpiCols = 8;
+constexpr int kEpiRows = 32;
+constexpr int kEpiIn = kStreams * kEpiRows * kEpiCols * 4;      // 4 KB
+constexpr int kEpiOut16 = kStreams * kEpiRows * kEpiCols * 2;   // 2 KB
+constexpr int kEpiWarpBytes = 4 * kEpiIn + kEpiIn + 2 * kEpiOut16;   // 24 KB
+constexpr int kUpSmem = kUpStages * kUpStageBytes + kUpEpiWarps * kEpiWarpBytes + 1024;
 
 constexpr int kStatusRange = kStatusRangeBit;
 
@@ -195,78 +204,86 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             }
         }
     } else {
-        // 8 converter warps: produce A for their (row quarter, K half); then epilogue
+        // 8 converter warps produce A: warp cw owns rows 16*cw..16*cw+15 of the tile;
+        // in each K block, lanes 0-15 and 16-31 read two rows at a time, 16 bytes each,
+        // so every load instruction covers two 256-byte row segments. The same warps then
+        // run the epilogue on their TMEM lane quarter.
+        const int cw = warp - 2;
         const int q = warp & 3, half = (warp - 2) >> 2;
-        const int m = q * 32 + lane;
+        const int m = q * 32 + lane;                    // epilogue row
+        const int kc = 4 * (lane & 15);                 // this lane's 4 columns in a K block
         int it = 0, lt = 0;
         for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
             const int tt = tile / (kStreams * kDownKSplit);
             const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
             const int t = tt * kTileM + m;
             const bool valid = t < T;
-            float ss = 0.f, amax = 0.f;
+            float ss[8], amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss[i] = 0.f;
             for (int kb = kq * kDownKBlocksPerTile; kb < (kq + 1) * kDownKBlocksPerTile; ++kb, ++it) {
                 const int slot = it % kDownStages;
                 const uint32_t ph = (it / kDownStages) & 1;
-                const int k = s * kWidth + kb * kBK + half * 32;
-                float x[32];
-                if (valid) {
-                    const float4* r4 = reinterpret_cast<const float4*>(R + (size_t)t * kCols + k);
+                const int k = s * kWidth + kb * kBK + kc;
+                float4 x[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 v = r4[i];
-                        x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
-                    }
-                    if (P != nullptr) {
-                        const float4* p4 = reinterpret_cast<const float4*>(P + (size_t)t * kCols + k);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 v = p4[i];
-                            x[4 * i] += v.x; x[4 * i + 1] += v.y; x[4 * i + 2] += v.z; x[4 * i + 3] += v.w;
+                for (int i = 0; i < 8; ++i) {
+                    const int row = 16 * cw + 2 * i + (lane >> 4);
+                    const int tr = tt * kTileM + row;
+                    x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (tr < T) {
+                        x[i] = *reinterpret_cast<const float4*>(R + (size_t)tr * kCols + k);
+                        if (P != nullptr) {
+                            const float4 p = *reinterpret_cast<const float4*>(P + (size_t)tr * kCols + k);
+                            x[i].x += p.x; x[i].y += p.y; x[i].z += p.z; x[i].w += p.w;
                         }
                     }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] = 0.f;
                 }
-                uint4 wv[4];
-                const uint4* w4 = reinterpret_cast<const uint4*>(w_norm + k);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) wv[i] = w4[i];
+                const uint2 wv = *reinterpret_cast<const uint2*>(w_norm + k);
+                const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x), w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
                 if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
                 uint8_t* ahi = sA(slot, 0);
                 uint8_t* alo = sA(slot, 1);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {          // 4 chunks of 8 elements
-                    const uint32_t wq[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float r0 = x[8 * j + 2 * e], r1 = x[8 * j + 2 * e + 1];
-                        ss = fmaf(r0, r0, ss);
-                        ss = fmaf(r1, r1, ss);
-                        const float a0 = r0 * bf16_lo(wq[e]), a1 = r1 * bf16_hi(wq[e]);
-                        amax = fmaxf(amax, fmaxf(fabsf(a0), fabsf(a1)));
-                        split2(a0, a1, hi[e], lo[e]);
-                    }
-                    const uint32_t off = sw128_offset(m, half * 32 + 8 * j);
-                    *reinterpret_cast<uint4*>(ahi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4*>(alo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                for (int i = 0; i < 8; ++i) {
+                    const int row = 16 * cw + 2 * i + (lane >> 4);
+                    const float4 r = x[i];
+                    float sq = r.x * r.x;
+                    sq = fmaf(r.y, r.y, sq);
+                    sq = fmaf(r.z, r.z, sq);
+                    sq = fmaf(r.w, r.w, sq);
+                    ss[i] += sq;
+                    const float a0 = r.x * w0, a1 = r.y * w1, a2 = r.z * w2, a3 = r.w * w3;
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))));
+                    uint32_t h0, l0, h1, l1;
+                    split2(a0, a1, h0, l0);
+                    split2(a2, a3, h1, l1);
+                    const uint32_t off = sw128_offset(row, kc);
+                    *reinterpret_cast<uint2*>(ahi + off) = make_uint2(h0, h1);
+                    *reinterpret_cast<uint2*>(alo + off) = make_uint2(l0, l1);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&full_bar[slot]);
             }
             if (abort_flag) break;
             if (amax >= 65504.f) atomicOr(status, kStatusRange);
-            // both K halves of a row must have their sums of squares in place
-            ss_s[half][m] = ss;
+            // sums of squares per row: the 16 lanes that share a row, in a fixed order
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float v = ss[i];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                if ((lane & 15) == 0) ss_s[0][16 * cw + 2 * i + (lane >> 4)] = v;
+            }
             mbar_arrive(&ss_bar);
             if (!mbar_wait(&ss_bar, lt & 1, &abort_flag, status)) break;
             // epilogue: store this quarter's partial dots and its sums of squares
             if (!mbar_wait(&acc_full, lt & 1, &abort_flag, status)) break;
             tc_fence_after();
             const size_t prow = ((size_t)t * kStreams + s) * kDownKSplit + kq;
-            if (valid && half == 0) ssq[prow] = ss_s[0][m] + ss_s[1][m];
+            if (valid && half == 0) ssq[prow] = ss_s[0][m];
             float* dst = partials + prow * kRank + half * (kDownN / 2);
 #pragma unroll 1
             for (int c0 = 0; c0 < kDownN / 2; c0 += 16) {
@@ -329,19 +346,24 @@ __global__ void lo_split_kernel(const float* __restrict__ partials, const float*
 // ---------------------------------------------------------------------------
 // up projection + gate (+ mix), one (128-token tile, 64 columns x 4 streams) per
 // tile, persistent CTAs, two TMEM accumulators so the epilogue of one tile runs
-// under the MMAs of the next.
+// under the MMAs of the next. The epilogue's global traffic goes through TMA: R
+// (and P) tiles are loaded into per-warp staging and the outputs are stored from it,
+// so every transfer is a whole tile of 32-byte rows instead of scattered words.
 // ---------------------------------------------------------------------------
+struct EpiMaps {
+    CUtensorMap R, P, out, out_bf16, out_fp16;
+};
+
 template <bool kFused>
 __global__ void __launch_bounds__(kUpThreads, 1)
-upmix_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
-                  const float* __restrict__ Rmix, const __grid_constant__ CUtensorMap tm_lo,
-                  const __grid_constant__ CUtensorMap tm_wu, float* __restrict__ out_f32,
-                  uint16_t* __restrict__ out_bf16, uint16_t* __restrict__ out_fp16,
-                  float* __restrict__ gated, int T, int* __restrict__ status) {
+upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtensorMap tm_lo,
+                  const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ EpiMaps em,
+                  int has_P, int T, int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[kUpStages], empty_bar[kUpStages];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
+    __shared__ __align__(8) uint64_t in_bar[kUpEpiWarps][2];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -355,7 +377,11 @@ upmix_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 256);
+            mbar_init(&acc_empty[b], 32 * kUpEpiWarps);
+        }
+        for (int w = 0; w < kUpEpiWarps; ++w) {
+            mbar_init(&in_bar[w][0], 1);
+            mbar_init(&in_bar[w][1], 1);
         }
         abort_flag = 0;
         fence_barrier_init();
@@ -418,94 +444,120 @@ upmix_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             }
         }
     } else {
-        // epilogue: lane quarter q of TMEM = tokens q*32..q*32+31 of the tile; the
-        // two warps of a quarter take 32 of the 64 columns each
-        const int q = warp & 3, half = (warp - 2) >> 2;
-        const int m = q * kTileM / 4 + lane;
-        int lt = 0;
+        // epilogue warp ew: TMEM lane quarter q = tokens q*32..q*32+31 of the tile
+        const int ew = warp - 2, q = warp & 3;
+        uint8_t* ebase = smem + kUpStages * kUpStageBytes + ew * kEpiWarpBytes;
+        // input buffers: R at ebase + buf * kEpiIn, P at ebase + (2 + buf) * kEpiIn
+        auto in_r = [&](int buf) { return ebase + buf * kEpiIn; };
+        auto in_p = [&](int buf) { return ebase + (2 + buf) * kEpiIn; };
+        uint8_t* st_f32 = ebase + 4 * kEpiIn;
+        uint8_t* st_b16 = st_f32 + kEpiIn;
+        uint8_t* st_h16 = st_b16 + kEpiOut16;
+        uint64_t* ib = in_bar[ew];
+        const uint32_t in_bytes = kEpiIn * (has_P ? 2 : 1);
+        auto issue_in = [&](int g, int c, int t0) {
+            const int buf = g & 1;
+            mbar_arrive_expect_tx(&ib[buf], in_bytes);
+#pragma unroll
+            for (int s = 0; s < kStreams; ++s) {
+                tma_load_3d(in_r(buf) + s * (kEpiIn / kStreams), &em.R, c, s, t0, &ib[buf]);
+                if (has_P)
+                    tma_load_3d(in_p(buf) + s * (kEpiIn / kStreams), &em.P, c, s, t0, &ib[buf]);
+            }
+        };
+        int g = 0, lt = 0;
         for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
             const int tt = tile / kUpColTiles, ct = tile % kUpColTiles;
             const int b = lt & 1;
-            const int t = tt * kTileM + m;
-            const bool valid = t < T;
+            const int t0 = tt * kTileM + q * kEpiRows;
+            const int t = t0 + lane;
             float mx[16];
-            if (kFused && valid) {
-                const float4* m4 = reinterpret_cast<const float4*>(Rmix + (size_t)t * 16);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float4 v = m4[i];
-                    mx[4 * i] = v.x; mx[4 * i + 1] = v.y; mx[4 * i + 2] = v.z; mx[4 * i + 3] = v.w;
-                }
-            }
-            if (!mbar_wait(&acc_full[b], (lt >> 1) & 1, &abort_flag, status)) break;
-            tc_fence_after();
-#pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                const int cl = half * 32 + cc * 16;            // first of 16 columns in the tile
-                const int c = ct * kUpCols + cl;
-                float g[kStreams][16];
-#pragma unroll
-                for (int s = 0; s < kStreams; ++s)
-                    tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + b * kUpN + s * kUpCols + cl,
-                              g[s]);
-                if (!valid) continue;
-#pragma unroll
-                for (int s = 0; s < kStreams; ++s) {
-                    const size_t off = (size_t)t * kCols + s * kWidth + c;
-                    const float4* r4 = reinterpret_cast<const float4*>(R + off);
-                    float rp[16];
+            if (kFused) {
+                if (t < T) {
+                    const float4* m4 = reinterpret_cast<const float4*>(Rmix + (size_t)t * 16);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float4 v = r4[i];
-                        rp[4 * i] = v.x; rp[4 * i + 1] = v.y; rp[4 * i + 2] = v.z; rp[4 * i + 3] = v.w;
+                        const float4 v = m4[i];
+                        mx[4 * i] = v.x; mx[4 * i + 1] = v.y; mx[4 * i + 2] = v.z; mx[4 * i + 3] = v.w;
                     }
-                    if (P != nullptr) {
-                        const float4* p4 = reinterpret_cast<const float4*>(P + off);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) mx[i] = 0.f;
+                }
+            }
+            if (lane == 0) issue_in(g, ct * kUpCols, t0);
+            if (!mbar_wait(&acc_full[b], (lt >> 1) & 1, &abort_flag, status)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * kUpN;
+            bool ok = true;
+#pragma unroll 1
+            for (int k = 0; k < kUpCols / kEpiCols; ++k, ++g) {
+                const int c = ct * kUpCols + k * kEpiCols;
+                if (lane == 0 && k + 1 < kUpCols / kEpiCols) issue_in(g + 1, c + kEpiCols, t0);
+                float v[kStreams][kEpiCols];
+#pragma unroll
+                for (int s = 0; s < kStreams; ++s) tmem_ld8(tbase + s * kUpCols + k * kEpiCols, v[s]);
+                if (!mbar_wait(&ib[g & 1], (g >> 1) & 1, &abort_flag, status)) { ok = false; break; }
+                // gate: v <- R' * sigmoid(u), row `lane` of each stream's staging
+#pragma unroll
+                for (int s = 0; s < kStreams; ++s) {
+                    const float4* r4 = reinterpret_cast<const float4*>(in_r(g & 1) + (s * kEpiRows + lane) * 32);
+                    float4 ra = r4[0], rb = r4[1];
+                    if (has_P) {
+                        const float4* p4 = reinterpret_cast<const float4*>(in_p(g & 1) + (s * kEpiRows + lane) * 32);
+                        const float4 pa = p4[0], pb = p4[1];
+                        ra.x += pa.x; ra.y += pa.y; ra.z += pa.z; ra.w += pa.w;
+                        rb.x += pb.x; rb.y += pb.y; rb.z += pb.z; rb.w += pb.w;
+                    }
+                    const float rp[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+                    for (int e = 0; e < kEpiCols; ++e) v[s][e] = gate_value(v[s][e], rp[e]);
+                }
+                __syncwarp();   // every lane has read this input buffer
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();   // the previous step's stores have read the staging
+#pragma unroll
+                for (int so = 0; so < kStreams; ++so) {
+                    float o[kEpiCols];
+#pragma unroll
+                    for (int e = 0; e < kEpiCols; ++e)
+                        o[e] = kFused ? mix_row(&mx[so * 4], v[0][e], v[1][e], v[2][e], v[3][e]) : v[so][e];
+                    float4* f4 = reinterpret_cast<float4*>(st_f32 + (so * kEpiRows + lane) * 32);
+                    f4[0] = make_float4(o[0], o[1], o[2], o[3]);
+                    f4[1] = make_float4(o[4], o[5], o[6], o[7]);
+                    if (kFused) {
+                        uint32_t bb[4], hh[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const float4 v = p4[i];
-                            rp[4 * i] += v.x; rp[4 * i + 1] += v.y; rp[4 * i + 2] += v.z; rp[4 * i + 3] += v.w;
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) g[s][e] = gate_value(g[s][e], rp[e]);
-                    if (!kFused) {
-                        float4* d4 = reinterpret_cast<float4*>(gated + off);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            d4[i] = make_float4(g[s][4 * i], g[s][4 * i + 1], g[s][4 * i + 2], g[s][4 * i + 3]);
-                    }
-                }
-                if (kFused) {
-#pragma unroll
-                    for (int so = 0; so < kStreams; ++so) {
-                        float o[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            o[e] = mix_row(&mx[so * 4], g[0][e], g[1][e], g[2][e], g[3][e]);
-                        const size_t off = (size_t)t * kCols + so * kWidth + c;
-                        float4* f4 = reinterpret_cast<float4*>(out_f32 + off);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            f4[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                        uint32_t bb[8], hh[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
                             bb[i] = (uint32_t)to_bf16_bits(o[2 * i]) | ((uint32_t)to_bf16_bits(o[2 * i + 1]) << 16);
                             hh[i] = (uint32_t)to_fp16_bits(o[2 * i]) | ((uint32_t)to_fp16_bits(o[2 * i + 1]) << 16);
                         }
-                        uint4* b4 = reinterpret_cast<uint4*>(out_bf16 + off);
-                        uint4* h4 = reinterpret_cast<uint4*>(out_fp16 + off);
-                        b4[0] = make_uint4(bb[0], bb[1], bb[2], bb[3]);
-                        b4[1] = make_uint4(bb[4], bb[5], bb[6], bb[7]);
-                        h4[0] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-                        h4[1] = make_uint4(hh[4], hh[5], hh[6], hh[7]);
+                        *reinterpret_cast<uint4*>(st_b16 + (so * kEpiRows + lane) * 16) =
+                            make_uint4(bb[0], bb[1], bb[2], bb[3]);
+                        *reinterpret_cast<uint4*>(st_h16 + (so * kEpiRows + lane) * 16) =
+                            make_uint4(hh[0], hh[1], hh[2], hh[3]);
                     }
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+#pragma unroll
+                    for (int so = 0; so < kStreams; ++so) {
+                        tma_store_3d(&em.out, c, so, t0, st_f32 + so * (kEpiIn / kStreams));
+                        if (kFused) {
+                            tma_store_3d(&em.out_bf16, c, so, t0, st_b16 + so * (kEpiOut16 / kStreams));
+                            tma_store_3d(&em.out_fp16, c, so, t0, st_h16 + so * (kEpiOut16 / kStreams));
+                        }
+                    }
+                    bulk_commit();
+                }
             }
+            if (!ok) break;
             tc_fence_before();
             mbar_arrive(&acc_empty[b]);
         }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -567,14 +619,30 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     return fn;
 }
 
-bool encode_fp16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                 const cuuint64_t* strides, const cuuint32_t* box) {
+bool encode_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, int rank,
+                const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                CUtensorMapSwizzle swz) {
     auto enc = get_encoder();
     if (enc == nullptr) return false;
     const cuuint32_t es[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, const_cast<void*>(base), dims, strides,
-               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return enc(map, dt, rank, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_fp16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                 const cuuint64_t* strides, const cuuint32_t* box) {
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, rank, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// A [T][4][2560] activation or output tensor seen as 3D (c, stream, token), in tiles
+// of 8 columns x 1 stream x 32 tokens (TMA clips and zero-fills past token T).
+bool encode_act(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base, int T) {
+    const cuuint64_t dims[3] = {kWidth, kStreams, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)kWidth * esize, (cuuint64_t)kCols * esize};
+    const cuuint32_t box[3] = {kEpiCols, 1, kEpiRows};
+    return encode_map(map, dt, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace
@@ -623,14 +691,25 @@ cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, bool fused, cudaStre
                                            c.s.status);
     const int up_tiles = n_tt * kUpColTiles;
     const int up_grid = up_tiles < c.sm_count ? up_tiles : c.sm_count;
+    EpiMaps em;
+    bool ok = encode_act(&em.R, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.R, a.T);
+    ok = ok && encode_act(&em.P, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.P ? a.P : a.R, a.T);
+    if (fused) {
+        ok = ok && encode_act(&em.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.out_f32, a.T);
+        ok = ok && encode_act(&em.out_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out_bf16, a.T);
+        ok = ok && encode_act(&em.out_fp16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.out_fp16, a.T);
+    } else {
+        ok = ok && encode_act(&em.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, c.gated, a.T);
+        em.out_bf16 = em.out;
+        em.out_fp16 = em.out;
+    }
+    if (!ok) return cudaErrorInvalidValue;
     if (fused) {
         upmix_tile_kernel<true><<<up_grid, kUpThreads, kUpSmem, st>>>(
-            a.R, a.P, a.Rmix, c.tm_lo, c.tm_wu, a.out_f32, a.out_bf16, a.out_fp16, nullptr, a.T,
-            c.s.status);
+            a.Rmix, c.tm_lo, c.tm_wu, em, a.P != nullptr, a.T, c.s.status);
     } else {
         upmix_tile_kernel<false><<<up_grid, kUpThreads, kUpSmem, st>>>(
-            a.R, a.P, a.Rmix, c.tm_lo, c.tm_wu, nullptr, nullptr, nullptr, c.gated, a.T,
-            c.s.status);
+            a.Rmix, c.tm_lo, c.tm_wu, em, a.P != nullptr, a.T, c.s.status);
         const int n = a.T * (kWidth / 4);
         const int mgrid = (n + 255) / 256 < 8 * c.sm_count ? (n + 255) / 256 : 8 * c.sm_count;
         mix_gated_kernel<<<mgrid, 256, 0, st>>>(c.gated, a.Rmix, a.out_f32, a.out_bf16, a.out_fp16,
