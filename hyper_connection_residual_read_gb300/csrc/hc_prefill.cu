@@ -65,16 +65,21 @@ constexpr int kUpStageBytes = 2 * kTileBytes16 + kUpBBytes;
 constexpr int kUpKBlocks = kRank / kBK;           // 5
 constexpr int kUpColTiles = kWidth / kUpCols;     // 40
 constexpr int kUpEpiWarps = 4;                    // one per TMEM lane quarter (32 tokens)
-constexpr int kUpThreads = 64 + 32 * kUpEpiWarps; // TMA, MMA, epilogue warps
-// The epilogue moves its 32 tokens x 8 columns x 4 streams per step through shared
-// memory with TMA: R (and P) tiles in, double-buffered; the fp32 result and its two
-// 16-bit images out.
+constexpr int kUpThreads = 96 + 32 * kUpEpiWarps; // operand TMA, MMA, R TMA, epilogue warps
+// The epilogue takes its tile in steps of 8 columns. A dedicated warp streams the R
+// (and P) tiles of those steps, 128 tokens x 8 columns x 4 streams, through a ring
+// of 16 KB slots ahead of the epilogue warps. Each epilogue warp stages its outputs
+// for TMA tile stores: fp32 per step (32-byte rows), bf16 and fp16 per two steps
+// (32-byte rows as well, so every row written is a whole DRAM sector).
 constexpr int kEpiCols = 8;
 constexpr int kEpiRows = 32;
-constexpr int kEpiIn = kStreams * kEpiRows * kEpiCols * 4;      // 4 KB
-constexpr int kEpiOut16 = kStreams * kEpiRows * kEpiCols * 2;   // 2 KB
-constexpr int kEpiWarpBytes = 4 * kEpiIn + kEpiIn + 2 * kEpiOut16;   // 24 KB
-constexpr int kUpSmem = kUpStages * kUpStageBytes + kUpEpiWarps * kEpiWarpBytes + 1024;
+constexpr int kRSlot = kStreams * kTileM * kEpiCols * 4;        // 16 KB
+constexpr int kRSlots = 3;
+constexpr int kEpiF32 = kStreams * kEpiRows * kEpiCols * 4;     // 4 KB
+constexpr int kEpi16 = kStreams * kEpiRows * 2 * kEpiCols * 2;  // 4 KB (16 columns)
+constexpr int kEpiWarpBytes = kEpiF32 + 2 * kEpi16;             // 12 KB
+constexpr int kUpSmem = kUpStages * kUpStageBytes + kRSlots * kRSlot +
+                        kUpEpiWarps * kEpiWarpBytes + 1024;
 
 constexpr int kStatusRange = kStatusRangeBit;
 
@@ -363,12 +368,15 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
     uint8_t* smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[kUpStages], empty_bar[kUpStages];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
-    __shared__ __align__(8) uint64_t in_bar[kUpEpiWarps][2];
+    __shared__ __align__(8) uint64_t r_full[kRSlots], r_empty[kRSlots];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = ((T + kTileM - 1) / kTileM) * kUpColTiles;
+    constexpr int kSteps = kUpCols / kEpiCols;   // 8 epilogue steps per tile
+    // with a pending write a step needs two slots (R, then P)
+    const int slots_per_step = has_P ? 2 : 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kUpStages; ++i) {
@@ -379,9 +387,9 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 32 * kUpEpiWarps);
         }
-        for (int w = 0; w < kUpEpiWarps; ++w) {
-            mbar_init(&in_bar[w][0], 1);
-            mbar_init(&in_bar[w][1], 1);
+        for (int i = 0; i < kRSlots; ++i) {
+            mbar_init(&r_full[i], 1);
+            mbar_init(&r_empty[i], kUpEpiWarps);
         }
         abort_flag = 0;
         fence_barrier_init();
@@ -394,8 +402,11 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
 
     auto sA = [&](int slot, int term) { return smem + slot * kUpStageBytes + term * kTileBytes16; };
     auto sB = [&](int slot) { return smem + slot * kUpStageBytes + 2 * kTileBytes16; };
+    uint8_t* rring = smem + kUpStages * kUpStageBytes;
+    uint8_t* ostage = rring + kRSlots * kRSlot;
 
     if (warp == 0) {
+        // operand producer: lo terms and W_up rows, K blocks of 64
         if (lane == 0) {
             int it = 0;
             for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
@@ -443,29 +454,35 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                 mma_commit(&acc_full[b]);
             }
         }
-    } else {
-        // epilogue warp ew: TMEM lane quarter q = tokens q*32..q*32+31 of the tile
-        const int ew = warp - 2, q = warp & 3;
-        uint8_t* ebase = smem + kUpStages * kUpStageBytes + ew * kEpiWarpBytes;
-        // input buffers: R at ebase + buf * kEpiIn, P at ebase + (2 + buf) * kEpiIn
-        auto in_r = [&](int buf) { return ebase + buf * kEpiIn; };
-        auto in_p = [&](int buf) { return ebase + (2 + buf) * kEpiIn; };
-        uint8_t* st_f32 = ebase + 4 * kEpiIn;
-        uint8_t* st_b16 = st_f32 + kEpiIn;
-        uint8_t* st_h16 = st_b16 + kEpiOut16;
-        uint64_t* ib = in_bar[ew];
-        const uint32_t in_bytes = kEpiIn * (has_P ? 2 : 1);
-        auto issue_in = [&](int g, int c, int t0) {
-            const int buf = g & 1;
-            mbar_arrive_expect_tx(&ib[buf], in_bytes);
+    } else if (warp == 2) {
+        // R (and P) producer: one slot per step (two with P), 4 streams per slot
+        if (lane == 0) {
+            int u = 0;   // slot uses
+            for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
+                const int tt = tile / kUpColTiles, ct = tile % kUpColTiles;
+                for (int k = 0; k < kSteps; ++k) {
+                    for (int which = 0; which < slots_per_step; ++which, ++u) {
+                        const int slot = u % kRSlots;
+                        if (!mbar_wait(&r_empty[slot], ((u / kRSlots) & 1) ^ 1, &abort_flag, status))
+                            break;
+                        mbar_arrive_expect_tx(&r_full[slot], kRSlot);
+                        const CUtensorMap* map = which ? &em.P : &em.R;
 #pragma unroll
-            for (int s = 0; s < kStreams; ++s) {
-                tma_load_3d(in_r(buf) + s * (kEpiIn / kStreams), &em.R, c, s, t0, &ib[buf]);
-                if (has_P)
-                    tma_load_3d(in_p(buf) + s * (kEpiIn / kStreams), &em.P, c, s, t0, &ib[buf]);
+                        for (int s = 0; s < kStreams; ++s)
+                            tma_load_3d(rring + slot * kRSlot + s * (kRSlot / kStreams), map,
+                                        ct * kUpCols + k * kEpiCols, s, tt * kTileM, &r_full[slot]);
+                    }
+                }
             }
-        };
-        int g = 0, lt = 0;
+        }
+    } else {
+        // epilogue warp: TMEM lane quarter q = tokens q*32..q*32+31 of the tile
+        const int ew = warp - 3, q = warp & 3;
+        uint8_t* st_f32 = ostage + ew * kEpiWarpBytes;
+        uint8_t* st_b16 = st_f32 + kEpiF32;
+        uint8_t* st_h16 = st_b16 + kEpi16;
+        const int row = q * kEpiRows + lane;         // this lane's token within the tile
+        int u = 0, lt = 0;
         for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
             const int tt = tile / kUpColTiles, ct = tile % kUpColTiles;
             const int b = lt & 1;
@@ -485,37 +502,43 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     for (int i = 0; i < 16; ++i) mx[i] = 0.f;
                 }
             }
-            if (lane == 0) issue_in(g, ct * kUpCols, t0);
             if (!mbar_wait(&acc_full[b], (lt >> 1) & 1, &abort_flag, status)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * kUpN;
             bool ok = true;
 #pragma unroll 1
-            for (int k = 0; k < kUpCols / kEpiCols; ++k, ++g) {
+            for (int k = 0; k < kSteps; ++k) {
                 const int c = ct * kUpCols + k * kEpiCols;
-                if (lane == 0 && k + 1 < kUpCols / kEpiCols) issue_in(g + 1, c + kEpiCols, t0);
                 float v[kStreams][kEpiCols];
 #pragma unroll
                 for (int s = 0; s < kStreams; ++s) tmem_ld8(tbase + s * kUpCols + k * kEpiCols, v[s]);
-                if (!mbar_wait(&ib[g & 1], (g >> 1) & 1, &abort_flag, status)) { ok = false; break; }
-                // gate: v <- R' * sigmoid(u), row `lane` of each stream's staging
+                // R' of this lane's token: slot layout [stream][128 tokens][8 columns]
+                float rp[kStreams][kEpiCols];
+                for (int which = 0; which < slots_per_step; ++which, ++u) {
+                    const int slot = u % kRSlots;
+                    if (!mbar_wait(&r_full[slot], (u / kRSlots) & 1, &abort_flag, status)) { ok = false; break; }
 #pragma unroll
-                for (int s = 0; s < kStreams; ++s) {
-                    const float4* r4 = reinterpret_cast<const float4*>(in_r(g & 1) + (s * kEpiRows + lane) * 32);
-                    float4 ra = r4[0], rb = r4[1];
-                    if (has_P) {
-                        const float4* p4 = reinterpret_cast<const float4*>(in_p(g & 1) + (s * kEpiRows + lane) * 32);
-                        const float4 pa = p4[0], pb = p4[1];
-                        ra.x += pa.x; ra.y += pa.y; ra.z += pa.z; ra.w += pa.w;
-                        rb.x += pb.x; rb.y += pb.y; rb.z += pb.z; rb.w += pb.w;
+                    for (int s = 0; s < kStreams; ++s) {
+                        const float4* r4 = reinterpret_cast<const float4*>(
+                            rring + slot * kRSlot + s * (kRSlot / kStreams) + row * 32);
+                        const float4 a = r4[0], bq = r4[1];
+                        const float x[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+                        for (int e = 0; e < kEpiCols; ++e) rp[s][e] = which ? rp[s][e] + x[e] : x[e];
                     }
-                    const float rp[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
-#pragma unroll
-                    for (int e = 0; e < kEpiCols; ++e) v[s][e] = gate_value(v[s][e], rp[e]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&r_empty[slot]);
                 }
-                __syncwarp();   // every lane has read this input buffer
+                if (!ok) break;
+#pragma unroll
+                for (int s = 0; s < kStreams; ++s)
+#pragma unroll
+                    for (int e = 0; e < kEpiCols; ++e) v[s][e] = gate_value(v[s][e], rp[s][e]);
+                // staging: the fp32 buffer is rewritten every step, the 16-bit ones every
+                // second step; wait until the stores that read them have done so
                 if (lane == 0) bulk_wait_read_all();
-                __syncwarp();   // the previous step's stores have read the staging
+                __syncwarp();
+                const int h = k & 1;                    // which 8 of the 16 staged columns
 #pragma unroll
                 for (int so = 0; so < kStreams; ++so) {
                     float o[kEpiCols];
@@ -532,9 +555,9 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                             bb[i] = (uint32_t)to_bf16_bits(o[2 * i]) | ((uint32_t)to_bf16_bits(o[2 * i + 1]) << 16);
                             hh[i] = (uint32_t)to_fp16_bits(o[2 * i]) | ((uint32_t)to_fp16_bits(o[2 * i + 1]) << 16);
                         }
-                        *reinterpret_cast<uint4*>(st_b16 + (so * kEpiRows + lane) * 16) =
+                        *reinterpret_cast<uint4*>(st_b16 + (so * kEpiRows + lane) * 32 + h * 16) =
                             make_uint4(bb[0], bb[1], bb[2], bb[3]);
-                        *reinterpret_cast<uint4*>(st_h16 + (so * kEpiRows + lane) * 16) =
+                        *reinterpret_cast<uint4*>(st_h16 + (so * kEpiRows + lane) * 32 + h * 16) =
                             make_uint4(hh[0], hh[1], hh[2], hh[3]);
                     }
                 }
@@ -543,10 +566,10 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                 if (lane == 0) {
 #pragma unroll
                     for (int so = 0; so < kStreams; ++so) {
-                        tma_store_3d(&em.out, c, so, t0, st_f32 + so * (kEpiIn / kStreams));
-                        if (kFused) {
-                            tma_store_3d(&em.out_bf16, c, so, t0, st_b16 + so * (kEpiOut16 / kStreams));
-                            tma_store_3d(&em.out_fp16, c, so, t0, st_h16 + so * (kEpiOut16 / kStreams));
+                        tma_store_3d(&em.out, c, so, t0, st_f32 + so * (kEpiF32 / kStreams));
+                        if (kFused && h == 1) {
+                            tma_store_3d(&em.out_bf16, c - kEpiCols, so, t0, st_b16 + so * (kEpi16 / kStreams));
+                            tma_store_3d(&em.out_fp16, c - kEpiCols, so, t0, st_h16 + so * (kEpi16 / kStreams));
                         }
                     }
                     bulk_commit();
@@ -637,11 +660,12 @@ bool encode_fp16(CUtensorMap* map, const void* base, int rank, const cuuint64_t*
 }
 
 // A [T][4][2560] activation or output tensor seen as 3D (c, stream, token), in tiles
-// of 8 columns x 1 stream x 32 tokens (TMA clips and zero-fills past token T).
-bool encode_act(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base, int T) {
+// of `cols` columns x 1 stream x `rows` tokens (TMA clips and zero-fills past T).
+bool encode_act(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base, int T,
+                int cols, int rows) {
     const cuuint64_t dims[3] = {kWidth, kStreams, (cuuint64_t)T};
     const cuuint64_t strides[2] = {(cuuint64_t)kWidth * esize, (cuuint64_t)kCols * esize};
-    const cuuint32_t box[3] = {kEpiCols, 1, kEpiRows};
+    const cuuint32_t box[3] = {(cuuint32_t)cols, 1, (cuuint32_t)rows};
     return encode_map(map, dt, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
@@ -692,14 +716,19 @@ cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, bool fused, cudaStre
     const int up_tiles = n_tt * kUpColTiles;
     const int up_grid = up_tiles < c.sm_count ? up_tiles : c.sm_count;
     EpiMaps em;
-    bool ok = encode_act(&em.R, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.R, a.T);
-    ok = ok && encode_act(&em.P, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.P ? a.P : a.R, a.T);
+    bool ok = encode_act(&em.R, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.R, a.T, kEpiCols, kTileM);
+    ok = ok && encode_act(&em.P, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.P ? a.P : a.R, a.T,
+                          kEpiCols, kTileM);
     if (fused) {
-        ok = ok && encode_act(&em.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.out_f32, a.T);
-        ok = ok && encode_act(&em.out_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out_bf16, a.T);
-        ok = ok && encode_act(&em.out_fp16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.out_fp16, a.T);
+        ok = ok && encode_act(&em.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.out_f32, a.T,
+                              kEpiCols, kEpiRows);
+        ok = ok && encode_act(&em.out_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out_bf16, a.T,
+                              2 * kEpiCols, kEpiRows);
+        ok = ok && encode_act(&em.out_fp16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.out_fp16, a.T,
+                              2 * kEpiCols, kEpiRows);
     } else {
-        ok = ok && encode_act(&em.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, c.gated, a.T);
+        ok = ok && encode_act(&em.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, c.gated, a.T,
+                              kEpiCols, kEpiRows);
         em.out_bf16 = em.out;
         em.out_fp16 = em.out;
     }
