@@ -37,6 +37,7 @@ void free_ctx(Ctx& c) {
     if (c.device >= 0) cudaSetDevice(c.device);
     cudaFree(c.s.lo);
     cudaFree(c.s.status);
+    cudaFree(c.s.sync);
     cudaFree(c.wd16);
     cudaFree(c.wu16);
     cudaFree(c.partials);
@@ -101,13 +102,16 @@ int run(int path, const ReadArgs& a, cudaStream_t st) {
     int err;
     Ctx* c = current_ctx(&err);
     if (!c) return err;
-    if (path < HC_PATH_AUTO || path > HC_PATH_PREFILL_UNFUSED) return HC_ERR_ARG;
+    if (path < HC_PATH_AUTO || path > HC_PATH_DECODE_SPLIT) return HC_ERR_ARG;
     if (int e = validate(*c, a)) return e;
     if (a.T == 0) return HC_OK;
     if (path == HC_PATH_AUTO) path = a.T <= kAutoDecodeMaxT ? HC_PATH_DECODE : HC_PATH_PREFILL;
     cudaError_t ce;
     switch (path) {
         case HC_PATH_DECODE:
+            ce = c->fused_decode ? launch_decode_fused(*c, a, st) : launch_decode(*c, a, st);
+            break;
+        case HC_PATH_DECODE_SPLIT:
             ce = launch_decode(*c, a, st);
             break;
         case HC_PATH_PREFILL:
@@ -242,6 +246,7 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     bool ok = true;
     ok &= cudaMalloc(&c.s.lo, sizeof(float) * (size_t)max_tokens * kRank) == cudaSuccess;
     ok &= cudaMalloc(&c.s.status, sizeof(int)) == cudaSuccess;
+    ok &= cudaMalloc(&c.s.sync, 2 * sizeof(unsigned)) == cudaSuccess;
     ok &= cudaMalloc(&c.wd16, sizeof(__half) * (size_t)kRank * kCols) == cudaSuccess;
     ok &= cudaMalloc(&c.wu16, sizeof(__half) * (size_t)kCols * kRank) == cudaSuccess;
     ok &= cudaMalloc(&c.partials, sizeof(float) * (size_t)max_tokens * kStreams * 4 * kRank) == cudaSuccess;
@@ -253,6 +258,8 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
         return HC_ERR_NOMEM;
     }
     if (cudaMemset(c.s.status, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(c.s.sync, 0, 2 * sizeof(unsigned)) != cudaSuccess ||
+        decode_fused_setup(&c.fused_decode) != cudaSuccess ||
         cudaMemset(c.lo16, 0, sizeof(__half) * 2 * (size_t)max_tokens * kRank) != cudaSuccess ||
         prefill_setup(c) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {

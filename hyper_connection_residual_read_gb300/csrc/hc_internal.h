@@ -32,6 +32,8 @@ constexpr int kStatusRangeBit = 2;   // a prefill activation did not fit fp16
 struct Scratch {
     float* lo = nullptr;             // [max_tokens][kRank], the down projection's output
     int* status = nullptr;           // device status word
+    unsigned* sync = nullptr;        // fused decode: [0] clusters that published lo,
+                                     // [1] CTAs that have read it (both reset per call)
 };
 
 struct Ctx {
@@ -40,6 +42,7 @@ struct Ctx {
     int max_tokens = 0;
     float eps = 1e-6f;
     int sm_count = 0;
+    bool fused_decode = false;       // the one-kernel decode read can run on this device
     char name[64] = {0};
     Scratch s;
     // prefill scratch
@@ -69,6 +72,11 @@ struct ReadArgs {
 
 // Decode kernels for any T: launched in chunks of kDecodeMaxT tokens.
 cudaError_t launch_decode(const Ctx& ctx, const ReadArgs& a, cudaStream_t st);
+
+// Decode read as one kernel per chunk of up to 8 tokens (needs s.lo and s.sync).
+// Sets kernel attributes; *usable tells whether all 20 clusters can be resident at once.
+cudaError_t decode_fused_setup(bool* usable);
+cudaError_t launch_decode_fused(const Ctx& ctx, const ReadArgs& a, cudaStream_t st);
 
 // Prefill (tensor-core tile) path: TMA maps and kernel attributes, then the launch.
 cudaError_t prefill_setup(Ctx& ctx);

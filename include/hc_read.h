@@ -86,9 +86,10 @@ enum hc_status {
  * tensor-core tile path above that; the others force one path (tests, bench). */
 enum hc_path {
     HC_PATH_AUTO = 0,
-    HC_PATH_DECODE = 1,          /* sliced down + up/gate/mix kernels (any T) */
+    HC_PATH_DECODE = 1,          /* one kernel per 8 tokens: sliced down, lo exchange, up/gate/mix */
     HC_PATH_PREFILL = 2,         /* tile down, fused up + gate + mix epilogue */
-    HC_PATH_PREFILL_UNFUSED = 3  /* tile down, up GEMM writing gated, then the mix */
+    HC_PATH_PREFILL_UNFUSED = 3, /* tile down, up GEMM writing gated, then the mix */
+    HC_PATH_DECODE_SPLIT = 4     /* the decode read as two kernels (down; up/gate/mix) */
 };
 
 /* Creates the context of `device` (makes it current), checks that it is sm_103,

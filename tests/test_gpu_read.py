@@ -20,7 +20,7 @@ from _hc import (EPS, MAX_TOKENS, TOL_F32, alloc_out, assert_matches_oracle, dev
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [None, hc.HC_PATH_DECODE]
+PATHS = [None, hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_SPLIT]
 
 
 @pytest.fixture(scope="module")
@@ -59,8 +59,15 @@ def test_verify_window_sweep(weights, T, with_P):
 
 
 @pytest.mark.parametrize("T", [9, 13, 16, 17, 31])
-def test_ragged_token_counts(weights, T):
-    got, want = run_case(weights, T, True, 100 + T, hc.HC_PATH_DECODE)
+@pytest.mark.parametrize("path", [hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_SPLIT])
+def test_ragged_token_counts(weights, T, path):
+    got, want = run_case(weights, T, True, 100 + T, path)
+    assert_matches_oracle(got, want)
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
+def test_split_decode_path(weights, T):
+    got, want = run_case(weights, T, True, 300 + T, hc.HC_PATH_DECODE_SPLIT)
     assert_matches_oracle(got, want)
 
 
@@ -85,15 +92,16 @@ def test_pending_write_equals_preadded(weights):
         assert np.array_equal(p.view(np.uint8), q.view(np.uint8))
 
 
-def test_token_batch_invariance_decode(weights):
+@pytest.mark.parametrize("path", [hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_SPLIT])
+def test_token_batch_invariance_decode(weights, path):
     """Token t's bits do not depend on the other tokens of the call."""
     w, W = weights
     a = synth.make_activations(9, 8, True)
     R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
-    full = gpu_read(8, R, P, W, M, hc.HC_PATH_DECODE)
+    full = gpu_read(8, R, P, W, M, path)
     for t in (0, 5, 7):
         one = gpu_read(1, R[t:t + 1].contiguous(), P[t:t + 1].contiguous(), W,
-                       M[t:t + 1].contiguous(), hc.HC_PATH_DECODE)
+                       M[t:t + 1].contiguous(), path)
         assert np.array_equal(one[0][0].view(np.uint32), full[0][t].view(np.uint32))
 
 
@@ -156,6 +164,8 @@ def test_argument_errors_are_refused(weights):
         call(T=MAX_TOKENS + 1)
     with pytest.raises(hc.HcReadError):
         hc.hc_read_path(17, 2, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o)
+    with pytest.raises(hc.HcReadError):
+        hc.hc_read_path(-1, 2, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o)
     assert hc.hc_read_status() == 0
 
 
