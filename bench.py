@@ -301,30 +301,37 @@ def gpu_arm(args) -> None:
     us_per_read = 1e3 * ms / (args.steps * reads_per_step * world)
     step_bytes = sum(read_bytes(T, p) for T, p in SWEEP)
 
-    # --- per-T times (graph of 96 reads of one T, rotated sets) ---
-    per_t = {}
-    for T in (1, 4, 8):
-        for p in (False, True):
-            a0 = synth.make_activations(500 + T, T, p)
-            R, Pd, M = to_dev(a0["R"]), to_dev(a0["P"]), to_dev(a0["Rmix"])
-            o = tuple(torch.empty((T, 4, 2560), dtype=dt, device=dev)
-                      for dt in (torch.float32, torch.int16, torch.int16))
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                for i in range(N_SETS):
-                    W = sets[i]
-                    hc.hc_read(T, R, Pd, W["w_norm"], W["W_down"], W["W_up"], M, *o,
-                               stream=stream)
-                stream.synchronize()
-                with torch.cuda.graph(gr, stream=stream):
+    # --- per-T times (graph of 48 reads of one T over the 48 sets), for each decode path ---
+    def per_t_times(path, Ts, with_p=(False, True)):
+        out = {}
+        for T in Ts:
+            for p in with_p:
+                a0 = synth.make_activations(500 + T, T, p)
+                R, Pd, M = to_dev(a0["R"]), to_dev(a0["P"]), to_dev(a0["Rmix"])
+                o = tuple(torch.empty((T, 4, 2560), dtype=dt, device=dev)
+                          for dt in (torch.float32, torch.int16, torch.int16))
+                gr = torch.cuda.CUDAGraph()
+
+                def enqueue():
                     for i in range(N_SETS):
                         W = sets[i]
-                        hc.hc_read(T, R, Pd, W["w_norm"], W["W_down"], W["W_up"], M, *o,
-                                   stream=stream)
-            ms_t = timed(lambda k: gr.replay(), 40, 3)
-            us = 1e3 * ms_t / (40 * N_SETS)
-            per_t[f"T{T}{'_P' if p else ''}"] = {
-                "us": us, "gbps": read_bytes(T, p) / (us * 1e-6) / 1e9}
+                        hc.hc_read_path(path, T, R, Pd, W["w_norm"], W["W_down"], W["W_up"], M,
+                                        *o, stream=stream)
+                with torch.cuda.stream(stream):
+                    enqueue()
+                    stream.synchronize()
+                    with torch.cuda.graph(gr, stream=stream):
+                        enqueue()
+                ms_t = timed(lambda k: gr.replay(), 40, 3)
+                us = 1e3 * ms_t / (40 * N_SETS)
+                out[f"T{T}{'_P' if p else ''}"] = {
+                    "us": us, "gbps": read_bytes(T, p) / (us * 1e-6) / 1e9}
+        return out
+
+    per_t = per_t_times(hc.HC_PATH_AUTO, (1, 4, 8))
+    per_t_paths = {name: {k: round(v["us"], 2) for k, v in per_t_times(path, range(1, 9), (True,)).items()}
+                   for name, path in (("two_kernels", hc.HC_PATH_DECODE),
+                                      ("one_kernel", hc.HC_PATH_DECODE_ONE_KERNEL))}
 
     # --- cold round: 96 reads of T=4 with P over the 48 sets ---
     a4 = synth.make_activations(600, 4, True)
@@ -421,6 +428,7 @@ def gpu_arm(args) -> None:
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": kernel_launches_per_step * args.steps,
         "decode_by_T": per_t,
+        "decode_paths_us_by_T_with_P": per_t_paths,
         "cold_round_96x_T4_P": cold_round,
         "prefill": prefill,
     }

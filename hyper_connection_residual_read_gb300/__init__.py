@@ -10,7 +10,7 @@ _BINDING = ("hc_read_init", "hc_read", "hc_read_path", "hc_read_check", "hc_read
             "hc_read_noalloc",
             "hc_read_shutdown", "hc_read_version", "strerror", "HcReadError", "load",
             "HC_PATH_AUTO", "HC_PATH_DECODE", "HC_PATH_PREFILL", "HC_PATH_PREFILL_UNFUSED",
-            "HC_PATH_DECODE_SPLIT",
+            "HC_PATH_DECODE_ONE_KERNEL",
             "EXPORTS", "LIB_PATH")
 
 

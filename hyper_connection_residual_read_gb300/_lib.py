@@ -27,7 +27,7 @@ HC_PATH_AUTO = 0
 HC_PATH_DECODE = 1
 HC_PATH_PREFILL = 2
 HC_PATH_PREFILL_UNFUSED = 3
-HC_PATH_DECODE_SPLIT = 4
+HC_PATH_DECODE_ONE_KERNEL = 4
 
 STREAMS, WIDTH, RANK = 4, 2560, 320
 

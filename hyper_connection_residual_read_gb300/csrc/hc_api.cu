@@ -102,17 +102,18 @@ int run(int path, const ReadArgs& a, cudaStream_t st) {
     int err;
     Ctx* c = current_ctx(&err);
     if (!c) return err;
-    if (path < HC_PATH_AUTO || path > HC_PATH_DECODE_SPLIT) return HC_ERR_ARG;
+    if (path < HC_PATH_AUTO || path > HC_PATH_DECODE_ONE_KERNEL) return HC_ERR_ARG;
     if (int e = validate(*c, a)) return e;
     if (a.T == 0) return HC_OK;
     if (path == HC_PATH_AUTO) path = a.T <= kAutoDecodeMaxT ? HC_PATH_DECODE : HC_PATH_PREFILL;
     cudaError_t ce;
     switch (path) {
         case HC_PATH_DECODE:
-            ce = c->fused_decode ? launch_decode_fused(*c, a, st) : launch_decode(*c, a, st);
-            break;
-        case HC_PATH_DECODE_SPLIT:
             ce = launch_decode(*c, a, st);
+            break;
+        case HC_PATH_DECODE_ONE_KERNEL:
+            if (!c->fused_decode) return HC_ERR_ARG;   // its clusters cannot all be resident here
+            ce = launch_decode_fused(*c, a, st);
             break;
         case HC_PATH_PREFILL:
             ce = launch_prefill(*c, a, true, st);

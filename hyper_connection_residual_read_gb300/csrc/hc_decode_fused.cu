@@ -15,10 +15,10 @@
 //    hyper-connection read on Arc A-series", Summary, change 4) and the 8 slices of
 //    a row block reduce through distributed shared memory in a fixed order (the
 //    page's change 1 does it with the last slice to finish).
-//  * Each cluster publishes its 16 rows of lo (fence, then one counter increment);
-//    every CTA waits, bounded by %globaltimer, until all 20 clusters have published,
-//    then reads lo and runs its up projection, gate and 4x4 mix. The last CTA to
-//    read lo resets the counters for the next call.
+//  * Each CTA publishes its 2 rows of lo with a release-add on a counter; every CTA
+//    waits, bounded by %globaltimer, until all 160 have published, then reads lo and
+//    runs its up projection, gate and 4x4 mix. The last CTA to read lo resets the
+//    counters for the next call.
 //
 // All CTAs are resident before any of them waits: a dependent launch cannot start
 // until every CTA of this grid has issued launch_dependents, and the previous
@@ -225,33 +225,45 @@ decode_fused_kernel(const float* __restrict__ R, const float* __restrict__ P,
     cluster.sync();
     if (tid < T * 2) {
         const int t = tid >> 1, j = 2 * sl + (tid & 1);
+        // all 16 remote loads first, then the arithmetic (each is a round trip)
+        float ssv[kDownSlices], pv[kDownSlices];
+#pragma unroll
+        for (int r = 0; r < kDownSlices; ++r) {
+            ssv[r] = *cluster.map_shared_rank(&ss_s[t], r);
+            pv[r] = *cluster.map_shared_rank(&part_s[t][j], r);
+        }
         float v = 0.f;
 #pragma unroll
         for (int st = 0; st < kStreams; ++st) {
-            const float* ssa = cluster.map_shared_rank(&ss_s[0], 2 * st);
-            const float* ssb = cluster.map_shared_rank(&ss_s[0], 2 * st + 1);
-            const float* pa = cluster.map_shared_rank(&part_s[0][0], 2 * st);
-            const float* pb = cluster.map_shared_rank(&part_s[0][0], 2 * st + 1);
-            const float ss = ssa[t] + ssb[t];
+            const float ss = ssv[2 * st] + ssv[2 * st + 1];
             const float rs = 1.0f / sqrtf(ss / (float)kWidth + eps);
-            const float d = pa[t * kDownRowsPerCta + j] + pb[t * kDownRowsPerCta + j];
+            const float d = pv[2 * st] + pv[2 * st + 1];
             v = fmaf(rs, d, v);
         }
         lo[t * kRank + rb * kDownRowsPerCta + j] = v;
-        __threadfence();
     }
-    cluster.sync();   // all 8 CTAs' lo rows stored and fenced; DSMEM reads done
-    if (tid == 0 && sl == 0) {
-        __threadfence();
-        atomicAdd(&sync[0], 1u);
+    // publish this CTA's rows: the CTA barrier orders the stores before thread 0's
+    // release-add at GPU scope. (No CTA leaves before every CTA has published, so the
+    // shared memory read above stays alive without a second cluster barrier.)
+    __syncthreads();
+    if (tid == 0)
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&sync[0]) : "memory");
+    // the gate needs R' of this lane's (token, stream, column): load it before waiting
+    const int up_cl = (warp & 7) * 2 + (lane >> 4), up_sp = (lane & 15) & 3;
+    float rp[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+        const size_t off = (size_t)t * kCols + up_sp * kWidth + cbase + up_cl;
+        rp[t] = R[off];
+        if (P != nullptr) rp[t] += P[off];
     }
 
     // 5. wait for every cluster's lo, then read it with R' and the mix
     if (tid == 0) {
         int ok = 1;
-        if (ld_acquire(&sync[0]) < (unsigned)kClusters) {
+        if (ld_acquire(&sync[0]) < (unsigned)kCtas) {
             const uint64_t t0 = gtimer();
-            while (ld_acquire(&sync[0]) < (unsigned)kClusters) {
+            while (ld_acquire(&sync[0]) < (unsigned)kCtas) {
                 if (gtimer() - t0 > kWaitNs) {
                     atomicOr(status, kStatusTimeout);
                     ok = 0;
@@ -306,13 +318,6 @@ decode_fused_kernel(const float* __restrict__ R, const float* __restrict__ P,
 #pragma unroll
             for (int i = 0; i < 5; ++i) wr[st][i] = src[i];
         }
-        float rp[T];
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-            const size_t off = (size_t)t * kCols + sp * kWidth + c;
-            rp[t] = R[off];
-            if (P != nullptr) rp[t] += P[off];
-        }
 #pragma unroll
         for (int t = 0; t < T; ++t) {
             const float4* l4 = reinterpret_cast<const float4*>(&lo_s[t][part * kPartLen]);
@@ -354,6 +359,9 @@ decode_fused_kernel(const float* __restrict__ R, const float* __restrict__ P,
             }
         }
     }
+    // no CTA leaves while a cluster peer might still read its shared memory (only
+    // possible on the timeout path; in the normal path every read is long done)
+    cluster.sync();
 }
 
 template <typename... KArgs, typename... Args>

@@ -86,10 +86,11 @@ enum hc_status {
  * tensor-core tile path above that; the others force one path (tests, bench). */
 enum hc_path {
     HC_PATH_AUTO = 0,
-    HC_PATH_DECODE = 1,          /* one kernel per 8 tokens: sliced down, lo exchange, up/gate/mix */
-    HC_PATH_PREFILL = 2,         /* tile down, fused up + gate + mix epilogue */
-    HC_PATH_PREFILL_UNFUSED = 3, /* tile down, up GEMM writing gated, then the mix */
-    HC_PATH_DECODE_SPLIT = 4     /* the decode read as two kernels (down; up/gate/mix) */
+    HC_PATH_DECODE = 1,            /* per 8 tokens: sliced down kernel, then up/gate/mix kernel */
+    HC_PATH_PREFILL = 2,           /* tile down, fused up + gate + mix epilogue */
+    HC_PATH_PREFILL_UNFUSED = 3,   /* tile down, up GEMM writing gated, then the mix */
+    HC_PATH_DECODE_ONE_KERNEL = 4  /* per 8 tokens: one kernel with an in-kernel lo exchange
+                                      (HC_ERR_ARG where its 160 CTAs cannot all be resident) */
 };
 
 /* Creates the context of `device` (makes it current), checks that it is sm_103,

@@ -20,7 +20,7 @@ from _hc import (EPS, MAX_TOKENS, TOL_F32, alloc_out, assert_matches_oracle, dev
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [None, hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_SPLIT]
+PATHS = [None, hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_ONE_KERNEL]
 
 
 @pytest.fixture(scope="module")
@@ -59,15 +59,15 @@ def test_verify_window_sweep(weights, T, with_P):
 
 
 @pytest.mark.parametrize("T", [9, 13, 16, 17, 31])
-@pytest.mark.parametrize("path", [hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_SPLIT])
+@pytest.mark.parametrize("path", [hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_ONE_KERNEL])
 def test_ragged_token_counts(weights, T, path):
     got, want = run_case(weights, T, True, 100 + T, path)
     assert_matches_oracle(got, want)
 
 
 @pytest.mark.parametrize("T", [1, 4, 8])
-def test_split_decode_path(weights, T):
-    got, want = run_case(weights, T, True, 300 + T, hc.HC_PATH_DECODE_SPLIT)
+def test_one_kernel_decode_path(weights, T):
+    got, want = run_case(weights, T, True, 300 + T, hc.HC_PATH_DECODE_ONE_KERNEL)
     assert_matches_oracle(got, want)
 
 
@@ -92,7 +92,7 @@ def test_pending_write_equals_preadded(weights):
         assert np.array_equal(p.view(np.uint8), q.view(np.uint8))
 
 
-@pytest.mark.parametrize("path", [hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_SPLIT])
+@pytest.mark.parametrize("path", [hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_ONE_KERNEL])
 def test_token_batch_invariance_decode(weights, path):
     """Token t's bits do not depend on the other tokens of the call."""
     w, W = weights

@@ -14,7 +14,8 @@ import torch
 import hyper_connection_residual_read_gb300 as hc
 from hyper_connection_residual_read_gb300 import synth
 
-from _hc import EPS, MAX_TOKENS, TOL_F32, alloc_out, dev_f32, dev_weights, gpu_read, rel_diff
+from _hc import (EPS, MAX_TOKENS, TOL_F32, alloc_out, assert_images_close, dev_f32,
+                 dev_weights, gpu_read, rel_diff)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,8 +34,10 @@ def test_noalloc_matches_hc_read_on_consecutive_calls():
         got = (o[0].cpu().numpy(), o[1].cpu().numpy().view(np.uint16),
                o[2].cpu().numpy().view(np.uint16))
         assert rel_diff(got[0], want[0]) <= TOL_F32
-        assert np.max(np.abs(got[1].astype(np.int32) - want[1].astype(np.int32))) <= 1
-        assert np.max(np.abs(got[2].astype(np.int32) - want[2].astype(np.int32))) <= 1
+        # same criterion as against the oracle: within 1 ulp, or within the fp32 band
+        delta = TOL_F32 * float(np.max(np.abs(want[0].astype(np.float64))))
+        assert_images_close(got[1], want[1], want[0], "bf16", delta)
+        assert_images_close(got[2], want[2], want[0], "fp16", delta)
 
 
 def test_noalloc_refuses_more_than_its_scratch_holds():
