@@ -24,7 +24,6 @@
 // Weights are loaded straight into registers with 16-byte streaming loads issued
 // before anything else, so a kernel's whole weight matrix is in flight at once.
 #include <cooperative_groups.h>
-#include <cuda_bf16.h>
 
 #include "hc_common.cuh"
 #include "hc_internal.h"
@@ -33,50 +32,40 @@ namespace hc {
 
 namespace {
 
-constexpr int kDownThreads = 320;   // 10 warps, 128 columns of the slice each
-constexpr int kUpThreads = 256;     // 8 warps: 4 M tiles x 2 K halves
-constexpr int kUpColsPerCta = 16;   // 2560 columns over 160 CTAs
-constexpr int kUpRows = kStreams * kUpColsPerCta;   // 64 W_up rows per CTA
-constexpr int kAStride = kDownSliceCols + 16;       // floats per token row of a (bank spread)
-constexpr int kWStride = kRank + 8;                 // bf16 per W_up row in shared memory
-constexpr int kLStride = kRank + 8;                 // bf16 per token row of a lo term
-constexpr int kUpSmem = kUpRows * kWStride * 2 + 3 * 8 * kLStride * 2;   // 57,728 B
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kDownThreads = 320;   // 10 warps: 2 row groups x 5 column groups
+constexpr int kDownColGroups = 5;   // 5 x 256 columns = 1280
+constexpr int kUpWarps = 4;         // 4 columns per warp, 16 per CTA
+constexpr int kUpThreads = 32 * kUpWarps;
 
-__device__ __forceinline__ uint64_t gtimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// mma.sync m16n8k16, bf16 inputs, fp32 accumulation: D += A (16x16) * B (16x8).
-// Fragments (g = lane / 4, q = lane % 4): a0 = A[g][2q..2q+1], a1 = A[g+8][2q..],
-// a2 = A[g][2q+8..], a3 = A[g+8][2q+8..]; b0 = B[2q..2q+1][g], b1 = B[2q+8..2q+9][g];
-// d0 = D[g][2q], d1 = D[g][2q+1], d2 = D[g+8][2q], d3 = D[g+8][2q+1].
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// x = hi + mid + lo with each term bf16 (round to nearest): 24 bits of x, so a
-// product with an exact bf16 weight loses nothing before the fp32 sum.
-__device__ __forceinline__ void split3(float x0, float x1, uint32_t (&t)[3]) {
-    float r0 = x0, r1 = x1;
+// Sum over the 32 lanes of eight per-lane values, one per row. On return the
+// lanes whose bits (4,3,2) equal the row's index hold that row's full sum:
+// row = (lane >> 2) & 7. Nine shuffles, fixed order.
+__device__ __forceinline__ float warp_reduce_8rows(const float (&v)[8], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float a[4];
 #pragma unroll
-    for (int i = 0; i < 3; ++i) {
-        const __nv_bfloat162 h = __floats2bfloat162_rn(r0, r1);
-        t[i] = *reinterpret_cast<const uint32_t*>(&h);
-        r0 -= __low2float(h);
-        r1 -= __high2float(h);
+    for (int i = 0; i < 4; ++i) {
+        float send = b4 ? v[i] : v[i + 4];
+        float keep = b4 ? v[i + 4] : v[i];
+        a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
     }
+    float b[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float send = b3 ? a[i] : a[i + 2];
+        float keep = b3 ? a[i + 2] : a[i];
+        b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float send = b2 ? b[0] : b[1];
+    float keep = b2 ? b[1] : b[0];
+    float c = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    c += __shfl_xor_sync(0xffffffffu, c, 2);
+    c += __shfl_xor_sync(0xffffffffu, c, 1);
+    return c;
 }
 
 template <int T>
-__global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kDownThreads, 2)
+__global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kDownThreads)
 down_slice_kernel(const float* __restrict__ R, const float* __restrict__ P,
                   const uint16_t* __restrict__ w_norm, const uint16_t* __restrict__ W_down,
                   float* __restrict__ lo, float eps) {
@@ -86,47 +75,47 @@ down_slice_kernel(const float* __restrict__ R, const float* __restrict__ P,
     const int s = sl >> 1;                     // stream of the slice
     const int c0 = (sl & 1) * kDownSliceCols;  // first column of the slice in the stream
     const int k0 = s * kWidth + c0;            // first column on the 10240 axis
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, q = lane & 3;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int rg = warp / kDownColGroups, cgp = warp % kDownColGroups;
+    const int j0 = rb * kDownRowsPerCta + rg * 8;
+    const int col = cgp * 256 + lane * 8;      // this lane's 8 columns within the slice
 
-    __shared__ __align__(16) float a_s[T][kAStride];
-    __shared__ float red_ss[kDownThreads / 32][T];
-    __shared__ float dred[kDownThreads / 32][kDownRowsPerCta][8];
-    __shared__ float part_s[T][kDownRowsPerCta];   // this slice's partial dots
-    __shared__ float ss_s[T];                      // this slice's sums of squares
-
-    // 1. weights first (layer parameters may be read before the previous kernel on
-    //    the stream has finished): the tensor-core A fragments of this warp's 128
-    //    columns, 8 k-steps x rows (g, g+8). The 16 K values of a step are taken in
-    //    the order that gives each thread 4 consecutive columns (8-byte loads); the
-    //    activations use the same order.
-    uint2 wa[8][2];
-    {
-        const uint16_t* r0 = W_down + (size_t)(rb * kDownRowsPerCta + g) * kCols + k0 + warp * 128 + 4 * q;
+    // 1. weights first (layer parameters may be read before the previous kernel
+    //    on the stream has finished): 8 rows x 8 columns, one 16-byte load per row
+    uint4 wv[8];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            wa[kk][0] = __ldg(reinterpret_cast<const uint2*>(r0 + kk * 16));
-            wa[kk][1] = __ldg(reinterpret_cast<const uint2*>(r0 + 8 * (size_t)kCols + kk * 16));
-        }
-    }
+    for (int r = 0; r < 8; ++r)
+        wv[r] = ldg_stream_v4(W_down + (size_t)(j0 + r) * kCols + k0 + col);
     const uint2 wn = *reinterpret_cast<const uint2*>(w_norm + k0 + 4 * tid);
     pdl_launch_dependents();
     pdl_wait();
 
-    // 2. activations a = R' * w_norm (fp32) and per-token sums of squares of R'
-    {
-        float4 xs[T];
+    // 2. activations a = R' * w_norm (fp32) and per-token sums of squares of R'.
+    //    Smem layout: a lane's 8 columns are stored as two float4 runs, 128 floats
+    //    apart, so that consecutive lanes read consecutive 16-byte words.
+    __shared__ float4 a_s[T][kDownSliceCols / 4];
+    __shared__ float red_ss[kDownThreads / 32][T];
+    __shared__ float red[T][kDownColGroups][kDownRowsPerCta];
+    __shared__ float part_s[T][kDownRowsPerCta];   // this slice's partial dots
+    __shared__ float ss_s[T];                      // this slice's sums of squares
+
+    float4 xs[T];
 #pragma unroll
-        for (int t = 0; t < T; ++t)
-            xs[t] = *reinterpret_cast<const float4*>(R + (size_t)t * kCols + k0 + 4 * tid);
-        if (P != nullptr) {
+    for (int t = 0; t < T; ++t)
+        xs[t] = *reinterpret_cast<const float4*>(R + (size_t)t * kCols + k0 + 4 * tid);
+    if (P != nullptr) {
 #pragma unroll
-            for (int t = 0; t < T; ++t) {
-                const float4 p = *reinterpret_cast<const float4*>(P + (size_t)t * kCols + k0 + 4 * tid);
-                xs[t].x += p.x; xs[t].y += p.y; xs[t].z += p.z; xs[t].w += p.w;
-            }
+        for (int t = 0; t < T; ++t) {
+            const float4 p = *reinterpret_cast<const float4*>(P + (size_t)t * kCols + k0 + 4 * tid);
+            xs[t].x += p.x; xs[t].y += p.y; xs[t].z += p.z; xs[t].w += p.w;
         }
-        const float w0 = bf16_lo(wn.x), w1 = bf16_hi(wn.x), w2 = bf16_lo(wn.y), w3 = bf16_hi(wn.y);
+    }
+    const float w0 = bf16_lo(wn.x), w1 = bf16_hi(wn.x), w2 = bf16_lo(wn.y), w3 = bf16_hi(wn.y);
+    {
+        const int c = 4 * tid;                       // first of this thread's 4 columns
+        const int scg = c >> 8, slane = (c & 255) >> 3, half = (c & 7) >> 2;
+        const int slot = scg * 64 + half * 32 + slane;   // float4 index
 #pragma unroll
         for (int t = 0; t < T; ++t) {
             const float4 x = xs[t];
@@ -134,8 +123,7 @@ down_slice_kernel(const float* __restrict__ R, const float* __restrict__ P,
             ss = fmaf(x.y, x.y, ss);
             ss = fmaf(x.z, x.z, ss);
             ss = fmaf(x.w, x.w, ss);
-            *reinterpret_cast<float4*>(&a_s[t][4 * tid]) =
-                make_float4(x.x * w0, x.y * w1, x.z * w2, x.w * w3);
+            a_s[t][slot] = make_float4(x.x * w0, x.y * w1, x.z * w2, x.w * w3);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
             if (lane == 0) red_ss[warp][t] = ss;
@@ -149,35 +137,43 @@ down_slice_kernel(const float* __restrict__ R, const float* __restrict__ P,
         ss_s[tid] = ss;
     }
 
-    // 3. partial dots on the tensor cores: D[16 rows][8 tokens] over this warp's 128
-    //    columns; B = a split into 3 bf16 terms (token g; tokens >= T are zero), one
-    //    accumulator per term so the three MMA chains are independent
-    {
-        float dt[3][4] = {};
+    // 3. partial dots of 8 rows over this lane's 8 columns, reduced over the warp
+    float wf[8][8];
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (g < T) x = *reinterpret_cast<const float4*>(&a_s[g < T ? g : 0][warp * 128 + kk * 16 + 4 * q]);
-            uint32_t b0[3], b1[3];
-            split3(x.x, x.y, b0);
-            split3(x.z, x.w, b1);
-            const uint32_t a0 = wa[kk][0].x, a2 = wa[kk][0].y, a1 = wa[kk][1].x, a3 = wa[kk][1].y;
+    for (int r = 0; r < 8; ++r) {
+        wf[r][0] = bf16_lo(wv[r].x); wf[r][1] = bf16_hi(wv[r].x);
+        wf[r][2] = bf16_lo(wv[r].y); wf[r][3] = bf16_hi(wv[r].y);
+        wf[r][4] = bf16_lo(wv[r].z); wf[r][5] = bf16_hi(wv[r].z);
+        wf[r][6] = bf16_lo(wv[r].w); wf[r][7] = bf16_hi(wv[r].w);
+    }
 #pragma unroll
-            for (int term = 0; term < 3; ++term) mma_bf16(dt[term], a0, a1, a2, a3, b0[term], b1[term]);
+    for (int t = 0; t < T; ++t) {
+        const float4 x0 = a_s[t][cgp * 64 + lane];
+        const float4 x1 = a_s[t][cgp * 64 + 32 + lane];
+        float acc[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            float v = wf[r][0] * x0.x;
+            v = fmaf(wf[r][1], x0.y, v);
+            v = fmaf(wf[r][2], x0.z, v);
+            v = fmaf(wf[r][3], x0.w, v);
+            v = fmaf(wf[r][4], x1.x, v);
+            v = fmaf(wf[r][5], x1.y, v);
+            v = fmaf(wf[r][6], x1.z, v);
+            v = fmaf(wf[r][7], x1.w, v);
+            acc[r] = v;
         }
-        dred[warp][g][2 * q] = (dt[0][0] + dt[1][0]) + dt[2][0];
-        dred[warp][g][2 * q + 1] = (dt[0][1] + dt[1][1]) + dt[2][1];
-        dred[warp][g + 8][2 * q] = (dt[0][2] + dt[1][2]) + dt[2][2];
-        dred[warp][g + 8][2 * q + 1] = (dt[0][3] + dt[1][3]) + dt[2][3];
+        const float sum = warp_reduce_8rows(acc, lane);
+        if ((lane & 3) == 0) red[t][cgp][rg * 8 + ((lane >> 2) & 7)] = sum;
     }
     __syncthreads();
 
-    // 4. this slice's partial for its 16 rows, the 10 warps summed in order
+    // 4. this slice's partial for its 16 rows, column groups summed in order
     if (tid < T * kDownRowsPerCta) {
         const int t = tid / kDownRowsPerCta, j = tid % kDownRowsPerCta;
-        float v = dred[0][j][t];
+        float v = red[t][0][j];
 #pragma unroll
-        for (int w = 1; w < kDownThreads / 32; ++w) v += dred[w][j][t];
+        for (int g = 1; g < kDownColGroups; ++g) v += red[t][g][j];
         part_s[t][j] = v;
     }
 
@@ -208,175 +204,110 @@ down_slice_kernel(const float* __restrict__ R, const float* __restrict__ P,
     cluster.sync();   // keep this CTA's shared memory alive until every reader is done
 }
 
+// lo in shared memory: each token's 320 values as 8 parts of 40, padded to 44
+// floats so that the 8 parts a warp reads at once fall in distinct banks.
+constexpr int kLoPart = 44;
+
 template <int T>
 __global__ void __launch_bounds__(kUpThreads)
 up_mix_kernel(const float* __restrict__ R, const float* __restrict__ P,
               const uint16_t* __restrict__ W_up, const float* __restrict__ lo,
               const float* __restrict__ Rmix, float* __restrict__ out_f32,
-              uint16_t* __restrict__ out_bf16, uint16_t* __restrict__ out_fp16,
-              int* __restrict__ status) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, q = lane & 3;
-    const int cbase = blockIdx.x * kUpColsPerCta;   // first output column of this CTA
+              uint16_t* __restrict__ out_bf16, uint16_t* __restrict__ out_fp16) {
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int cc = lane >> 3;                  // which of the warp's 4 columns
+    const int part = lane & 7;                 // which 40 of the 320 inputs
+    const int c = (blockIdx.x * kUpWarps + warp) * 4 + cc;   // output column 0..2559
+    const int sp = part & 3;                   // stream gated by this lane (lanes 0..3)
 
-    // dynamic shared memory: the 64 W_up rows (padded; shared row 4 * column + stream,
-    // so the 16 rows of an M tile are consecutive) and the 3 bf16 terms of lo
-    extern __shared__ __align__(16) uint8_t dsm[];
-    uint16_t* wup_s = reinterpret_cast<uint16_t*>(dsm);
-    uint16_t* lob_s = reinterpret_cast<uint16_t*>(dsm + kUpRows * kWStride * 2);
-    __shared__ __align__(16) float m_s[T][16];
-    __shared__ float ured[4][32][4];
-    __shared__ __align__(8) uint64_t wbar;
-
-    // 1. W_up rows by the bulk-copy engine (layer parameters: before the wait)
-    const uint32_t wbar_a = static_cast<uint32_t>(__cvta_generic_to_shared(&wbar));
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(wbar_a));
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(wbar_a),
-                     "r"((uint32_t)(kUpRows * kRank * 2))
-                     : "memory");
-    }
-    __syncthreads();
-    if (warp == 0) {
-        for (int r = lane; r < kUpRows; r += 32) {
-            const int st = r / kUpColsPerCta, cl = r % kUpColsPerCta;
-            const uint16_t* src = W_up + (size_t)(st * kWidth + cbase + cl) * kRank;
-            const uint32_t dst = static_cast<uint32_t>(
-                __cvta_generic_to_shared(wup_s + (cl * kStreams + st) * kWStride));
-            asm volatile(
-                "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-                    "r"(dst), "l"(src), "r"((uint32_t)(kRank * 2)), "r"(wbar_a)
-                : "memory");
-        }
+    // 1. the 4 up rows of column c (one per stream), this lane's 40 inputs each
+    uint4 wv[kStreams][5];
+#pragma unroll
+    for (int st = 0; st < kStreams; ++st) {
+        const uint16_t* wrow = W_up + (size_t)(st * kWidth + c) * kRank + part * 40;
+#pragma unroll
+        for (int q = 0; q < 5; ++q) wv[st][q] = ldg_stream_v4(wrow + 8 * q);
     }
     pdl_launch_dependents();
     pdl_wait();
 
-    // warp w owns M tile mt = w / 2 (columns 4mt..4mt+3 of the CTA; tile row
-    // m = 4 * column + stream) and K half kh = w % 2. Thread rows g and g+8 of the
-    // tile: stream g % 4, columns 4mt + g/4 and 4mt + 2 + g/4.
-    const int mt = warp >> 1, kh = warp & 1;
-    const int us = g & 3, ucA = 4 * mt + (g >> 2), ucB = ucA + 2;
-    // 2. R' for the gate at (tokens 2q and 2q+1, stream us, columns ucA and ucB)
-    float rp[2][2];
+    // 2. everything the token loop needs, requested at once: lo, R' and the mix
+    __shared__ __align__(16) float lo_s[T][8][kLoPart];
+    __shared__ __align__(16) float m_s[T][16];
+    float rp[T];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int t = 2 * q + i;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            float v = 0.f;
-            if (t < T) {
-                const size_t off = (size_t)t * kCols + us * kWidth + cbase + (cc ? ucB : ucA);
-                v = R[off];
-                if (P != nullptr) v += P[off];
-            }
-            rp[i][cc] = v;
-        }
+    for (int t = 0; t < T; ++t) {
+        const size_t off = (size_t)t * kCols + sp * kWidth + c;
+        rp[t] = R[off];
     }
-    // lo as 3 bf16 terms (tokens >= T are zero) and the mix matrices
-    for (int e = tid; e < 8 * kRank / 2; e += kUpThreads) {
-        const int t = e / (kRank / 2), k = 2 * (e % (kRank / 2));
-        float2 v = make_float2(0.f, 0.f);
-        if (t < T) v = *reinterpret_cast<const float2*>(lo + t * kRank + k);
-        uint32_t terms[3];
-        split3(v.x, v.y, terms);
+    if (P != nullptr) {
 #pragma unroll
-        for (int term = 0; term < 3; ++term)
-            *reinterpret_cast<uint32_t*>(lob_s + (term * 8 + t) * kLStride + k) = terms[term];
+        for (int t = 0; t < T; ++t) rp[t] += P[(size_t)t * kCols + sp * kWidth + c];
     }
-    if (tid < T * 4) reinterpret_cast<float4*>(&m_s[0][0])[tid] = reinterpret_cast<const float4*>(Rmix)[tid];
+    for (int e = tid; e < T * kRank / 4; e += kUpThreads) {
+        const int t = e / (kRank / 4), j = 4 * (e % (kRank / 4));
+        const float4 v = *reinterpret_cast<const float4*>(lo + (size_t)t * kRank + j);
+        *reinterpret_cast<float4*>(&lo_s[t][j / 40][j % 40]) = v;
+    }
+    if (tid < T * 4) reinterpret_cast<float4*>(&m_s[0][0])[tid] =
+        reinterpret_cast<const float4*>(Rmix)[tid];
     __syncthreads();
 
-    // 3. the W_up rows must have arrived (bounded wait)
-    {
-        uint32_t done = 0;
-        const uint64_t t0 = gtimer();
-        while (true) {
-            asm volatile(
-                "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0; "
-                "selp.u32 %0, 1, 0, p; }"
-                : "=r"(done)
-                : "r"(wbar_a)
-                : "memory");
-            if (done) break;
-            if (gtimer() - t0 > kWaitNs) {
-                atomicOr(status, kStatusTimeout);
-                break;
-            }
-        }
-    }
-
-    // 4. u = W_up . lo on the tensor cores over this warp's K half (10 k-steps), A by
-    //    ldmatrix from the W_up rows, B = the lo terms; one accumulator per term
-    float d[4];
-    {
-        const uint32_t arow = static_cast<uint32_t>(__cvta_generic_to_shared(
-            wup_s + (16 * mt + (lane & 15)) * kWStride + (lane >> 4) * 8));
-        float dt[3][4] = {};
 #pragma unroll
-        for (int ks = 0; ks < 10; ++ks) {
-            const int kb = kh * 160 + ks * 16;
-            uint32_t a0, a1, a2, a3;
-            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
-                         : "r"(arow + kb * 2));
+    for (int t = 0; t < T; ++t) {
+        const float4* l4 = reinterpret_cast<const float4*>(&lo_s[t][part][0]);
+        float acc[kStreams] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int term = 0; term < 3; ++term) {
-                const uint16_t* bt = lob_s + (term * 8 + g) * kLStride + kb + 2 * q;
-                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(bt);
-                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(bt + 8);
-                mma_bf16(dt[term], a0, a1, a2, a3, b0, b1);
+        for (int q = 0; q < 5; ++q) {
+            const float4 xa = l4[2 * q], xb = l4[2 * q + 1];
+#pragma unroll
+            for (int st = 0; st < kStreams; ++st) {
+                const uint4 w = wv[st][q];
+                float v = acc[st];
+                v = fmaf(bf16_lo(w.x), xa.x, v);
+                v = fmaf(bf16_hi(w.x), xa.y, v);
+                v = fmaf(bf16_lo(w.y), xa.z, v);
+                v = fmaf(bf16_hi(w.y), xa.w, v);
+                v = fmaf(bf16_lo(w.z), xb.x, v);
+                v = fmaf(bf16_hi(w.z), xb.y, v);
+                v = fmaf(bf16_lo(w.w), xb.z, v);
+                v = fmaf(bf16_hi(w.w), xb.w, v);
+                acc[st] = v;
             }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d[i] = (dt[0][i] + dt[1][i]) + dt[2][i];
-    }
-    // the two K halves of an M tile, in order (half 0 + half 1)
-    if (kh == 1) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ured[mt][lane][i] = d[i];
-    }
-    __syncthreads();
-    if (kh == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) d[i] += ured[mt][lane][i];
-        // 5. gate, then mix across the 4 stream lanes of a column (lane stride 4)
-        float gv[2][2];
-        gv[0][0] = gate_value(d[0], rp[0][0]);   // token 2q,   column A
-        gv[1][0] = gate_value(d[1], rp[1][0]);   // token 2q+1, column A
-        gv[0][1] = gate_value(d[2], rp[0][1]);   // token 2q,   column B
-        gv[1][1] = gate_value(d[3], rp[1][1]);   // token 2q+1, column B
-        const int base = (lane & ~15) | q;       // lane of stream 0 for this (column, q)
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const float g0 = __shfl_sync(0xffffffffu, gv[i][cc], base);
-                const float g1 = __shfl_sync(0xffffffffu, gv[i][cc], base + 4);
-                const float g2 = __shfl_sync(0xffffffffu, gv[i][cc], base + 8);
-                const float g3 = __shfl_sync(0xffffffffu, gv[i][cc], base + 12);
-                const int t = 2 * q + i;
-                if (t < T) {
-                    const float m = mix_row(&m_s[t][us * 4], g0, g1, g2, g3);
-                    const size_t off = (size_t)t * kCols + us * kWidth + cbase + (cc ? ucB : ucA);
-                    out_f32[off] = m;
-                    out_bf16[off] = to_bf16_bits(m);
-                    out_fp16[off] = to_fp16_bits(m);
-                }
-            }
+        for (int st = 0; st < kStreams; ++st) {
+            acc[st] += __shfl_xor_sync(0xffffffffu, acc[st], 4);
+            acc[st] += __shfl_xor_sync(0xffffffffu, acc[st], 2);
+            acc[st] += __shfl_xor_sync(0xffffffffu, acc[st], 1);
+        }
+        // lane `part` (0..3) of the column group gates stream `part`
+        const float u = sp == 0 ? acc[0] : sp == 1 ? acc[1] : sp == 2 ? acc[2] : acc[3];
+        const float g = gate_value(u, rp[t]);
+        const int base = lane & ~7;
+        const float g0 = __shfl_sync(0xffffffffu, g, base + 0);
+        const float g1 = __shfl_sync(0xffffffffu, g, base + 1);
+        const float g2 = __shfl_sync(0xffffffffu, g, base + 2);
+        const float g3 = __shfl_sync(0xffffffffu, g, base + 3);
+        if (part < 4) {
+            const float m = mix_row(&m_s[t][part * 4], g0, g1, g2, g3);
+            const size_t off = (size_t)t * kCols + part * kWidth + c;
+            out_f32[off] = m;
+            out_bf16[off] = to_bf16_bits(m);
+            out_fp16[off] = to_fp16_bits(m);
         }
     }
 }
 
 // Launch with programmatic stream serialisation (see pdl_wait).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem, cudaStream_t st,
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
                        Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -386,33 +317,18 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// The up kernel's dynamic shared memory size is set once per device and T.
-template <int T>
-cudaError_t ensure_attrs() {
-    static bool done[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (done[dev]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(up_mix_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kUpSmem);
-    if (e == cudaSuccess) done[dev] = true;
-    return e;
-}
-
 template <int T>
 cudaError_t launch_chunk(const Ctx& ctx, const ReadArgs& a, int t0, cudaStream_t st) {
-    cudaError_t e = ensure_attrs<T>();
-    if (e != cudaSuccess) return e;
     const size_t off = (size_t)t0 * kCols;
     const float* R = a.R + off;
     const float* P = a.P ? a.P + off : nullptr;
     float* lo = ctx.s.lo + (size_t)t0 * kRank;
-    e = launch_pdl(down_slice_kernel<T>, dim3(kDownSlices, kDownRowBlocks), dim3(kDownThreads), 0,
-                   st, R, P, a.w_norm, a.W_down, lo, ctx.eps);
+    cudaError_t e = launch_pdl(down_slice_kernel<T>, dim3(kDownSlices, kDownRowBlocks),
+                               dim3(kDownThreads), st, R, P, a.w_norm, a.W_down, lo, ctx.eps);
     if (e != cudaSuccess) return e;
-    return launch_pdl(up_mix_kernel<T>, dim3(kWidth / kUpColsPerCta), dim3(kUpThreads), kUpSmem, st,
-                      R, P, a.W_up, (const float*)lo, a.Rmix + (size_t)t0 * 16, a.out_f32 + off,
-                      a.out_bf16 + off, a.out_fp16 + off, ctx.s.status);
+    return launch_pdl(up_mix_kernel<T>, dim3(kWidth / (4 * kUpWarps)), dim3(kUpThreads), st,
+                      R, P, a.W_up, (const float*)lo, a.Rmix + (size_t)t0 * 16,
+                      a.out_f32 + off, a.out_bf16 + off, a.out_fp16 + off);
 }
 
 }  // namespace
