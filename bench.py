@@ -389,8 +389,11 @@ def gpu_arm(args) -> None:
     ms_e = timed(e2e_step, e2e_steps, min(args.warmup, 5) + 3)
     e2e_us = 1e3 * ms_e / (e2e_steps * reads_per_step * world)
 
-    # --- prefill chunks (one call per chunk) ---
+    # --- prefill chunks: the whole read, and the fused up + gate + mix stage alone
+    #     (re-run on the chunk's lo) next to the unfused pair (up GEMM writing gated,
+    #     then the mix) in the same build ---
     prefill = {}
+    peaks = measured_peaks()
     W0 = sets[0]
     for T in (8192, 32768):
         c = synth.make_prefill_chunk(104 if T == 32768 else 100, T)
@@ -401,14 +404,26 @@ def gpu_arm(args) -> None:
         def chunk(k):
             hc.hc_read(T, R, None, W0["w_norm"], W0["W_down"], W0["W_up"], M, *o,
                        stream=stream)
-        reps = 5 if T == 8192 else 3
-        ms_p = timed(chunk, reps, 2)
-        ms1 = ms_p / reps
-        prefill[f"T{T}"] = {"ms": ms1, "tokens_per_s": T / (ms1 * 1e-3),
-                            "gbps": prefill_read_bytes(T) / (ms1 * 1e-3) / 1e9}
+
+        def upmix_fused(k):
+            hc.hc_read_upmix(True, T, R, None, M, *o, stream=stream)
+
+        def upmix_pair(k):
+            hc.hc_read_upmix(False, T, R, None, M, *o, stream=stream)
+
+        reps = 10 if T == 8192 else 4
+        ms_read = timed(chunk, reps, 3) / reps          # leaves this chunk's lo in scratch
+        ms_fused = timed(upmix_fused, reps, 3) / reps
+        ms_pair = timed(upmix_pair, reps, 3) / reps
+        fused_gbps = prefill_upmix_bytes(T) / (ms_fused * 1e-3) / 1e9
+        prefill[f"T{T}"] = {
+            "read_ms": ms_read, "tokens_per_s": T / (ms_read * 1e-3),
+            "read_gbps": prefill_read_bytes(T) / (ms_read * 1e-3) / 1e9,
+            "upmix_fused_ms": ms_fused, "upmix_fused_gbps": fused_gbps,
+            "upmix_fused_frac": fused_gbps / peaks["hbm_gbs"],
+            "upmix_unfused_pair_ms": ms_pair, "fused_speedup": ms_pair / ms_fused}
         del R, M, o
 
-    peaks = measured_peaks()
     achieved = step_bytes / (ms / args.steps * 1e-3) / 1e9
     traffic = NCU_TRAFFIC_PER_READ
     kernel_launches_per_step = sum(2 * ((T + 7) // 8) for T, _ in SWEEP)

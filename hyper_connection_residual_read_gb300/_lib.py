@@ -33,7 +33,8 @@ STREAMS, WIDTH, RANK = 4, 2560, 320
 
 # every symbol include/hc_read.h declares
 EXPORTS = ("hc_read_init", "hc_read", "hc_read_path", "hc_read_check", "hc_read_status",
-           "hc_read_strerror", "hc_read_shutdown", "hc_read_version", "hc_read_noalloc")
+           "hc_read_strerror", "hc_read_shutdown", "hc_read_version", "hc_read_noalloc",
+           "hc_read_upmix")
 
 
 class HcReadError(RuntimeError):
@@ -93,6 +94,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_read_version.restype = i32
     lib.hc_read_noalloc.argtypes = [i32] + [vp] * 9 + [ctypes.c_float, vp]
     lib.hc_read_noalloc.restype = i32
+    lib.hc_read_upmix.argtypes = [i32, i32] + [vp] * 7
+    lib.hc_read_upmix.restype = i32
     _lib = lib
     return lib
 
@@ -156,6 +159,13 @@ def hc_read_noalloc(tokens, R, P, w_norm, W_down, W_up, Rmix, out_f32, out_bf16,
     _check("hc_read_noalloc", load().hc_read_noalloc(
         tokens, _ptr(R), _ptr(P), _ptr(w_norm), _ptr(W_down), _ptr(W_up), _ptr(Rmix),
         _ptr(out_f32), _ptr(out_bf16), _ptr(out_fp16), eps, _stream(stream)))
+
+
+def hc_read_upmix(fused, tokens, R, P, Rmix, out_f32, out_bf16, out_fp16, stream=None) -> None:
+    """Re-runs the up projection + gate + mix stage of the last tile-path call."""
+    _check("hc_read_upmix", load().hc_read_upmix(
+        int(bool(fused)), tokens, _ptr(R), _ptr(P), _ptr(Rmix), _ptr(out_f32), _ptr(out_bf16),
+        _ptr(out_fp16), _stream(stream)))
 
 
 def hc_read_check(max_tokens: int = 8, seed: int = 0) -> tuple[int, dict]:

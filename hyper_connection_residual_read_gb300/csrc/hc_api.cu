@@ -286,6 +286,30 @@ extern "C" int hc_read(int tokens, const float* R, const float* P, const uint16_
                         out_bf16, out_fp16, stream);
 }
 
+extern "C" int hc_read_upmix(int fused, int tokens, const float* R, const float* P,
+                             const float* Rmix, float* out_f32, uint16_t* out_bf16,
+                             uint16_t* out_fp16, void* stream) {
+    int err;
+    Ctx* c = current_ctx(&err);
+    if (!c) return err;
+    // the weights are not used by this stage: validate against harmless stand-ins
+    ReadArgs a{tokens, R, P, reinterpret_cast<const uint16_t*>(c->wd16),
+               reinterpret_cast<const uint16_t*>(c->wd16), reinterpret_cast<const uint16_t*>(c->wu16),
+               Rmix, out_f32, out_bf16, out_fp16};
+    if (int e = validate(*c, a)) return e;
+    if (tokens == 0) return HC_OK;
+    if (!fused && c->gated == nullptr) {
+        if (cudaMalloc(&c->gated, sizeof(float) * (size_t)c->max_tokens * kCols) != cudaSuccess) {
+            cudaGetLastError();
+            c->gated = nullptr;
+            return HC_ERR_NOMEM;
+        }
+    }
+    return launch_prefill_upmix(*c, a, fused != 0, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? HC_OK
+               : HC_ERR_CUDA;
+}
+
 extern "C" int hc_read_status(void* stream) {
     int err;
     Ctx* c = current_ctx(&err);

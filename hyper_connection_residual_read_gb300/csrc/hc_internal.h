@@ -81,5 +81,9 @@ cudaError_t launch_decode_fused(const Ctx& ctx, const ReadArgs& a, cudaStream_t 
 // Prefill (tensor-core tile) path: TMA maps and kernel attributes, then the launch.
 cudaError_t prefill_setup(Ctx& ctx);
 cudaError_t launch_prefill(const Ctx& ctx, const ReadArgs& a, bool fused, cudaStream_t st);
+// The two halves of the tile path: weights to fp16, down GEMM and lo split; then the
+// up GEMM with its gate + mix epilogue (fused) or writing gated + the mix (unfused).
+cudaError_t launch_prefill_down(const Ctx& ctx, const ReadArgs& a, cudaStream_t st);
+cudaError_t launch_prefill_upmix(const Ctx& ctx, const ReadArgs& a, bool fused, cudaStream_t st);
 
 }  // namespace hc

@@ -701,7 +701,7 @@ cudaError_t prefill_setup(Ctx& c) {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kUpSmem);
 }
 
-cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, bool fused, cudaStream_t st) {
+cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, cudaStream_t st) {
     const int n8 = kRank * kCols / 8;
     convert_weights_kernel<<<2 * c.sm_count, 512, 0, st>>>(a.W_down, a.W_up, c.wd16, c.wu16, n8);
     const int n_tt = (a.T + kTileM - 1) / kTileM;
@@ -713,6 +713,11 @@ cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, bool fused, cudaStre
     const int rgrid = (n4 + 255) / 256 < 8 * c.sm_count ? (n4 + 255) / 256 : 8 * c.sm_count;
     lo_split_kernel<<<rgrid, 256, 0, st>>>(c.partials, c.ssq, c.lo16, a.T, c.max_tokens, c.eps,
                                            c.s.status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, bool fused, cudaStream_t st) {
+    const int n_tt = (a.T + kTileM - 1) / kTileM;
     const int up_tiles = n_tt * kUpColTiles;
     const int up_grid = up_tiles < c.sm_count ? up_tiles : c.sm_count;
     EpiMaps em;
@@ -745,6 +750,12 @@ cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, bool fused, cudaStre
                                                 a.T);
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, bool fused, cudaStream_t st) {
+    cudaError_t e = launch_prefill_down(c, a, st);
+    if (e != cudaSuccess) return e;
+    return launch_prefill_upmix(c, a, fused, st);
 }
 
 }  // namespace hc

@@ -119,6 +119,18 @@ int hc_read_path(int path, int tokens,
                  float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
                  void* stream);
 
+/* Runs again only the second half of the tile path for the tokens of the most
+ * recent HC_PATH_PREFILL / HC_PATH_PREFILL_UNFUSED call on this context: the up
+ * projection on the lo that call left in the context's scratch (and the fp16 copy
+ * of its W_up), with the gate and the 4x4 mix, fused into the GEMM's epilogue
+ * (fused != 0) or as the unfused pair. R, P and Rmix must be that call's (or
+ * equal) tensors. Stage timing and the fused-versus-unfused comparison use it;
+ * a read needs only hc_read. Same argument checks and errors as hc_read. */
+int hc_read_upmix(int fused, int tokens,
+                  const float* R, const float* P, const float* Rmix,
+                  float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
+                  void* stream);
+
 /* Result of the once-per-device self check. */
 typedef struct hc_check_report {
     int device;

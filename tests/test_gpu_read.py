@@ -250,6 +250,24 @@ def test_prefill_fused_equals_unfused_bitwise(weights):
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
 
 
+def test_upmix_stage_rerun_matches_the_read(weights):
+    """The up + gate + mix stage run again on the read's lo gives the read's bits,
+    fused and unfused."""
+    w, W = weights
+    T = 260
+    a = synth.make_activations(14, T, True)
+    R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+    ref = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL)
+    for fused in (True, False):
+        o = alloc_out(T)
+        hc.hc_read_upmix(fused, T, R, P, M, *o)
+        torch.cuda.synchronize()
+        got = (o[0].cpu().numpy(), o[1].cpu().numpy().view(np.uint16),
+               o[2].cpu().numpy().view(np.uint16))
+        for x, y in zip(ref, got):
+            assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
 def test_prefill_bitwise_repeatable_and_pending_write(weights):
     w, W = weights
     T = 260
