@@ -39,10 +39,12 @@ SWEEP = [(T, p) for T in range(1, 9) for p in (False, True)]      # 16 reads per
 N_SETS = 48
 EPS = float(np.float32(1e-6))
 
-# DRAM bytes per read measured by ncu for the decode kernels (sum of both kernels,
-# one 4-token read with a pending write); None until a capture of the current
-# kernels exists.
-NCU_TRAFFIC_PER_READ = None
+# DRAM bytes (read + write) that ncu counted for one 4-token read with a pending
+# write, both decode kernels together (down_slice_kernel<4> 6,924,058 B,
+# up_mix_kernel<4> 6,910,490 B; 48 rotated weight sets, so the weights come from
+# DRAM). The sweep's traffic is taken as its algorithmic bytes times the ratio of
+# this figure to the same read's algorithmic bytes.
+NCU_TRAFFIC_T4_P = 13834547
 
 
 def read_bytes(T: int, with_P: bool) -> int:
@@ -425,7 +427,7 @@ def gpu_arm(args) -> None:
         del R, M, o
 
     achieved = step_bytes / (ms / args.steps * 1e-3) / 1e9
-    traffic = NCU_TRAFFIC_PER_READ
+    traffic = step_bytes * NCU_TRAFFIC_T4_P / read_bytes(4, True)
     kernel_launches_per_step = sum(2 * ((T + 7) // 8) for T, _ in SWEEP)
 
     line = {
@@ -436,6 +438,8 @@ def gpu_arm(args) -> None:
         "roofline": {"bound": "hbm", "kernel": "decode read (down_slice + up_mix kernels)",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "traffic_basis": "ncu DRAM bytes of one T=4 read with P, scaled to the "
+                                      "sweep by algorithmic bytes",
                      "peak_source": peaks["source"],
                      "bytes_per_step": step_bytes},
         "clocks": clocks,
