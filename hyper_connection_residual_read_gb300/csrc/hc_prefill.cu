@@ -64,22 +64,20 @@ constexpr int kUpBBytes = kUpN * kBK * 2;         // 32 KB
 constexpr int kUpStageBytes = 2 * kTileBytes16 + kUpBBytes;
 constexpr int kUpKBlocks = kRank / kBK;           // 5
 constexpr int kUpColTiles = kWidth / kUpCols;     // 40
-constexpr int kUpEpiWarps = 4;                    // one per TMEM lane quarter (32 tokens)
+// Eight epilogue warps: two per TMEM lane quarter (32 tokens), one for each half of
+// the tile's steps. The epilogue takes its tile in steps of 8 columns; a dedicated
+// warp streams the R (and P) tiles of those steps, 128 tokens x 8 columns x 4
+// streams, through a ring of 16 KB slots ahead of the epilogue warps. Each lane
+// owns one token row and writes it with 32-byte stores: 8 fp32 columns of a
+// stream per step, and 16 columns of each 16-bit image per pair of steps, so
+// every store fills whole DRAM sectors and no output passes through shared memory.
+constexpr int kUpEpiWarps = 8;
 constexpr int kUpThreads = 96 + 32 * kUpEpiWarps; // operand TMA, MMA, R TMA, epilogue warps
-// The epilogue takes its tile in steps of 8 columns. A dedicated warp streams the R
-// (and P) tiles of those steps, 128 tokens x 8 columns x 4 streams, through a ring
-// of 16 KB slots ahead of the epilogue warps. Each epilogue warp stages its outputs
-// for TMA tile stores: fp32 per step (32-byte rows), bf16 and fp16 per two steps
-// (32-byte rows as well, so every row written is a whole DRAM sector).
 constexpr int kEpiCols = 8;
 constexpr int kEpiRows = 32;
 constexpr int kRSlot = kStreams * kTileM * kEpiCols * 4;        // 16 KB
-constexpr int kRSlots = 3;
-constexpr int kEpiF32 = kStreams * kEpiRows * kEpiCols * 4;     // 4 KB
-constexpr int kEpi16 = kStreams * kEpiRows * 2 * kEpiCols * 2;  // 4 KB (16 columns)
-constexpr int kEpiWarpBytes = kEpiF32 + 2 * kEpi16;             // 12 KB
-constexpr int kUpSmem = kUpStages * kUpStageBytes + kRSlots * kRSlot +
-                        kUpEpiWarps * kEpiWarpBytes + 1024;
+constexpr int kRSlots = 6;
+constexpr int kUpSmem = kUpStages * kUpStageBytes + kRSlots * kRSlot + 1024;
 
 constexpr int kStatusRange = kStatusRangeBit;
 
@@ -356,14 +354,31 @@ __global__ void lo_split_kernel(const float* __restrict__ partials, const float*
 // so every transfer is a whole tile of 32-byte rows instead of scattered words.
 // ---------------------------------------------------------------------------
 struct EpiMaps {
-    CUtensorMap R, P, out, out_bf16, out_fp16;
+    CUtensorMap R, P;
 };
+
+// 32-byte global accesses (one whole DRAM sector per lane).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 template <bool kFused>
 __global__ void __launch_bounds__(kUpThreads, 1)
 upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtensorMap tm_lo,
                   const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ EpiMaps em,
-                  int has_P, int T, int* __restrict__ status) {
+                  float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16,
+                  uint16_t* __restrict__ out_fp16, int has_P, int T, int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[kUpStages], empty_bar[kUpStages];
@@ -387,9 +402,10 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 32 * kUpEpiWarps);
         }
+        // each step is taken by one group of four epilogue warps
         for (int i = 0; i < kRSlots; ++i) {
             mbar_init(&r_full[i], 1);
-            mbar_init(&r_empty[i], kUpEpiWarps);
+            mbar_init(&r_empty[i], 4);
         }
         abort_flag = 0;
         fence_barrier_init();
@@ -403,7 +419,6 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
     auto sA = [&](int slot, int term) { return smem + slot * kUpStageBytes + term * kTileBytes16; };
     auto sB = [&](int slot) { return smem + slot * kUpStageBytes + 2 * kTileBytes16; };
     uint8_t* rring = smem + kUpStages * kUpStageBytes;
-    uint8_t* ostage = rring + kRSlots * kRSlot;
 
     if (warp == 0) {
         // operand producer: lo terms and W_up rows, K blocks of 64
@@ -455,7 +470,8 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
             }
         }
     } else if (warp == 2) {
-        // R (and P) producer: one slot per step (two with P), 4 streams per slot
+        // R (and P) producer: one slot per step (two with P), 4 streams per slot,
+        // in step order
         if (lane == 0) {
             int u = 0;   // slot uses
             for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
@@ -476,21 +492,19 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
             }
         }
     } else {
-        // epilogue warp: TMEM lane quarter q = tokens q*32..q*32+31 of the tile
-        const int ew = warp - 3, q = warp & 3;
-        uint8_t* st_f32 = ostage + ew * kEpiWarpBytes;
-        uint8_t* st_b16 = st_f32 + kEpiF32;
-        uint8_t* st_h16 = st_b16 + kEpi16;
+        // epilogue warp: TMEM lane quarter q = tokens q*32..q*32+31 of the tile; group
+        // g takes the step pairs {2g, 2g+1} and {4+2g, 5+2g}
+        const int ew = warp - 3, q = warp & 3, g = ew >> 2;
         const int row = q * kEpiRows + lane;         // this lane's token within the tile
-        int u = 0, lt = 0;
+        int lt = 0;
         for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
             const int tt = tile / kUpColTiles, ct = tile % kUpColTiles;
             const int b = lt & 1;
-            const int t0 = tt * kTileM + q * kEpiRows;
-            const int t = t0 + lane;
+            const int t = tt * kTileM + row;
+            const bool valid = t < T;
             float mx[16];
             if (kFused) {
-                if (t < T) {
+                if (valid) {
                     const float4* m4 = reinterpret_cast<const float4*>(Rmix + (size_t)t * 16);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -505,82 +519,75 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
             if (!mbar_wait(&acc_full[b], (lt >> 1) & 1, &abort_flag, status)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * kUpN;
+            const int u_tile = lt * kSteps * slots_per_step;
             bool ok = true;
 #pragma unroll 1
-            for (int k = 0; k < kSteps; ++k) {
-                const int c = ct * kUpCols + k * kEpiCols;
-                float v[kStreams][kEpiCols];
+            for (int pi = 0; pi < 2 && ok; ++pi) {
+                const int k0 = 4 * pi + 2 * g;
+                uint32_t bb[kStreams][8], hh[kStreams][8];   // 16 columns of the images
 #pragma unroll
-                for (int s = 0; s < kStreams; ++s) tmem_ld8(tbase + s * kUpCols + k * kEpiCols, v[s]);
-                // R' of this lane's token: slot layout [stream][128 tokens][8 columns]
-                float rp[kStreams][kEpiCols];
-                for (int which = 0; which < slots_per_step; ++which, ++u) {
-                    const int slot = u % kRSlots;
-                    if (!mbar_wait(&r_full[slot], (u / kRSlots) & 1, &abort_flag, status)) { ok = false; break; }
+                for (int j = 0; j < 2; ++j) {
+                    const int k = k0 + j;
+                    const int c = ct * kUpCols + k * kEpiCols;
+                    float v[kStreams][kEpiCols];
 #pragma unroll
-                    for (int s = 0; s < kStreams; ++s) {
-                        const float4* r4 = reinterpret_cast<const float4*>(
-                            rring + slot * kRSlot + s * (kRSlot / kStreams) + row * 32);
-                        const float4 a = r4[0], bq = r4[1];
-                        const float x[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
+                    for (int s = 0; s < kStreams; ++s) tmem_ld8(tbase + s * kUpCols + k * kEpiCols, v[s]);
+                    // R' of this lane's token: slot layout [stream][128 tokens][8 columns]
+                    float rp[kStreams][kEpiCols];
+                    for (int which = 0; which < slots_per_step; ++which) {
+                        const int u = u_tile + k * slots_per_step + which;
+                        const int slot = u % kRSlots;
+                        if (!mbar_wait(&r_full[slot], (u / kRSlots) & 1, &abort_flag, status)) { ok = false; break; }
 #pragma unroll
-                        for (int e = 0; e < kEpiCols; ++e) rp[s][e] = which ? rp[s][e] + x[e] : x[e];
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&r_empty[slot]);
-                }
-                if (!ok) break;
+                        for (int s = 0; s < kStreams; ++s) {
+                            const float4* r4 = reinterpret_cast<const float4*>(
+                                rring + slot * kRSlot + s * (kRSlot / kStreams) + row * 32);
+                            const float4 a = r4[0], bq = r4[1];
+                            const float x[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
 #pragma unroll
-                for (int s = 0; s < kStreams; ++s)
-#pragma unroll
-                    for (int e = 0; e < kEpiCols; ++e) v[s][e] = gate_value(v[s][e], rp[s][e]);
-                // staging: the fp32 buffer is rewritten every step, the 16-bit ones every
-                // second step; wait until the stores that read them have done so
-                if (lane == 0) bulk_wait_read_all();
-                __syncwarp();
-                const int h = k & 1;                    // which 8 of the 16 staged columns
-#pragma unroll
-                for (int so = 0; so < kStreams; ++so) {
-                    float o[kEpiCols];
-#pragma unroll
-                    for (int e = 0; e < kEpiCols; ++e)
-                        o[e] = kFused ? mix_row(&mx[so * 4], v[0][e], v[1][e], v[2][e], v[3][e]) : v[so][e];
-                    float4* f4 = reinterpret_cast<float4*>(st_f32 + (so * kEpiRows + lane) * 32);
-                    f4[0] = make_float4(o[0], o[1], o[2], o[3]);
-                    f4[1] = make_float4(o[4], o[5], o[6], o[7]);
-                    if (kFused) {
-                        uint32_t bb[4], hh[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            bb[i] = (uint32_t)to_bf16_bits(o[2 * i]) | ((uint32_t)to_bf16_bits(o[2 * i + 1]) << 16);
-                            hh[i] = (uint32_t)to_fp16_bits(o[2 * i]) | ((uint32_t)to_fp16_bits(o[2 * i + 1]) << 16);
+                            for (int e = 0; e < kEpiCols; ++e) rp[s][e] = which ? rp[s][e] + x[e] : x[e];
                         }
-                        *reinterpret_cast<uint4*>(st_b16 + (so * kEpiRows + lane) * 32 + h * 16) =
-                            make_uint4(bb[0], bb[1], bb[2], bb[3]);
-                        *reinterpret_cast<uint4*>(st_h16 + (so * kEpiRows + lane) * 32 + h * 16) =
-                            make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&r_empty[slot]);
                     }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
+                    if (!ok) break;
+#pragma unroll
+                    for (int s = 0; s < kStreams; ++s)
+#pragma unroll
+                        for (int e = 0; e < kEpiCols; ++e) v[s][e] = gate_value(v[s][e], rp[s][e]);
 #pragma unroll
                     for (int so = 0; so < kStreams; ++so) {
-                        tma_store_3d(&em.out, c, so, t0, st_f32 + so * (kEpiF32 / kStreams));
-                        if (kFused && h == 1) {
-                            tma_store_3d(&em.out_bf16, c - kEpiCols, so, t0, st_b16 + so * (kEpi16 / kStreams));
-                            tma_store_3d(&em.out_fp16, c - kEpiCols, so, t0, st_h16 + so * (kEpi16 / kStreams));
+                        float o[kEpiCols];
+#pragma unroll
+                        for (int e = 0; e < kEpiCols; ++e)
+                            o[e] = kFused ? mix_row(&mx[so * 4], v[0][e], v[1][e], v[2][e], v[3][e]) : v[so][e];
+                        uint32_t w[8];
+#pragma unroll
+                        for (int e = 0; e < kEpiCols; ++e) w[e] = __float_as_uint(o[e]);
+                        if (valid) st_global_v8(out_f32 + (size_t)t * kCols + so * kWidth + c, w);
+                        if (kFused) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                bb[so][4 * j + i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+                                hh[so][4 * j + i] = pack_f16x2(o[2 * i], o[2 * i + 1]);
+                            }
                         }
                     }
-                    bulk_commit();
+                }
+                if (!ok) break;
+                if (kFused && valid) {
+                    const size_t off = (size_t)t * kCols + ct * kUpCols + k0 * kEpiCols;
+#pragma unroll
+                    for (int so = 0; so < kStreams; ++so) {
+                        st_global_v8(out_bf16 + off + so * kWidth, bb[so]);
+                        st_global_v8(out_fp16 + off + so * kWidth, hh[so]);
+                    }
                 }
             }
             if (!ok) break;
             tc_fence_before();
             mbar_arrive(&acc_empty[b]);
         }
-        if (lane == 0) bulk_wait_all();
-        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -724,26 +731,15 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, bool fused, cu
     bool ok = encode_act(&em.R, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.R, a.T, kEpiCols, kTileM);
     ok = ok && encode_act(&em.P, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.P ? a.P : a.R, a.T,
                           kEpiCols, kTileM);
-    if (fused) {
-        ok = ok && encode_act(&em.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.out_f32, a.T,
-                              kEpiCols, kEpiRows);
-        ok = ok && encode_act(&em.out_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out_bf16, a.T,
-                              2 * kEpiCols, kEpiRows);
-        ok = ok && encode_act(&em.out_fp16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.out_fp16, a.T,
-                              2 * kEpiCols, kEpiRows);
-    } else {
-        ok = ok && encode_act(&em.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, c.gated, a.T,
-                              kEpiCols, kEpiRows);
-        em.out_bf16 = em.out;
-        em.out_fp16 = em.out;
-    }
     if (!ok) return cudaErrorInvalidValue;
     if (fused) {
         upmix_tile_kernel<true><<<up_grid, kUpThreads, kUpSmem, st>>>(
-            a.Rmix, c.tm_lo, c.tm_wu, em, a.P != nullptr, a.T, c.s.status);
+            a.Rmix, c.tm_lo, c.tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16, a.P != nullptr, a.T,
+            c.s.status);
     } else {
         upmix_tile_kernel<false><<<up_grid, kUpThreads, kUpSmem, st>>>(
-            a.Rmix, c.tm_lo, c.tm_wu, em, a.P != nullptr, a.T, c.s.status);
+            a.Rmix, c.tm_lo, c.tm_wu, em, c.gated, nullptr, nullptr, a.P != nullptr, a.T,
+            c.s.status);
         const int n = a.T * (kWidth / 4);
         const int mgrid = (n + 255) / 256 < 8 * c.sm_count ? (n + 255) / 256 : 8 * c.sm_count;
         mix_gated_kernel<<<mgrid, 256, 0, st>>>(c.gated, a.Rmix, a.out_f32, a.out_bf16, a.out_fp16,

@@ -51,6 +51,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete is suspended until it
+// completes or `hint_ns` nanoseconds pass, so a waiting warp takes no issue slots
+// from the warps that share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
+// Suspension granted to one try of a waiting thread.
+constexpr uint32_t kSuspendHintNs = 20000;   // 20 us
+
 // Waits for the phase of `bar` with the given parity to complete. Returns false
 // if the CTA's abort flag is raised or the wait runs out of time (then it raises
 // the flag and records a timeout in the device status word).
@@ -59,7 +77,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_suspend(bar, parity, kSuspendHintNs)) return true;
         if (*abort_flag) return false;
         if (globaltimer() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
