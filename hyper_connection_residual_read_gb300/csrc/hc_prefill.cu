@@ -118,20 +118,31 @@ __global__ void convert_weights_kernel(const uint16_t* __restrict__ wd, const ui
 }
 
 // ---------------------------------------------------------------------------
-// down projection, one (128-token tile, stream) per tile, persistent CTAs
+// down projection, one (128-token tile, stream, K quarter) per tile, persistent CTAs
+//
+// R reaches shared memory by TMA into the stage's A region, 32 KB of fp32 per K
+// block, laid out so that the 16 rows each converter warp owns occupy exactly the
+// bytes where that warp then writes the rows' two fp16 terms (hi in the first
+// 16 KB, lo in the second, 128-byte swizzled): the warp reads its rows into
+// registers, scales and splits them, and overwrites them in place, with no
+// synchronisation beyond the warp. The view of R that gives this layout is
+// (column, stream, row r, half h, group g) with token = 16 g + 8 h + r; a tile's
+// two loads (h = 0, 1) each take 8 rows of 8 groups. A last tile with fewer than
+// 128 tokens is read by the converter warps from global memory instead.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kDownThreads, 1)
 down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                  const uint16_t* __restrict__ w_norm, const __grid_constant__ CUtensorMap tm_wd,
-                 float* __restrict__ partials, float* __restrict__ ssq, int T,
-                 int* __restrict__ status) {
+                 const __grid_constant__ CUtensorMap tm_r, float* __restrict__ partials,
+                 float* __restrict__ ssq, int T, int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[kDownStages], empty_bar[kDownStages];
+    __shared__ __align__(8) uint64_t r_full[kDownStages];
     __shared__ __align__(8) uint64_t acc_full, acc_empty, ss_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
-    __shared__ float ss_s[2][kTileM];
+    __shared__ float ss_s[kTileM];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = ((T + kTileM - 1) / kTileM) * kStreams * kDownKSplit;
@@ -140,6 +151,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         for (int i = 0; i < kDownStages; ++i) {
             mbar_init(&full_bar[i], 256 + 1);
             mbar_init(&empty_bar[i], 1);
+            mbar_init(&r_full[i], 1);
         }
         mbar_init(&acc_full, 1);
         mbar_init(&acc_empty, 256);
@@ -157,11 +169,14 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
     auto sB = [&](int slot) { return smem + slot * kDownStageBytes + 2 * kTileBytes16; };
 
     if (warp == 0) {
-        // B producer: the stream's W_down columns, 320 rows as two boxes of 160
+        // producer: the stream's W_down columns (320 rows as two boxes of 160) and,
+        // for a full tile, the R block
         if (lane == 0) {
             int it = 0;
             for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
+                const int tt = tile / (kStreams * kDownKSplit);
                 const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
+                const bool full = (tt + 1) * kTileM <= T;
                 for (int kb = kq * kDownKBlocksPerTile; kb < (kq + 1) * kDownKBlocksPerTile; ++kb, ++it) {
                     const int slot = it % kDownStages;
                     const uint32_t ph = (it / kDownStages) & 1;
@@ -170,6 +185,13 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     const int x = s * kWidth + kb * kBK;
                     tma_load_2d(sB(slot), &tm_wd, x, 0, &full_bar[slot]);
                     tma_load_2d(sB(slot) + kDownBBytes / 2, &tm_wd, x, kDownN / 2, &full_bar[slot]);
+                    if (full) {
+                        mbar_arrive_expect_tx(&r_full[slot], 2 * kTileBytes16);
+                        tma_load_5d(sA(slot, 0), &tm_r, kb * kBK, s, 0, 0, tt * 8, &r_full[slot]);
+                        tma_load_5d(sA(slot, 1), &tm_r, kb * kBK, s, 0, 1, tt * 8, &r_full[slot]);
+                    } else {
+                        mbar_arrive(&r_full[slot]);
+                    }
                 }
             }
         }
@@ -208,9 +230,8 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         }
     } else {
         // 8 converter warps produce A: warp cw owns rows 16*cw..16*cw+15 of the tile;
-        // in each K block, lanes 0-15 and 16-31 read two rows at a time, 16 bytes each,
-        // so every load instruction covers two 256-byte row segments. The same warps then
-        // run the epilogue on their TMEM lane quarter.
+        // lanes 0-15 and 16-31 take two rows at a time, 4 columns each. The same
+        // warps then run the epilogue on their TMEM lane quarter.
         const int cw = warp - 2;
         const int q = warp & 3, half = (warp - 2) >> 2;
         const int m = q * 32 + lane;                    // epilogue row
@@ -219,6 +240,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
             const int tt = tile / (kStreams * kDownKSplit);
             const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
+            const bool full = (tt + 1) * kTileM <= T;
             const int t = tt * kTileM + m;
             const bool valid = t < T;
             float ss[8], amax = 0.f;
@@ -229,24 +251,42 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                 const uint32_t ph = (it / kDownStages) & 1;
                 const int k = s * kWidth + kb * kBK + kc;
                 float4 x[8];
+                // P (and, in a last partial tile, R) straight from global memory,
+                // issued before the wait
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int row = 16 * cw + 2 * i + (lane >> 4);
-                    const int tr = tt * kTileM + row;
+                    const int tr = tt * kTileM + 16 * cw + 2 * i + (lane >> 4);
                     x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (tr < T) {
-                        x[i] = *reinterpret_cast<const float4*>(R + (size_t)tr * kCols + k);
-                        if (P != nullptr) {
-                            const float4 p = *reinterpret_cast<const float4*>(P + (size_t)tr * kCols + k);
-                            x[i].x += p.x; x[i].y += p.y; x[i].z += p.z; x[i].w += p.w;
+                        if (P != nullptr) x[i] = *reinterpret_cast<const float4*>(P + (size_t)tr * kCols + k);
+                        if (!full) {
+                            const float4 r = *reinterpret_cast<const float4*>(R + (size_t)tr * kCols + k);
+                            x[i].x += r.x; x[i].y += r.y; x[i].z += r.z; x[i].w += r.w;
                         }
                     }
                 }
                 const uint2 wv = *reinterpret_cast<const uint2*>(w_norm + k);
                 const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x), w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
-                if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
+                if (!mbar_wait(&r_full[slot], ph, &abort_flag, status)) break;
                 uint8_t* ahi = sA(slot, 0);
                 uint8_t* alo = sA(slot, 1);
+                if (full) {
+                    // R rows j = 2i + (lane >> 4) of this warp: half j >> 3, row j & 7
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int j = 2 * i + (lane >> 4);
+                        const float4 r = *reinterpret_cast<const float4*>(
+                            sA(slot, j >> 3) + (cw * 8 + (j & 7)) * 256 + kc * 4);
+                        // R + P in that order: the pending write's single rounding
+                        if (P != nullptr) {
+                            x[i].x = r.x + x[i].x; x[i].y = r.y + x[i].y;
+                            x[i].z = r.z + x[i].z; x[i].w = r.w + x[i].w;
+                        } else {
+                            x[i] = r;
+                        }
+                    }
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int row = 16 * cw + 2 * i + (lane >> 4);
@@ -278,7 +318,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
                 v += __shfl_xor_sync(0xffffffffu, v, 4);
                 v += __shfl_xor_sync(0xffffffffu, v, 8);
-                if ((lane & 15) == 0) ss_s[0][16 * cw + 2 * i + (lane >> 4)] = v;
+                if ((lane & 15) == 0) ss_s[16 * cw + 2 * i + (lane >> 4)] = v;
             }
             mbar_arrive(&ss_bar);
             if (!mbar_wait(&ss_bar, lt & 1, &abort_flag, status)) break;
@@ -286,7 +326,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             if (!mbar_wait(&acc_full, lt & 1, &abort_flag, status)) break;
             tc_fence_after();
             const size_t prow = ((size_t)t * kStreams + s) * kDownKSplit + kq;
-            if (valid && half == 0) ssq[prow] = ss_s[0][m];
+            if (valid && half == 0) ssq[prow] = ss_s[m];
             float* dst = partials + prow * kRank + half * (kDownN / 2);
 #pragma unroll 1
             for (int c0 = 0; c0 < kDownN / 2; c0 += 16) {
@@ -654,7 +694,7 @@ bool encode_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, int 
                 CUtensorMapSwizzle swz) {
     auto enc = get_encoder();
     if (enc == nullptr) return false;
-    const cuuint32_t es[3] = {1, 1, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
     return enc(map, dt, rank, const_cast<void*>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -674,6 +714,20 @@ bool encode_act(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void*
     const cuuint64_t strides[2] = {(cuuint64_t)kWidth * esize, (cuuint64_t)kCols * esize};
     const cuuint32_t box[3] = {(cuuint32_t)cols, 1, (cuuint32_t)rows};
     return encode_map(map, dt, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// R [T][4][2560] fp32 seen as (column, stream, row r, half h, group g), token =
+// 16 g + 8 h + r, in boxes of 64 columns x 1 stream x 8 rows x 1 half x 8 groups.
+// Only whole groups of 16 tokens are described; the kernel uses the map for full
+// 128-token tiles only.
+bool encode_down_r(CUtensorMap* map, const float* R, int T) {
+    const cuuint64_t groups = T / 16 > 0 ? (cuuint64_t)(T / 16) : 1;
+    const cuuint64_t dims[5] = {kWidth, kStreams, 8, 2, groups};
+    const cuuint64_t row = (cuuint64_t)kCols * 4;
+    const cuuint64_t strides[4] = {(cuuint64_t)kWidth * 4, row, 8 * row, 16 * row};
+    const cuuint32_t box[5] = {kBK, 1, 8, 1, 8};
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, R, 5, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace
@@ -714,8 +768,10 @@ cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, cudaStream_t st
     const int n_tt = (a.T + kTileM - 1) / kTileM;
     const int down_tiles = n_tt * kStreams * kDownKSplit;
     const int down_grid = down_tiles < c.sm_count ? down_tiles : c.sm_count;
-    down_tile_kernel<<<down_grid, kDownThreads, kDownSmem, st>>>(a.R, a.P, a.w_norm, c.tm_wd,
-                                                                 c.partials, c.ssq, a.T, c.s.status);
+    CUtensorMap tm_r;
+    if (!encode_down_r(&tm_r, a.R, a.T)) return cudaErrorInvalidValue;
+    down_tile_kernel<<<down_grid, kDownThreads, kDownSmem, st>>>(
+        a.R, a.P, a.w_norm, c.tm_wd, tm_r, c.partials, c.ssq, a.T, c.s.status);
     const int n4 = a.T * (kRank / 4);
     const int rgrid = (n4 + 255) / 256 < 8 * c.sm_count ? (n4 + 255) / 256 : 8 * c.sm_count;
     lo_split_kernel<<<rgrid, 256, 0, st>>>(c.partials, c.ssq, c.lo16, a.T, c.max_tokens, c.eps,
