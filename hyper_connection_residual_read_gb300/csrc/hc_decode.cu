@@ -23,6 +23,11 @@
 //
 // Weights are loaded straight into registers with 16-byte streaming loads issued
 // before anything else, so a kernel's whole weight matrix is in flight at once.
+//
+// Only the weight pointers carry __restrict__. A load through a const __restrict__
+// pointer may be treated as invariant and moved above griddepcontrol.wait; the
+// activations (R, P, lo, Rmix) are written by the kernels before these on the
+// stream, so their loads must stay after the wait.
 #include <cooperative_groups.h>
 
 #include "hc_common.cuh"
@@ -66,9 +71,8 @@ __device__ __forceinline__ float warp_reduce_8rows(const float (&v)[8], int lane
 
 template <int T>
 __global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kDownThreads)
-down_slice_kernel(const float* __restrict__ R, const float* __restrict__ P,
-                  const uint16_t* __restrict__ w_norm, const uint16_t* __restrict__ W_down,
-                  float* __restrict__ lo, float eps) {
+down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w_norm,
+                  const uint16_t* __restrict__ W_down, float* lo, float eps) {
     namespace cg = cooperative_groups;
     const int sl = blockIdx.x;                 // K slice 0..7 == rank in the cluster
     const int rb = blockIdx.y;                 // row block 0..19 == the cluster
@@ -210,10 +214,9 @@ constexpr int kLoPart = 44;
 
 template <int T>
 __global__ void __launch_bounds__(kUpThreads)
-up_mix_kernel(const float* __restrict__ R, const float* __restrict__ P,
-              const uint16_t* __restrict__ W_up, const float* __restrict__ lo,
-              const float* __restrict__ Rmix, float* __restrict__ out_f32,
-              uint16_t* __restrict__ out_bf16, uint16_t* __restrict__ out_fp16) {
+up_mix_kernel(const float* R, const float* P, const uint16_t* __restrict__ W_up,
+              const float* lo, const float* Rmix, float* out_f32, uint16_t* out_bf16,
+              uint16_t* out_fp16) {
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int cc = lane >> 3;                  // which of the warp's 4 columns
@@ -245,10 +248,23 @@ up_mix_kernel(const float* __restrict__ R, const float* __restrict__ P,
 #pragma unroll
         for (int t = 0; t < T; ++t) rp[t] += P[(size_t)t * kCols + sp * kWidth + c];
     }
-    for (int e = tid; e < T * kRank / 4; e += kUpThreads) {
-        const int t = e / (kRank / 4), j = 4 * (e % (kRank / 4));
-        const float4 v = *reinterpret_cast<const float4*>(lo + (size_t)t * kRank + j);
-        *reinterpret_cast<float4*>(&lo_s[t][j / 40][j % 40]) = v;
+    // lo of the chunk ([T][320], contiguous): every load is issued before the first
+    // store, so the staging costs one round trip whatever T is
+    constexpr int kLoVec = T * kRank / 4;
+    constexpr int kLoIter = (kLoVec + kUpThreads - 1) / kUpThreads;
+    float4 lv[kLoIter];
+#pragma unroll
+    for (int i = 0; i < kLoIter; ++i) {
+        const int e = tid + i * kUpThreads;
+        if (e < kLoVec) lv[i] = reinterpret_cast<const float4*>(lo)[e];
+    }
+#pragma unroll
+    for (int i = 0; i < kLoIter; ++i) {
+        const int e = tid + i * kUpThreads;
+        if (e < kLoVec) {
+            const int t = e / (kRank / 4), j = 4 * (e % (kRank / 4));
+            *reinterpret_cast<float4*>(&lo_s[t][j / 40][j % 40]) = lv[i];
+        }
     }
     if (tid < T * 4) reinterpret_cast<float4*>(&m_s[0][0])[tid] =
         reinterpret_cast<const float4*>(Rmix)[tid];

@@ -84,12 +84,10 @@ __device__ __forceinline__ float warp_reduce_8rows(const float (&v)[8], int lane
 
 template <int T>
 __global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kThreads, 2)
-decode_fused_kernel(const float* __restrict__ R, const float* __restrict__ P,
-                    const uint16_t* __restrict__ w_norm, const uint16_t* __restrict__ W_down,
-                    const uint16_t* __restrict__ W_up, const float* __restrict__ Rmix,
-                    float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16,
-                    uint16_t* __restrict__ out_fp16, float* __restrict__ lo,
-                    unsigned* __restrict__ sync, float eps, int* __restrict__ status) {
+decode_fused_kernel(const float* R, const float* P, const uint16_t* __restrict__ w_norm,
+                    const uint16_t* __restrict__ W_down, const uint16_t* __restrict__ W_up,
+                    const float* Rmix, float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
+                    float* lo, unsigned* sync, float eps, int* status) {
     namespace cg = cooperative_groups;
     const int sl = blockIdx.x, rb = blockIdx.y;
     const int cid = rb * kDownSlices + sl;                 // 0..159

@@ -58,6 +58,37 @@ def test_verify_window_sweep(weights, T, with_P):
     assert_matches_oracle(got, want)
 
 
+@pytest.mark.parametrize("path", [hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_ONE_KERNEL])
+def test_chained_reads_wait_for_their_inputs(weights, path):
+    """Three reads back to back on one stream, each taking the previous read's fp32
+    output as its residual, with no synchronisation between them. The decode kernels
+    start early (programmatic dependent launch) and may read only weights before
+    the previous kernel has finished: a read that loaded its residual, its pending
+    write, the mix or lo too soon would see a partly written or stale buffer. A
+    read of other inputs first leaves a different lo in scratch."""
+    w, W = weights
+    for T in (1, 5, 8):
+        other = synth.make_activations(900 + T, T, True)
+        gpu_read(T, dev_f32(other["R"]), dev_f32(other["P"]), W, dev_f32(other["Rmix"]), path)
+        acts = [synth.make_activations(910 + 3 * T + i, T, True) for i in range(3)]
+        R = dev_f32(acts[0]["R"])
+        Ps = [dev_f32(a["P"]) for a in acts]
+        Ms = [dev_f32(a["Rmix"]) for a in acts]
+        outs = [alloc_out(T) for _ in acts]
+        torch.cuda.synchronize()
+        for P, M, o in zip(Ps, Ms, outs):
+            hc.hc_read_path(path, T, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o)
+            R = o[0]
+        torch.cuda.synchronize()
+        r = acts[0]["R"]
+        for a, o in zip(acts, outs):
+            want = O.hc_read(r, a["P"], w["w_norm"], w["W_down"], w["W_up"], a["Rmix"], EPS)
+            got = (o[0].cpu().numpy(), o[1].cpu().numpy().view(np.uint16),
+                   o[2].cpu().numpy().view(np.uint16))
+            assert_matches_oracle(got, want)
+            r = got[0]
+
+
 @pytest.mark.parametrize("T", [9, 13, 16, 17, 31])
 @pytest.mark.parametrize("path", [hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_ONE_KERNEL])
 def test_ragged_token_counts(weights, T, path):
