@@ -53,7 +53,9 @@ constexpr int kDownKBlocks = kWidth / kBK;        // 40 per stream
 // relative shrink of the result.
 constexpr int kDownKSplit = 4;
 constexpr int kDownKBlocksPerTile = kDownKBlocks / kDownKSplit;   // 10
-constexpr int kDownThreads = 320;                  // TMA, MMA, 8 converter/epilogue warps
+// TMA, MMA, 8 converter warps, 4 epilogue warps (one per TMEM lane quarter): the
+// epilogue of one tile runs while the converters already produce the next tile's A
+constexpr int kDownThreads = 448;
 constexpr int kDownSmem = kDownStages * kDownStageBytes + 1024;
 
 // upmix_tile
@@ -92,6 +94,22 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
     const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
     hi = *reinterpret_cast<const uint32_t*>(&h);
     lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// 32-byte global accesses (one whole DRAM sector per lane).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // ---------------------------------------------------------------------------
@@ -139,10 +157,10 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
     uint8_t* smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[kDownStages], empty_bar[kDownStages];
     __shared__ __align__(8) uint64_t r_full[kDownStages];
-    __shared__ __align__(8) uint64_t acc_full, acc_empty, ss_bar;
+    __shared__ __align__(8) uint64_t acc_full, acc_empty, ss_full[2];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
-    __shared__ float ss_s[kTileM];
+    __shared__ float ss_s[2][kTileM];   // per-row sums of squares, by tile parity
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = ((T + kTileM - 1) / kTileM) * kStreams * kDownKSplit;
@@ -154,8 +172,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             mbar_init(&r_full[i], 1);
         }
         mbar_init(&acc_full, 1);
-        mbar_init(&acc_empty, 256);
-        mbar_init(&ss_bar, 256);
+        mbar_init(&acc_empty, 128);
+        mbar_init(&ss_full[0], 256);
+        mbar_init(&ss_full[1], 256);
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -228,21 +247,16 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                 mma_commit(&acc_full);
             }
         }
-    } else {
+    } else if (warp < 10) {
         // 8 converter warps produce A: warp cw owns rows 16*cw..16*cw+15 of the tile;
-        // lanes 0-15 and 16-31 take two rows at a time, 4 columns each. The same
-        // warps then run the epilogue on their TMEM lane quarter.
+        // lanes 0-15 and 16-31 take two rows at a time, 4 columns each
         const int cw = warp - 2;
-        const int q = warp & 3, half = (warp - 2) >> 2;
-        const int m = q * 32 + lane;                    // epilogue row
         const int kc = 4 * (lane & 15);                 // this lane's 4 columns in a K block
         int it = 0, lt = 0;
         for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
             const int tt = tile / (kStreams * kDownKSplit);
             const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
             const bool full = (tt + 1) * kTileM <= T;
-            const int t = tt * kTileM + m;
-            const bool valid = t < T;
             float ss[8], amax = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss[i] = 0.f;
@@ -310,7 +324,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             }
             if (abort_flag) break;
             if (amax >= 65504.f) atomicOr(status, kStatusRange);
-            // sums of squares per row: the 16 lanes that share a row, in a fixed order
+            // sums of squares per row: the 16 lanes that share a row, in a fixed order.
+            // The buffer of this parity was last read by the epilogue two tiles ago,
+            // which has finished: the MMAs of this tile could not start before it.
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 float v = ss[i];
@@ -318,29 +334,44 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
                 v += __shfl_xor_sync(0xffffffffu, v, 4);
                 v += __shfl_xor_sync(0xffffffffu, v, 8);
-                if ((lane & 15) == 0) ss_s[16 * cw + 2 * i + (lane >> 4)] = v;
+                if ((lane & 15) == 0) ss_s[lt & 1][16 * cw + 2 * i + (lane >> 4)] = v;
             }
-            mbar_arrive(&ss_bar);
-            if (!mbar_wait(&ss_bar, lt & 1, &abort_flag, status)) break;
-            // epilogue: store this quarter's partial dots and its sums of squares
+            mbar_arrive(&ss_full[lt & 1]);
+        }
+    } else {
+        // 4 epilogue warps: TMEM lane quarter q = rows q*32..q*32+31, all 320 columns;
+        // store this quarter's partial dots and its sums of squares
+        const int q = warp & 3;
+        const int m = q * 32 + lane;
+        int lt = 0;
+        for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
+            const int tt = tile / (kStreams * kDownKSplit);
+            const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
+            const int t = tt * kTileM + m;
+            const bool valid = t < T;
             if (!mbar_wait(&acc_full, lt & 1, &abort_flag, status)) break;
             tc_fence_after();
             const size_t prow = ((size_t)t * kStreams + s) * kDownKSplit + kq;
-            if (valid && half == 0) ssq[prow] = ss_s[m];
-            float* dst = partials + prow * kRank + half * (kDownN / 2);
+            float* dst = partials + prow * kRank;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kDownN / 2; c0 += 16) {
+            for (int c0 = 0; c0 < kDownN; c0 += 16) {
                 float v[16];
-                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + half * (kDownN / 2) + c0, v);
+                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
                 if (valid) {
+                    uint32_t w0[8], w1[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        *reinterpret_cast<float4*>(dst + c0 + 4 * i) =
-                            make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    for (int i = 0; i < 8; ++i) {
+                        w0[i] = __float_as_uint(v[i]);
+                        w1[i] = __float_as_uint(v[8 + i]);
+                    }
+                    st_global_v8(dst + c0, w0);
+                    st_global_v8(dst + c0 + 8, w1);
                 }
             }
             tc_fence_before();
             mbar_arrive(&acc_empty);
+            if (!mbar_wait(&ss_full[lt & 1], (lt >> 1) & 1, &abort_flag, status)) break;
+            if (valid) ssq[prow] = ss_s[lt & 1][m];
         }
     }
     tc_fence_before();
@@ -396,22 +427,6 @@ __global__ void lo_split_kernel(const float* __restrict__ partials, const float*
 struct EpiMaps {
     CUtensorMap R, P;
 };
-
-// 32-byte global accesses (one whole DRAM sector per lane).
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
-    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]),
-                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-                 : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
 
 template <bool kFused>
 __global__ void __launch_bounds__(kUpThreads, 1)
