@@ -64,6 +64,24 @@ def prefill_read_bytes(T: int) -> int:
     return WEIGHT_BYTES + T * (40960 + 64 + 81920)
 
 
+def reduce_max(value: float, world: int, device=None) -> float:
+    """The largest of the ranks' values, returned on every rank (the slowest rank's
+    time is the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def us_per_unit(ms_max: float, units_per_rank: int, world: int) -> float:
+    """Whole-job microseconds per unit: the slowest rank's time over the units that
+    all ranks processed (every rank runs the same number of units)."""
+    return 1e3 * ms_max / (units_per_rank * world)
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -288,19 +306,14 @@ def gpu_arm(args) -> None:
                 fn(k)
             e1.record(stream)
             barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return reduce_max(e0.elapsed_time(e1), world, dev)
 
     # --- main number: graph replays of the sweep ---
     with ClockSampler(local) as clk:
         ms = timed(lambda k: graphs[k % n_groups].replay(), args.steps, args.warmup)
     clocks = clk.summary()
     reads_per_step = len(SWEEP)
-    us_per_read = 1e3 * ms / (args.steps * reads_per_step * world)
+    us_per_read = us_per_unit(ms, args.steps * reads_per_step, world)
     step_bytes = sum(read_bytes(T, p) for T, p in SWEEP)
 
     # --- per-T times (graph of 48 reads of one T over the 48 sets), for each decode path ---
@@ -389,7 +402,7 @@ def gpu_arm(args) -> None:
 
     e2e_steps = max(10, min(args.steps, 500))
     ms_e = timed(e2e_step, e2e_steps, min(args.warmup, 5) + 3)
-    e2e_us = 1e3 * ms_e / (e2e_steps * reads_per_step * world)
+    e2e_us = us_per_unit(ms_e, e2e_steps * reads_per_step, world)
 
     # --- prefill chunks: the whole read, and the fused up + gate + mix stage alone
     #     (re-run on the chunk's lo) next to the unfused pair (up GEMM writing gated,
