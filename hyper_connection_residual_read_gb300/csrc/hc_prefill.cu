@@ -354,18 +354,17 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             const size_t prow = ((size_t)t * kStreams + s) * kDownKSplit + kq;
             float* dst = partials + prow * kRank;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kDownN; c0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
+            for (int c0 = 0; c0 < kDownN; c0 += 32) {
+                float v[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
                 if (valid) {
-                    uint32_t w0[8], w1[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        w0[i] = __float_as_uint(v[i]);
-                        w1[i] = __float_as_uint(v[8 + i]);
+                    for (int g = 0; g < 4; ++g) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(v[8 * g + i]);
+                        st_global_v8(dst + c0 + 8 * g, w);
                     }
-                    st_global_v8(dst + c0, w0);
-                    st_global_v8(dst + c0 + 8, w1);
                 }
             }
             tc_fence_before();
@@ -585,8 +584,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     const int k = k0 + j;
                     const int c = ct * kUpCols + k * kEpiCols;
                     float v[kStreams][kEpiCols];
-#pragma unroll
-                    for (int s = 0; s < kStreams; ++s) tmem_ld8(tbase + s * kUpCols + k * kEpiCols, v[s]);
+                    tmem_ld8x4<kUpCols>(tbase + k * kEpiCols, v);
                     // R' of this lane's token: slot layout [stream][128 tokens][8 columns]
                     float rp[kStreams][kEpiCols];
                     for (int which = 0; which < slots_per_step; ++which) {
