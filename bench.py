@@ -439,6 +439,24 @@ def gpu_arm(args) -> None:
             "upmix_unfused_pair_ms": ms_pair, "fused_speedup": ms_pair / ms_fused}
         del R, M, o
 
+    # --- decode / prefill crossover: both paths on the same reads (one weight set,
+    #     pending write, the tokens of one chunk), µs per read ---
+    crossover = {}
+    c = synth.make_prefill_chunk(105, 256)
+    Rc, Mc = to_dev(c["R"]), to_dev(c["Rmix"])
+    Pc = to_dev((0.1 * np.random.default_rng(106).standard_normal(c["R"].shape)).astype(np.float32))
+    for T in (8, 9, 16, 24, 32, 48, 64, 128, 256):
+        o = tuple(torch.empty((T, 4, 2560), dtype=dt, device=dev)
+                  for dt in (torch.float32, torch.int16, torch.int16))
+        row = {}
+        for name, path in (("decode", hc.HC_PATH_DECODE), ("prefill", hc.HC_PATH_PREFILL)):
+            def one(k, path=path):
+                hc.hc_read_path(path, T, Rc, Pc, W0["w_norm"], W0["W_down"], W0["W_up"], Mc, *o,
+                                stream=stream)
+            row[name] = 1e3 * timed(one, 20, 3) / 20
+        crossover[f"T{T}"] = row
+    del Rc, Mc, Pc
+
     achieved = step_bytes / (ms / args.steps * 1e-3) / 1e9
     traffic = step_bytes * NCU_TRAFFIC_T4_P / read_bytes(4, True)
     kernel_launches_per_step = sum(2 * ((T + 7) // 8) for T, _ in SWEEP)
@@ -463,6 +481,7 @@ def gpu_arm(args) -> None:
         "decode_paths_us_by_T_with_P": per_t_paths,
         "cold_round_96x_T4_P": cold_round,
         "prefill": prefill,
+        "crossover_us_per_read": crossover,
     }
     if rank == 0:
         if not args.no_cpu_baseline:

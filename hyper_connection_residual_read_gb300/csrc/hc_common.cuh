@@ -16,15 +16,6 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
     return v;
 }
 
-// 8-byte streaming load that skips L1.
-__device__ __forceinline__ uint2 ldg_stream_v2(const void* p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-                 : "=r"(v.x), "=r"(v.y)
-                 : "l"(p));
-    return v;
-}
-
 // Programmatic dependent launch. A kernel launched with programmatic stream
 // serialisation may start while the previous kernel on the stream is still
 // running; `pdl_wait` blocks until that kernel has completed and its writes are

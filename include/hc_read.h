@@ -82,8 +82,9 @@ enum hc_status {
     HC_ERR_RANGE = -8      /* a tile-path activation did not fit fp16 (status word) */
 };
 
-/* Which kernels run. HC_PATH_AUTO picks the decode kernels for small T and the
- * tensor-core tile path above that; the others force one path (tests, bench). */
+/* Which kernels run. HC_PATH_AUTO picks the decode kernels for T <= 32 (the measured
+ * crossover) and the tensor-core tile path above that; the others force one path
+ * (tests, bench). */
 enum hc_path {
     HC_PATH_AUTO = 0,
     HC_PATH_DECODE = 1,            /* per 8 tokens: sliced down kernel, then up/gate/mix kernel */
