@@ -11,9 +11,11 @@
 //      Summary, change 4): a slice stages R' * w_norm unscaled together with its
 //      per-token sum of squares, and the reduce applies each stream's rs to that
 //      stream's partial dots. The 8 slices of a row block form one thread-block
-//      cluster and reduce through distributed shared memory in a fixed order
-//      (the page's change 1 does it with the last slice to finish; a cluster
-//      needs no global counter), so the result is bitwise repeatable.
+//      cluster: each pushes its partials into the shared memory of the CTA that
+//      finishes those rows, one cluster barrier publishes them, and each CTA sums
+//      its inbox in a fixed order (the page's change 1 does it with the last slice
+//      to finish; a cluster needs no global counter), so the result is bitwise
+//      repeatable.
 //
 //  up_mix_kernel - a warp owns 4 output columns; 8 lanes per column each sum 40
 //      of the 320 inputs for all 4 up rows i = s*2560 + c of that column, an xor
@@ -92,6 +94,9 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
     for (int r = 0; r < 8; ++r)
         wv[r] = ldg_stream_v4(W_down + (size_t)(j0 + r) * kCols + k0 + col);
     const uint2 wn = *reinterpret_cast<const uint2*>(w_norm + k0 + 4 * tid);
+    // first half of a cluster barrier: the wait before the pushes of step 4 then
+    // finds every CTA of the cluster started (their shared memory exists)
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     pdl_launch_dependents();
     pdl_wait();
 
@@ -101,8 +106,8 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
     __shared__ float4 a_s[T][kDownSliceCols / 4];
     __shared__ float red_ss[kDownThreads / 32][T];
     __shared__ float red[T][kDownColGroups][kDownRowsPerCta];
-    __shared__ float part_s[T][kDownRowsPerCta];   // this slice's partial dots
     __shared__ float ss_s[T];                      // this slice's sums of squares
+    __shared__ float inbox[kDownSlices][T][3];     // pushed by each slice: 2 partials, ss
 
     float4 xs[T];
 #pragma unroll
@@ -172,40 +177,39 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
     }
     __syncthreads();
 
-    // 4. this slice's partial for its 16 rows, column groups summed in order
+    // 4. this slice's partial for its 16 rows, column groups summed in order, pushed
+    //    into the shared memory of the CTA that finishes the row: CTA d finishes rows
+    //    2d and 2d+1 of the block and receives, from every slice r, those two
+    //    partials and r's sums of squares. Remote stores need no round trip, and after
+    //    the one cluster barrier that publishes them no CTA touches another's memory.
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    cg::cluster_group cluster = cg::this_cluster();
     if (tid < T * kDownRowsPerCta) {
         const int t = tid / kDownRowsPerCta, j = tid % kDownRowsPerCta;
         float v = red[t][0][j];
 #pragma unroll
         for (int g = 1; g < kDownColGroups; ++g) v += red[t][g][j];
-        part_s[t][j] = v;
+        *cluster.map_shared_rank(&inbox[sl][t][j & 1], j >> 1) = v;
+    } else if (tid >= 128 && tid < 128 + T * kDownSlices) {
+        const int t = (tid - 128) / kDownSlices, d = (tid - 128) % kDownSlices;
+        *cluster.map_shared_rank(&inbox[sl][t][2], d) = ss_s[t];
     }
-
-    // 5. reduce over the 8 slices of the row block through distributed shared
-    //    memory: CTA `sl` finishes rows 2*sl and 2*sl+1 of the block, summing the
-    //    slices of each stream in order and applying that stream's rs.
-    cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
+
+    // 5. CTA `sl` finishes rows 2*sl and 2*sl+1 of the block, summing the slices of
+    //    each stream in order and applying that stream's rs
     if (tid < T * 2) {
-        const int t = tid >> 1, j = 2 * sl + (tid & 1);
-        // all 16 remote loads first, then the arithmetic (each is a round trip)
-        float ssv[kDownSlices], pv[kDownSlices];
-#pragma unroll
-        for (int r = 0; r < kDownSlices; ++r) {
-            ssv[r] = *cluster.map_shared_rank(&ss_s[t], r);
-            pv[r] = *cluster.map_shared_rank(&part_s[t][j], r);
-        }
+        const int t = tid >> 1, jj = tid & 1;
         float v = 0.f;
 #pragma unroll
         for (int st = 0; st < kStreams; ++st) {
-            const float ss = ssv[2 * st] + ssv[2 * st + 1];
+            const float ss = inbox[2 * st][t][2] + inbox[2 * st + 1][t][2];
             const float rs = 1.0f / sqrtf(ss / (float)kWidth + eps);
-            const float d = pv[2 * st] + pv[2 * st + 1];
+            const float d = inbox[2 * st][t][jj] + inbox[2 * st + 1][t][jj];
             v = fmaf(rs, d, v);
         }
-        lo[t * kRank + rb * kDownRowsPerCta + j] = v;
+        lo[t * kRank + rb * kDownRowsPerCta + 2 * sl + jj] = v;
     }
-    cluster.sync();   // keep this CTA's shared memory alive until every reader is done
 }
 
 // lo in shared memory: each token's 320 values as 8 parts of 40, padded to 44
