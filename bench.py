@@ -421,22 +421,36 @@ def gpu_arm(args) -> None:
                        stream=stream)
 
         def upmix_fused(k):
-            hc.hc_read_upmix(True, T, R, None, M, *o, stream=stream)
+            hc.hc_read_upmix(hc.HC_PATH_PREFILL, T, R, None, None, M, *o, stream=stream)
 
         def upmix_pair(k):
-            hc.hc_read_upmix(False, T, R, None, M, *o, stream=stream)
+            hc.hc_read_upmix(hc.HC_PATH_PREFILL_UNFUSED, T, R, None, None, M, *o, stream=stream)
+
+        def chunk_bf16(k):
+            hc.hc_read_path(hc.HC_PATH_PREFILL_BF16_LO, T, R, None, W0["w_norm"], W0["W_down"],
+                            W0["W_up"], M, *o, stream=stream)
+
+        def upmix_bf16(k):
+            hc.hc_read_upmix(hc.HC_PATH_PREFILL_BF16_LO, T, R, None, W0["W_up"], M, *o,
+                             stream=stream)
 
         reps = 10 if T == 8192 else 4
         ms_read = timed(chunk, reps, 3) / reps          # leaves this chunk's lo in scratch
         ms_fused = timed(upmix_fused, reps, 3) / reps
         ms_pair = timed(upmix_pair, reps, 3) / reps
+        ms_read16 = timed(chunk_bf16, reps, 3) / reps   # the pages' bf16-lo numerics
+        ms_up16 = timed(upmix_bf16, reps, 3) / reps
         fused_gbps = prefill_upmix_bytes(T) / (ms_fused * 1e-3) / 1e9
+        # the bf16-lo stage reads lo as one bf16 term (640 B per token instead of 1,280)
+        up16_gbps = (prefill_upmix_bytes(T) - 640 * T) / (ms_up16 * 1e-3) / 1e9
         prefill[f"T{T}"] = {
             "read_ms": ms_read, "tokens_per_s": T / (ms_read * 1e-3),
             "read_gbps": prefill_read_bytes(T) / (ms_read * 1e-3) / 1e9,
             "upmix_fused_ms": ms_fused, "upmix_fused_gbps": fused_gbps,
             "upmix_fused_frac": fused_gbps / peaks["hbm_gbs"],
-            "upmix_unfused_pair_ms": ms_pair, "fused_speedup": ms_pair / ms_fused}
+            "upmix_unfused_pair_ms": ms_pair, "fused_speedup": ms_pair / ms_fused,
+            "bf16_lo_read_ms": ms_read16, "bf16_lo_upmix_ms": ms_up16,
+            "bf16_lo_upmix_frac": up16_gbps / peaks["hbm_gbs"]}
         del R, M, o
 
     # --- decode / prefill crossover: both paths on the same reads (one weight set,

@@ -28,13 +28,14 @@ HC_PATH_DECODE = 1
 HC_PATH_PREFILL = 2
 HC_PATH_PREFILL_UNFUSED = 3
 HC_PATH_DECODE_ONE_KERNEL = 4
+HC_PATH_PREFILL_BF16_LO = 5
 
 STREAMS, WIDTH, RANK = 4, 2560, 320
 
 # every symbol include/hc_read.h declares
 EXPORTS = ("hc_read_init", "hc_read", "hc_read_path", "hc_read_check", "hc_read_status",
            "hc_read_strerror", "hc_read_shutdown", "hc_read_version", "hc_read_noalloc",
-           "hc_read_upmix")
+           "hc_read_upmix", "hc_read_lo_bf16")
 
 
 class HcReadError(RuntimeError):
@@ -94,8 +95,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_read_version.restype = i32
     lib.hc_read_noalloc.argtypes = [i32] + [vp] * 9 + [ctypes.c_float, vp]
     lib.hc_read_noalloc.restype = i32
-    lib.hc_read_upmix.argtypes = [i32, i32] + [vp] * 7
+    lib.hc_read_upmix.argtypes = [i32, i32] + [vp] * 8
     lib.hc_read_upmix.restype = i32
+    lib.hc_read_lo_bf16.argtypes = [i32, vp, vp]
+    lib.hc_read_lo_bf16.restype = i32
     _lib = lib
     return lib
 
@@ -161,11 +164,20 @@ def hc_read_noalloc(tokens, R, P, w_norm, W_down, W_up, Rmix, out_f32, out_bf16,
         _ptr(out_f32), _ptr(out_bf16), _ptr(out_fp16), eps, _stream(stream)))
 
 
-def hc_read_upmix(fused, tokens, R, P, Rmix, out_f32, out_bf16, out_fp16, stream=None) -> None:
-    """Re-runs the up projection + gate + mix stage of the last tile-path call."""
+def hc_read_upmix(path, tokens, R, P, W_up, Rmix, out_f32, out_bf16, out_fp16,
+                  stream=None) -> None:
+    """Re-runs the up projection + gate + mix stage of the last tile-path call
+    (``path``: HC_PATH_PREFILL, HC_PATH_PREFILL_UNFUSED or HC_PATH_PREFILL_BF16_LO;
+    ``W_up`` is read by the last one only and may be None otherwise)."""
     _check("hc_read_upmix", load().hc_read_upmix(
-        int(bool(fused)), tokens, _ptr(R), _ptr(P), _ptr(Rmix), _ptr(out_f32), _ptr(out_bf16),
+        path, tokens, _ptr(R), _ptr(P), _ptr(W_up), _ptr(Rmix), _ptr(out_f32), _ptr(out_bf16),
         _ptr(out_fp16), _stream(stream)))
+
+
+def hc_read_lo_bf16(tokens, lo_out, stream=None) -> None:
+    """Copies the bf16 lo of the last HC_PATH_PREFILL_BF16_LO call into ``lo_out``
+    ([tokens][320] 16-bit device tensor)."""
+    _check("hc_read_lo_bf16", load().hc_read_lo_bf16(tokens, _ptr(lo_out), _stream(stream)))
 
 
 def hc_read_check(max_tokens: int = 8, seed: int = 0) -> tuple[int, dict]:

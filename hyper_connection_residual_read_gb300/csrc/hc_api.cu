@@ -102,7 +102,7 @@ int run(int path, const ReadArgs& a, cudaStream_t st) {
     int err;
     Ctx* c = current_ctx(&err);
     if (!c) return err;
-    if (path < HC_PATH_AUTO || path > HC_PATH_DECODE_ONE_KERNEL) return HC_ERR_ARG;
+    if (path < HC_PATH_AUTO || path > HC_PATH_PREFILL_BF16_LO) return HC_ERR_ARG;
     if (int e = validate(*c, a)) return e;
     if (a.T == 0) return HC_OK;
     if (path == HC_PATH_AUTO) path = a.T <= kAutoDecodeMaxT ? HC_PATH_DECODE : HC_PATH_PREFILL;
@@ -116,7 +116,14 @@ int run(int path, const ReadArgs& a, cudaStream_t st) {
             ce = launch_decode_fused(*c, a, st);
             break;
         case HC_PATH_PREFILL:
-            ce = launch_prefill(*c, a, true, st);
+            ce = launch_prefill(*c, a, PrefillMode::kFused, st);
+            c->lo_mode = 1;
+            c->lo_tokens = a.T;
+            break;
+        case HC_PATH_PREFILL_BF16_LO:
+            ce = launch_prefill(*c, a, PrefillMode::kFusedBf16Lo, st);
+            c->lo_mode = 2;
+            c->lo_tokens = a.T;
             break;
         default:
             if (c->gated == nullptr) {
@@ -128,7 +135,9 @@ int run(int path, const ReadArgs& a, cudaStream_t st) {
                     return HC_ERR_NOMEM;
                 }
             }
-            ce = launch_prefill(*c, a, false, st);
+            ce = launch_prefill(*c, a, PrefillMode::kUnfused, st);
+            c->lo_mode = 1;
+            c->lo_tokens = a.T;
             break;
     }
     return ce == cudaSuccess ? HC_OK : HC_ERR_CUDA;
@@ -286,26 +295,50 @@ extern "C" int hc_read(int tokens, const float* R, const float* P, const uint16_
                         out_bf16, out_fp16, stream);
 }
 
-extern "C" int hc_read_upmix(int fused, int tokens, const float* R, const float* P,
-                             const float* Rmix, float* out_f32, uint16_t* out_bf16,
-                             uint16_t* out_fp16, void* stream) {
+extern "C" int hc_read_upmix(int path, int tokens, const float* R, const float* P,
+                             const uint16_t* W_up, const float* Rmix, float* out_f32,
+                             uint16_t* out_bf16, uint16_t* out_fp16, void* stream) {
     int err;
     Ctx* c = current_ctx(&err);
     if (!c) return err;
-    // the weights are not used by this stage: validate against harmless stand-ins
+    PrefillMode mode;
+    if (path == HC_PATH_PREFILL) mode = PrefillMode::kFused;
+    else if (path == HC_PATH_PREFILL_UNFUSED) mode = PrefillMode::kUnfused;
+    else if (path == HC_PATH_PREFILL_BF16_LO) mode = PrefillMode::kFusedBf16Lo;
+    else return HC_ERR_ARG;
+    // lo must hold what this stage reads: the last tile-path call's lo, of this form,
+    // for at least these tokens
+    const int want = mode == PrefillMode::kFusedBf16Lo ? 2 : 1;
+    if (tokens > 0 && (c->lo_mode != want || tokens > c->lo_tokens)) return HC_ERR_ARG;
+    // W_down is not used by this stage: validate against a harmless stand-in
     ReadArgs a{tokens, R, P, reinterpret_cast<const uint16_t*>(c->wd16),
-               reinterpret_cast<const uint16_t*>(c->wd16), reinterpret_cast<const uint16_t*>(c->wu16),
+               reinterpret_cast<const uint16_t*>(c->wd16),
+               mode == PrefillMode::kFusedBf16Lo ? W_up : reinterpret_cast<const uint16_t*>(c->wu16),
                Rmix, out_f32, out_bf16, out_fp16};
     if (int e = validate(*c, a)) return e;
     if (tokens == 0) return HC_OK;
-    if (!fused && c->gated == nullptr) {
+    if (mode == PrefillMode::kUnfused && c->gated == nullptr) {
         if (cudaMalloc(&c->gated, sizeof(float) * (size_t)c->max_tokens * kCols) != cudaSuccess) {
             cudaGetLastError();
             c->gated = nullptr;
             return HC_ERR_NOMEM;
         }
     }
-    return launch_prefill_upmix(*c, a, fused != 0, static_cast<cudaStream_t>(stream)) == cudaSuccess
+    return launch_prefill_upmix(*c, a, mode, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? HC_OK
+               : HC_ERR_CUDA;
+}
+
+extern "C" int hc_read_lo_bf16(int tokens, uint16_t* lo_out, void* stream) {
+    int err;
+    Ctx* c = current_ctx(&err);
+    if (!c) return err;
+    if (tokens < 0 || c->lo_mode != 2 || tokens > c->lo_tokens) return HC_ERR_ARG;
+    if (tokens == 0) return HC_OK;
+    if (lo_out == nullptr || (reinterpret_cast<uintptr_t>(lo_out) & 15) != 0) return HC_ERR_ARG;
+    if (int e = check_ptr(lo_out, c->device)) return e;
+    return cudaMemcpyAsync(lo_out, c->lo16, sizeof(uint16_t) * (size_t)tokens * kRank,
+                           cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? HC_OK
                : HC_ERR_CUDA;
 }

@@ -57,6 +57,11 @@ struct Ctx {
     CUtensorMap tm_wd;               // TMA maps over wd16, wu16, lo16
     CUtensorMap tm_wu;
     CUtensorMap tm_lo;
+    CUtensorMap tm_lo_bf16;          // lo16's first term read as bf16 (bf16-lo mode)
+    // what the last tile-path call left in lo16: 0 nothing, 1 two fp16 terms, 2 one
+    // bf16 term; and for how many tokens
+    int lo_mode = 0;
+    int lo_tokens = 0;
 };
 
 struct ReadArgs {
@@ -82,10 +87,12 @@ cudaError_t launch_decode_fused(const Ctx& ctx, const ReadArgs& a, cudaStream_t 
 
 // Prefill (tensor-core tile) path: TMA maps and kernel attributes, then the launch.
 cudaError_t prefill_setup(Ctx& ctx);
-cudaError_t launch_prefill(const Ctx& ctx, const ReadArgs& a, bool fused, cudaStream_t st);
+enum class PrefillMode { kFused, kUnfused, kFusedBf16Lo };
+cudaError_t launch_prefill(const Ctx& ctx, const ReadArgs& a, PrefillMode mode, cudaStream_t st);
 // The two halves of the tile path: weights to fp16, down GEMM and lo split; then the
 // up GEMM with its gate + mix epilogue (fused) or writing gated + the mix (unfused).
-cudaError_t launch_prefill_down(const Ctx& ctx, const ReadArgs& a, cudaStream_t st);
-cudaError_t launch_prefill_upmix(const Ctx& ctx, const ReadArgs& a, bool fused, cudaStream_t st);
+cudaError_t launch_prefill_down(const Ctx& ctx, const ReadArgs& a, PrefillMode mode, cudaStream_t st);
+cudaError_t launch_prefill_upmix(const Ctx& ctx, const ReadArgs& a, PrefillMode mode,
+                                 cudaStream_t st);
 
 }  // namespace hc

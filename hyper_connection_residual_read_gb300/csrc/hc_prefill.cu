@@ -117,9 +117,9 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // ---------------------------------------------------------------------------
 __global__ void convert_weights_kernel(const uint16_t* __restrict__ wd, const uint16_t* __restrict__ wu,
                                        __half* __restrict__ wd16, __half* __restrict__ wu16,
-                                       int n8_each) {
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 2 * n8_each;
-         i += gridDim.x * blockDim.x) {
+                                       int n8_each, bool down_only) {
+    const int n = down_only ? n8_each : 2 * n8_each;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const bool up = i >= n8_each;
         const int j = up ? i - n8_each : i;
         const uint4 v = *reinterpret_cast<const uint4*>((up ? wu : wd) + 8 * (size_t)j);
@@ -384,6 +384,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
 // ---------------------------------------------------------------------------
 // lo = sum of the 4 stream partials (in stream order), split into two fp16 terms
 // ---------------------------------------------------------------------------
+template <bool kBf16>
 __global__ void lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ssq,
                                 __half* __restrict__ lo16, int T, int max_tokens, float eps,
                                 int* __restrict__ status) {
@@ -406,6 +407,12 @@ __global__ void lo_split_kernel(const float* __restrict__ partials, const float*
             v.x = fmaf(rs, d.x, v.x); v.y = fmaf(rs, d.y, v.y);
             v.z = fmaf(rs, d.z, v.z); v.w = fmaf(rs, d.w, v.w);
         }
+        if (kBf16) {
+            // the pages' numerics: lo rounded once to bf16 (nearest even), one term
+            *reinterpret_cast<uint2*>(lo16 + (size_t)t * kRank + j) =
+                make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+            continue;
+        }
         if (fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) >= 65504.f)
             atomicOr(status, kStatusRange);
         uint32_t h0, l0, h1, l1;
@@ -427,7 +434,9 @@ struct EpiMaps {
     CUtensorMap R, P;
 };
 
-template <bool kFused>
+// kTerms = 2: A is lo as two fp16 terms and B the fp16 copy of W_up (fp32-accurate);
+// kTerms = 1: A is lo rounded to bf16 and B the caller's bf16 W_up (one MMA per step).
+template <bool kFused, int kTerms>
 __global__ void __launch_bounds__(kUpThreads, 1)
 upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtensorMap tm_lo,
                   const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ EpiMaps em,
@@ -484,9 +493,10 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     const int slot = it % kUpStages;
                     const uint32_t ph = (it / kUpStages) & 1;
                     if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
-                    mbar_arrive_expect_tx(&full_bar[slot], kUpStageBytes);
-                    tma_load_3d(sA(slot, 0), &tm_lo, kb * kBK, tt * kTileM, 0, &full_bar[slot]);
-                    tma_load_3d(sA(slot, 1), &tm_lo, kb * kBK, tt * kTileM, 1, &full_bar[slot]);
+                    mbar_arrive_expect_tx(&full_bar[slot], kTerms * kTileBytes16 + kUpBBytes);
+#pragma unroll
+                    for (int term = 0; term < kTerms; ++term)
+                        tma_load_3d(sA(slot, term), &tm_lo, kb * kBK, tt * kTileM, term, &full_bar[slot]);
 #pragma unroll
                     for (int s = 0; s < kStreams; ++s)
                         tma_load_2d(sB(slot) + s * (kUpBBytes / kStreams), &tm_wu, kb * kBK,
@@ -496,7 +506,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(kTileM, kUpN);
+            const uint32_t idesc = kTerms == 2 ? idesc_f16_f32(kTileM, kUpN) : idesc_bf16_f32(kTileM, kUpN);
             int it = 0, lt = 0;
             for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
                 const int b = lt & 1;
@@ -510,7 +520,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     tc_fence_after();
                     const uint32_t b0 = smem_u32(sB(slot));
 #pragma unroll
-                    for (int term = 0; term < 2; ++term) {
+                    for (int term = 0; term < kTerms; ++term) {
                         const uint32_t a0 = smem_u32(sA(slot, term));
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
@@ -768,16 +778,29 @@ cudaError_t prefill_setup(Ctx& c) {
     cudaError_t e = cudaFuncSetAttribute(down_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kDownSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(upmix_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    {
+        const cuuint64_t dims[3] = {kRank, (cuuint64_t)c.max_tokens, 1};
+        const cuuint64_t strides[2] = {kRank * 2, (cuuint64_t)c.max_tokens * kRank * 2};
+        const cuuint32_t box[3] = {kBK, kTileM, 1};
+        if (!encode_map(&c.tm_lo_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.lo16, 3, dims, strides,
+                        box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    e = cudaFuncSetAttribute(upmix_tile_kernel<true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kUpSmem);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(upmix_tile_kernel<false>,
+    e = cudaFuncSetAttribute(upmix_tile_kernel<true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kUpSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(upmix_tile_kernel<false, 2>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kUpSmem);
 }
 
-cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, cudaStream_t st) {
+cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, PrefillMode mode, cudaStream_t st) {
     const int n8 = kRank * kCols / 8;
-    convert_weights_kernel<<<2 * c.sm_count, 512, 0, st>>>(a.W_down, a.W_up, c.wd16, c.wu16, n8);
+    // the bf16-lo mode feeds the caller's bf16 W_up to the up GEMM: only W_down is converted
+    convert_weights_kernel<<<2 * c.sm_count, 512, 0, st>>>(a.W_down, a.W_up, c.wd16, c.wu16,
+                                                           n8, mode == PrefillMode::kFusedBf16Lo);
     const int n_tt = (a.T + kTileM - 1) / kTileM;
     const int down_tiles = n_tt * kStreams * kDownKSplit;
     const int down_grid = down_tiles < c.sm_count ? down_tiles : c.sm_count;
@@ -787,12 +810,16 @@ cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, cudaStream_t st
         a.R, a.P, a.w_norm, c.tm_wd, tm_r, c.partials, c.ssq, a.T, c.s.status);
     const int n4 = a.T * (kRank / 4);
     const int rgrid = (n4 + 255) / 256 < 8 * c.sm_count ? (n4 + 255) / 256 : 8 * c.sm_count;
-    lo_split_kernel<<<rgrid, 256, 0, st>>>(c.partials, c.ssq, c.lo16, a.T, c.max_tokens, c.eps,
-                                           c.s.status);
+    if (mode == PrefillMode::kFusedBf16Lo)
+        lo_split_kernel<true><<<rgrid, 256, 0, st>>>(c.partials, c.ssq, c.lo16, a.T, c.max_tokens,
+                                                     c.eps, c.s.status);
+    else
+        lo_split_kernel<false><<<rgrid, 256, 0, st>>>(c.partials, c.ssq, c.lo16, a.T, c.max_tokens,
+                                                      c.eps, c.s.status);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, bool fused, cudaStream_t st) {
+cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mode, cudaStream_t st) {
     const int n_tt = (a.T + kTileM - 1) / kTileM;
     const int up_tiles = n_tt * kUpColTiles;
     const int up_grid = up_tiles < c.sm_count ? up_tiles : c.sm_count;
@@ -801,26 +828,43 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, bool fused, cu
     ok = ok && encode_act(&em.P, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.P ? a.P : a.R, a.T,
                           kEpiCols, kTileM);
     if (!ok) return cudaErrorInvalidValue;
-    if (fused) {
-        upmix_tile_kernel<true><<<up_grid, kUpThreads, kUpSmem, st>>>(
-            a.Rmix, c.tm_lo, c.tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16, a.P != nullptr, a.T,
-            c.s.status);
-    } else {
-        upmix_tile_kernel<false><<<up_grid, kUpThreads, kUpSmem, st>>>(
-            a.Rmix, c.tm_lo, c.tm_wu, em, c.gated, nullptr, nullptr, a.P != nullptr, a.T,
-            c.s.status);
-        const int n = a.T * (kWidth / 4);
-        const int mgrid = (n + 255) / 256 < 8 * c.sm_count ? (n + 255) / 256 : 8 * c.sm_count;
-        mix_gated_kernel<<<mgrid, 256, 0, st>>>(c.gated, a.Rmix, a.out_f32, a.out_bf16, a.out_fp16,
-                                                a.T);
+    const int has_P = a.P != nullptr;
+    switch (mode) {
+        case PrefillMode::kFused:
+            upmix_tile_kernel<true, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
+                a.Rmix, c.tm_lo, c.tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16, has_P, a.T,
+                c.s.status);
+            break;
+        case PrefillMode::kFusedBf16Lo: {
+            CUtensorMap tm_wu_bf16;   // over the caller's W_up [kCols][kRank] bf16
+            const cuuint64_t dims[2] = {kRank, kCols};
+            const cuuint64_t strides[1] = {kRank * 2};
+            const cuuint32_t box[2] = {kBK, kUpCols};
+            if (!encode_map(&tm_wu_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.W_up, 2, dims, strides,
+                            box, CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
+            upmix_tile_kernel<true, 1><<<up_grid, kUpThreads, kUpSmem, st>>>(
+                a.Rmix, c.tm_lo_bf16, tm_wu_bf16, em, a.out_f32, a.out_bf16, a.out_fp16, has_P,
+                a.T, c.s.status);
+            break;
+        }
+        case PrefillMode::kUnfused: {
+            upmix_tile_kernel<false, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
+                a.Rmix, c.tm_lo, c.tm_wu, em, c.gated, nullptr, nullptr, has_P, a.T, c.s.status);
+            const int n = a.T * (kWidth / 4);
+            const int mgrid = (n + 255) / 256 < 8 * c.sm_count ? (n + 255) / 256 : 8 * c.sm_count;
+            mix_gated_kernel<<<mgrid, 256, 0, st>>>(c.gated, a.Rmix, a.out_f32, a.out_bf16,
+                                                    a.out_fp16, a.T);
+            break;
+        }
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, bool fused, cudaStream_t st) {
-    cudaError_t e = launch_prefill_down(c, a, st);
+cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, PrefillMode mode, cudaStream_t st) {
+    cudaError_t e = launch_prefill_down(c, a, mode, st);
     if (e != cudaSuccess) return e;
-    return launch_prefill_upmix(c, a, fused, st);
+    return launch_prefill_upmix(c, a, mode, st);
 }
 
 }  // namespace hc

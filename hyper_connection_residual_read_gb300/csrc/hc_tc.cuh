@@ -164,6 +164,12 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (K-major), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Byte offset of 16-bit element (row r, k) in a K-major 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
     return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 +

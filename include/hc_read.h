@@ -90,8 +90,16 @@ enum hc_path {
     HC_PATH_DECODE = 1,            /* per 8 tokens: sliced down kernel, then up/gate/mix kernel */
     HC_PATH_PREFILL = 2,           /* tile down, fused up + gate + mix epilogue */
     HC_PATH_PREFILL_UNFUSED = 3,   /* tile down, up GEMM writing gated, then the mix */
-    HC_PATH_DECODE_ONE_KERNEL = 4  /* per 8 tokens: one kernel with an in-kernel lo exchange
+    HC_PATH_DECODE_ONE_KERNEL = 4, /* per 8 tokens: one kernel with an in-kernel lo exchange
                                       (HC_ERR_ARG where its 160 CTAs cannot all be resident) */
+    HC_PATH_PREFILL_BF16_LO = 5    /* the pages' prefill numerics: tile down as in
+                                      HC_PATH_PREFILL, then lo rounded once to bf16 and a
+                                      single-term bf16 up GEMM on the caller's W_up with the
+                                      fused epilogue ("#1370 prefill: opt-in STRATA_HC_UPMIX=1
+                                      on CUDA ...", "What it does": the BF16 mma). Its output
+                                      is exact to fp32 tolerance only against the read computed
+                                      from that bf16 lo (hc_read_lo_bf16), not against the
+                                      fp32-accurate read: expect about 1e-3 relative there. */
 };
 
 /* Creates the context of `device` (makes it current), checks that it is sm_103,
@@ -121,16 +129,28 @@ int hc_read_path(int path, int tokens,
                  void* stream);
 
 /* Runs again only the second half of the tile path for the tokens of the most
- * recent HC_PATH_PREFILL / HC_PATH_PREFILL_UNFUSED call on this context: the up
- * projection on the lo that call left in the context's scratch (and the fp16 copy
- * of its W_up), with the gate and the 4x4 mix, fused into the GEMM's epilogue
- * (fused != 0) or as the unfused pair. R, P and Rmix must be that call's (or
- * equal) tensors. Stage timing and the fused-versus-unfused comparison use it;
- * a read needs only hc_read. Same argument checks and errors as hc_read. */
-int hc_read_upmix(int fused, int tokens,
-                  const float* R, const float* P, const float* Rmix,
+ * recent tile-path call on this context: the up projection on the lo that call left
+ * in the context's scratch, with the gate and the 4x4 mix, as `path` says:
+ * HC_PATH_PREFILL (fused epilogue), HC_PATH_PREFILL_UNFUSED (up GEMM writing gated,
+ * then the mix) or HC_PATH_PREFILL_BF16_LO (one bf16 term, fused). The fp16 paths use
+ * the fp16 copy of W_up made by that call and ignore W_up; the bf16 path reads W_up
+ * (bf16, [10240][320]). R, P and Rmix must be that call's (or equal) tensors.
+ * HC_ERR_ARG if the last tile-path call left lo in the other form or for fewer
+ * tokens, or for any path but these three. Stage timing and the fused-versus-unfused
+ * comparison use it; a read needs only hc_read. Otherwise the checks and errors of
+ * hc_read. The pages have no counterpart of it. */
+int hc_read_upmix(int path, int tokens,
+                  const float* R, const float* P, const uint16_t* W_up, const float* Rmix,
                   float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
                   void* stream);
+
+/* Copies the bf16 lo ([tokens][320] bf16 bits, row-major) that the most recent
+ * HC_PATH_PREFILL_BF16_LO call on this context fed to its up GEMM into lo_out
+ * (device memory, 16-byte aligned, caller-owned), asynchronously on `stream`. It is
+ * the stage input that checks of that path condition on. HC_ERR_ARG if the last
+ * tile-path call was not HC_PATH_PREFILL_BF16_LO, tokens exceeds its token count, or
+ * lo_out is null, misaligned or not device memory of the context's device. */
+int hc_read_lo_bf16(int tokens, uint16_t* lo_out, void* stream);
 
 /* Result of the once-per-device self check. */
 typedef struct hc_check_report {

@@ -188,6 +188,17 @@ def hc_read(R, P, w_norm, W_down, W_up, Rmix, eps: float = 1e-6, stages: bool = 
             "out_f32": f32, "out_bf16": b16, "out_fp16": h16}
 
 
+def hc_read_from_lo(R, P, lo, W_up, Rmix):
+    """The read after its down projection, from a given ``lo`` ([T][r], real values):
+    the pending write, then the up projection, gate, mix and images (steps 4-5).
+    With ``lo`` the exact down output it is the whole read. Given the bf16 ``lo`` that
+    a bf16-lo tile path fed to its up GEMM, it is that path's reference: [UPMIX] "What
+    it does" runs the up projection as a BF16 ``mma`` whose A operand is ``lo``."""
+    Rp = pending_write(R, P)
+    u = up(np.asarray(lo, dtype=F64), W_up)
+    return images(mix(gate(u, Rp), Rmix))
+
+
 def hc_read_tokens(token_ids, R, P, w_norm, W_down, W_up, Rmix, eps: float = 1e-6):
     """The read for a subset of tokens of a long chunk (tokens are independent,
     so this equals rows ``token_ids`` of the whole read)."""

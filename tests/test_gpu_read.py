@@ -281,22 +281,79 @@ def test_prefill_fused_equals_unfused_bitwise(weights):
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
 
 
+def _host(o):
+    return (o[0].cpu().numpy(), o[1].cpu().numpy().view(np.uint16),
+            o[2].cpu().numpy().view(np.uint16))
+
+
 def test_upmix_stage_rerun_matches_the_read(weights):
     """The up + gate + mix stage run again on the read's lo gives the read's bits,
-    fused and unfused."""
+    fused and unfused, and on the bf16-lo path; a stage whose lo form does not
+    match the last tile-path call is refused."""
     w, W = weights
     T = 260
     a = synth.make_activations(14, T, True)
     R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
     ref = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL)
-    for fused in (True, False):
+    for path in (hc.HC_PATH_PREFILL, hc.HC_PATH_PREFILL_UNFUSED):
         o = alloc_out(T)
-        hc.hc_read_upmix(fused, T, R, P, M, *o)
+        hc.hc_read_upmix(path, T, R, P, None, M, *o)
         torch.cuda.synchronize()
-        got = (o[0].cpu().numpy(), o[1].cpu().numpy().view(np.uint16),
-               o[2].cpu().numpy().view(np.uint16))
-        for x, y in zip(ref, got):
+        for x, y in zip(ref, _host(o)):
             assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    o = alloc_out(T)
+    with pytest.raises(hc.HcReadError):
+        hc.hc_read_upmix(hc.HC_PATH_PREFILL_BF16_LO, T, R, P, W["W_up"], M, *o)
+    with pytest.raises(hc.HcReadError):
+        hc.hc_read_upmix(hc.HC_PATH_PREFILL, T + 1, R, P, None, M, *o)
+    ref16 = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL_BF16_LO)
+    hc.hc_read_upmix(hc.HC_PATH_PREFILL_BF16_LO, T, R, P, W["W_up"], M, *o)
+    torch.cuda.synchronize()
+    for x, y in zip(ref16, _host(o)):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    with pytest.raises(hc.HcReadError):
+        hc.hc_read_upmix(hc.HC_PATH_PREFILL, T, R, P, None, M, *o)
+
+
+def _bf16_lo(T):
+    lo = torch.empty((T, 320), dtype=torch.int16, device="cuda")
+    hc.hc_read_lo_bf16(T, lo)
+    torch.cuda.synchronize()
+    return lo.cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("T,with_P,seed", [(300, True, 31), (8192, False, 100)])
+def test_bf16_lo_path_against_the_read_from_its_lo(weights, T, with_P, seed):
+    """The pages' prefill numerics: lo rounded once to bf16 for a one-term bf16 up
+    GEMM. Its output matches, to the fp32 tolerance, the oracle's read computed from
+    that same bf16 lo (exported by the library); the exported lo is the bf16
+    rounding of the exact lo, within the fp32 path's own error; and the path is
+    bitwise repeatable."""
+    w, W = weights
+    if T == 8192:
+        a = synth.make_prefill_chunk(seed, T)
+        a["P"] = None
+    else:
+        a = synth.make_activations(seed, T, with_P)
+    R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+    got = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL_BF16_LO)
+    lo_bits = _bf16_lo(T)
+    rng = np.random.default_rng(seed)
+    idx = np.arange(T) if T <= 512 else np.unique(np.concatenate(
+        [np.arange(128), np.arange(T - 128, T), rng.choice(T, 256, replace=False)]))
+    Ps = None if a["P"] is None else a["P"][idx]
+    lo = O.bf16_bits_to_f64(lo_bits[idx])
+    want = O.hc_read_from_lo(a["R"][idx], Ps, lo, w["W_up"], a["Rmix"][idx])
+    assert_matches_oracle(tuple(x[idx] for x in got), want)
+    exact = O.hc_read(a["R"][idx], Ps, w["w_norm"], w["W_down"], w["W_up"], a["Rmix"][idx],
+                      EPS, stages=True)["lo"]
+    # half a bf16 ulp of rounding (at most 2^-8 of the value), plus the fp32 path's error
+    bound = np.abs(exact) * 2.0 ** -8 + 2e-6 * np.abs(exact).max()
+    assert np.all(np.abs(lo - exact) <= bound)
+    again = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL_BF16_LO)
+    for x, y in zip(got, again):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    assert hc.hc_read_status() == 0
 
 
 def test_prefill_bitwise_repeatable_and_pending_write(weights):

@@ -421,3 +421,23 @@ def test_planted_mistakes_are_caught(name, monkeypatch):
     monkeypatch.setattr(O, name.strip(), fn)
     errs = compare_to_brute(3, 2, 4, 8, 3, True, 0.5, dyadic=False)
     assert max(errs.values()) > 1e-6, (name, errs)
+
+
+def test_read_from_lo_is_the_read_after_its_down_projection():
+    """hc_read_from_lo on the exact lo reproduces the whole read bit for bit (same
+    float64 steps); on a different lo it differs, so lo is really its input."""
+    rng = np.random.default_rng(77)
+    T, n, C, r = 3, 4, 16, 5
+    R = rng.standard_normal((T, n, C)).astype(np.float32)
+    P = (0.1 * rng.standard_normal((T, n, C))).astype(np.float32)
+    w_norm = O.f32_to_bf16_bits((1 + 0.1 * rng.standard_normal((n, C))).astype(np.float32))
+    W_down = O.f32_to_bf16_bits((0.2 * rng.standard_normal((r, n * C))).astype(np.float32))
+    W_up = O.f32_to_bf16_bits((0.2 * rng.standard_normal((n * C, r))).astype(np.float32))
+    logits = rng.standard_normal((T, n, n))
+    Rmix = (np.exp(logits) / np.exp(logits).sum(-1, keepdims=True)).astype(np.float32)
+    st = O.hc_read(R, P, w_norm, W_down, W_up, Rmix, 1e-6, stages=True)
+    got = O.hc_read_from_lo(R, P, st["lo"], W_up, Rmix)
+    for x, y in zip(got, (st["out_f32"], st["out_bf16"], st["out_fp16"])):
+        assert np.array_equal(x, y)
+    other = O.hc_read_from_lo(R, P, st["lo"] * 1.5, W_up, Rmix)
+    assert not np.array_equal(other[0], st["out_f32"])
