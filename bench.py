@@ -438,6 +438,14 @@ def gpu_arm(args) -> None:
         ms_read = timed(chunk, reps, 3) / reps          # leaves this chunk's lo in scratch
         ms_fused = timed(upmix_fused, reps, 3) / reps
         ms_pair = timed(upmix_pair, reps, 3) / reps
+        oy = tuple(torch.empty((T, 2560), dtype=dt, device=dev)
+                   for dt in (torch.float32, torch.int16, torch.int16))
+
+        def chunk_y(k):
+            hc.hc_read_y(T, R, None, W0["w_norm"], W0["W_down"], W0["W_up"], *oy, stream=stream)
+
+        ms_read_y = timed(chunk_y, reps, 3) / reps      # the 2560-wide read-out
+        del oy
         ms_read16 = timed(chunk_bf16, reps, 3) / reps   # the pages' bf16-lo numerics
         ms_up16 = timed(upmix_bf16, reps, 3) / reps
         fused_gbps = prefill_upmix_bytes(T) / (ms_fused * 1e-3) / 1e9
@@ -450,7 +458,9 @@ def gpu_arm(args) -> None:
             "upmix_fused_frac": fused_gbps / peaks["hbm_gbs"],
             "upmix_unfused_pair_ms": ms_pair, "fused_speedup": ms_pair / ms_fused,
             "bf16_lo_read_ms": ms_read16, "bf16_lo_upmix_ms": ms_up16,
-            "bf16_lo_upmix_frac": up16_gbps / peaks["hbm_gbs"]}
+            "bf16_lo_upmix_frac": up16_gbps / peaks["hbm_gbs"],
+            "readout_y_read_ms": ms_read_y,
+            "readout_y_read_gbps": (WEIGHT_BYTES + T * (40960 + 20480)) / (ms_read_y * 1e-3) / 1e9}
         del R, M, o
 
     # --- decode / prefill crossover: both paths on the same reads (one weight set,

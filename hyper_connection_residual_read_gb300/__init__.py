@@ -7,7 +7,7 @@ missing: there is no fallback implementation.
 from . import synth  # noqa: F401
 
 _BINDING = ("hc_read_init", "hc_read", "hc_read_path", "hc_read_check", "hc_read_status",
-            "hc_read_noalloc", "hc_read_upmix", "hc_read_lo_bf16",
+            "hc_read_noalloc", "hc_read_upmix", "hc_read_lo_bf16", "hc_read_y",
             "hc_read_shutdown", "hc_read_version", "strerror", "HcReadError", "load",
             "HC_PATH_AUTO", "HC_PATH_DECODE", "HC_PATH_PREFILL", "HC_PATH_PREFILL_UNFUSED",
             "HC_PATH_DECODE_ONE_KERNEL", "HC_PATH_PREFILL_BF16_LO",

@@ -35,7 +35,7 @@ STREAMS, WIDTH, RANK = 4, 2560, 320
 # every symbol include/hc_read.h declares
 EXPORTS = ("hc_read_init", "hc_read", "hc_read_path", "hc_read_check", "hc_read_status",
            "hc_read_strerror", "hc_read_shutdown", "hc_read_version", "hc_read_noalloc",
-           "hc_read_upmix", "hc_read_lo_bf16")
+           "hc_read_upmix", "hc_read_lo_bf16", "hc_read_y")
 
 
 class HcReadError(RuntimeError):
@@ -97,6 +97,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_read_noalloc.restype = i32
     lib.hc_read_upmix.argtypes = [i32, i32] + [vp] * 8
     lib.hc_read_upmix.restype = i32
+    lib.hc_read_y.argtypes = [i32] + [vp] * 9
+    lib.hc_read_y.restype = i32
     lib.hc_read_lo_bf16.argtypes = [i32, vp, vp]
     lib.hc_read_lo_bf16.restype = i32
     _lib = lib
@@ -172,6 +174,15 @@ def hc_read_upmix(path, tokens, R, P, W_up, Rmix, out_f32, out_bf16, out_fp16,
     _check("hc_read_upmix", load().hc_read_upmix(
         path, tokens, _ptr(R), _ptr(P), _ptr(W_up), _ptr(Rmix), _ptr(out_f32), _ptr(out_bf16),
         _ptr(out_fp16), _stream(stream)))
+
+
+def hc_read_y(tokens, R, P, w_norm, W_down, W_up, out_f32, out_bf16, out_fp16,
+              stream=None) -> None:
+    """The read with the 2560-wide read-out y = sum of the gated streams ([T][2560]
+    fp32 and its bf16 / fp16 images) instead of the 4x4 mix."""
+    _check("hc_read_y", load().hc_read_y(
+        tokens, _ptr(R), _ptr(P), _ptr(w_norm), _ptr(W_down), _ptr(W_up), _ptr(out_f32),
+        _ptr(out_bf16), _ptr(out_fp16), _stream(stream)))
 
 
 def hc_read_lo_bf16(tokens, lo_out, stream=None) -> None:

@@ -71,23 +71,26 @@ int check_ptr(const void* p, int device) {
 
 int validate(const Ctx& c, const ReadArgs& a) {
     if (a.T < 0 || a.T > c.max_tokens) return HC_ERR_ARG;
-    const void* ptrs[] = {a.R, a.w_norm, a.W_down, a.W_up, a.Rmix, a.out_f32, a.out_bf16,
-                          a.out_fp16};
+    // the y read-out has no mix matrix (Rmix is null there and not checked)
+    const bool y = a.out_cols == kWidth;
+    const void* ptrs[] = {a.R, a.w_norm, a.W_down, a.W_up, y ? a.R : a.Rmix, a.out_f32,
+                          a.out_bf16, a.out_fp16};
     for (const void* p : ptrs)
         if (int e = check_ptr(p, c.device)) return e;
     if (a.P != nullptr)
         if (int e = check_ptr(a.P, c.device)) return e;
     const size_t act = (size_t)a.T * kCols;
+    const size_t out = (size_t)a.T * a.out_cols;
     auto rng = [](const void* p, size_t bytes) {
         uintptr_t b = reinterpret_cast<uintptr_t>(p);
         return Range{b, b + bytes};
     };
-    const Range outs[3] = {rng(a.out_f32, act * 4), rng(a.out_bf16, act * 2),
-                           rng(a.out_fp16, act * 2)};
+    const Range outs[3] = {rng(a.out_f32, out * 4), rng(a.out_bf16, out * 2),
+                           rng(a.out_fp16, out * 2)};
     Range ins[6] = {rng(a.R, act * 4), rng(a.w_norm, (size_t)kCols * 2),
                     rng(a.W_down, (size_t)kRank * kCols * 2),
-                    rng(a.W_up, (size_t)kCols * kRank * 2), rng(a.Rmix, (size_t)a.T * 64),
-                    Range{0, 0}};
+                    rng(a.W_up, (size_t)kCols * kRank * 2),
+                    y ? Range{0, 0} : rng(a.Rmix, (size_t)a.T * 64), Range{0, 0}};
     if (a.P) ins[5] = rng(a.P, act * 4);
     for (int i = 0; i < 3; ++i) {
         for (int j = i + 1; j < 3; ++j)
@@ -327,6 +330,22 @@ extern "C" int hc_read_upmix(int path, int tokens, const float* R, const float* 
     return launch_prefill_upmix(*c, a, mode, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? HC_OK
                : HC_ERR_CUDA;
+}
+
+extern "C" int hc_read_y(int tokens, const float* R, const float* P, const uint16_t* w_norm,
+                         const uint16_t* W_down, const uint16_t* W_up, float* out_f32,
+                         uint16_t* out_bf16, uint16_t* out_fp16, void* stream) {
+    int err;
+    Ctx* c = current_ctx(&err);
+    if (!c) return err;
+    ReadArgs a{tokens, R, P, w_norm, W_down, W_up, nullptr, out_f32, out_bf16, out_fp16, kWidth};
+    if (int e = validate(*c, a)) return e;
+    if (tokens == 0) return HC_OK;
+    const cudaError_t ce = launch_prefill(*c, a, PrefillMode::kReadoutY,
+                                          static_cast<cudaStream_t>(stream));
+    c->lo_mode = 1;
+    c->lo_tokens = tokens;
+    return ce == cudaSuccess ? HC_OK : HC_ERR_CUDA;
 }
 
 extern "C" int hc_read_lo_bf16(int tokens, uint16_t* lo_out, void* stream) {

@@ -75,6 +75,7 @@ struct ReadArgs {
     float* out_f32;
     uint16_t* out_bf16;
     uint16_t* out_fp16;
+    int out_cols = kCols;            // output floats per token (kWidth for the y read-out)
 };
 
 // Decode kernels for any T: launched in chunks of kDecodeMaxT tokens.
@@ -87,7 +88,8 @@ cudaError_t launch_decode_fused(const Ctx& ctx, const ReadArgs& a, cudaStream_t 
 
 // Prefill (tensor-core tile) path: TMA maps and kernel attributes, then the launch.
 cudaError_t prefill_setup(Ctx& ctx);
-enum class PrefillMode { kFused, kUnfused, kFusedBf16Lo };
+// kReadoutY: the 2560-wide read-out y = sum of the gated streams, [T][2560] outputs.
+enum class PrefillMode { kFused, kUnfused, kFusedBf16Lo, kReadoutY };
 cudaError_t launch_prefill(const Ctx& ctx, const ReadArgs& a, PrefillMode mode, cudaStream_t st);
 // The two halves of the tile path: weights to fp16, down GEMM and lo split; then the
 // up GEMM with its gate + mix epilogue (fused) or writing gated + the mix (unfused).

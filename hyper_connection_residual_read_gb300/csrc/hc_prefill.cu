@@ -434,9 +434,13 @@ struct EpiMaps {
     CUtensorMap R, P;
 };
 
+// kOut: what the epilogue writes. kOutGated: gated (fp32, the unfused pair's first
+// half); kOutMix: the 4x4 mix with the bf16/fp16 images; kOutY: the 2560-wide
+// read-out y[c] = sum_s gated[s][c] (streams in order) with its images.
 // kTerms = 2: A is lo as two fp16 terms and B the fp16 copy of W_up (fp32-accurate);
 // kTerms = 1: A is lo rounded to bf16 and B the caller's bf16 W_up (one MMA per step).
-template <bool kFused, int kTerms>
+constexpr int kOutGated = 0, kOutMix = 1, kOutY = 2;
+template <int kOut, int kTerms>
 __global__ void __launch_bounds__(kUpThreads, 1)
 upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtensorMap tm_lo,
                   const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ EpiMaps em,
@@ -453,6 +457,8 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = ((T + kTileM - 1) / kTileM) * kUpColTiles;
     constexpr int kSteps = kUpCols / kEpiCols;   // 8 epilogue steps per tile
+    constexpr int kOutStreams = kOut == kOutY ? 1 : kStreams;   // output rows per token
+    constexpr size_t kRowStride = kOut == kOutY ? kWidth : kCols;   // output floats per token
     // with a pending write a step needs two slots (R, then P)
     const int slots_per_step = has_P ? 2 : 1;
 
@@ -567,7 +573,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
             const int t = tt * kTileM + row;
             const bool valid = t < T;
             float mx[16];
-            if (kFused) {
+            if (kOut == kOutMix) {
                 if (valid) {
                     const float4* m4 = reinterpret_cast<const float4*>(Rmix + (size_t)t * 16);
 #pragma unroll
@@ -588,7 +594,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
 #pragma unroll 1
             for (int pi = 0; pi < 2 && ok; ++pi) {
                 const int k0 = 4 * pi + 2 * g;
-                uint32_t bb[kStreams][8], hh[kStreams][8];   // 16 columns of the images
+                uint32_t bb[kOutStreams][8], hh[kOutStreams][8];   // 16 columns of the images
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const int k = k0 + j;
@@ -619,16 +625,22 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
 #pragma unroll
                         for (int e = 0; e < kEpiCols; ++e) v[s][e] = gate_value(v[s][e], rp[s][e]);
 #pragma unroll
-                    for (int so = 0; so < kStreams; ++so) {
+                    for (int so = 0; so < kOutStreams; ++so) {
                         float o[kEpiCols];
 #pragma unroll
-                        for (int e = 0; e < kEpiCols; ++e)
-                            o[e] = kFused ? mix_row(&mx[so * 4], v[0][e], v[1][e], v[2][e], v[3][e]) : v[so][e];
+                        for (int e = 0; e < kEpiCols; ++e) {
+                            if (kOut == kOutMix)
+                                o[e] = mix_row(&mx[so * 4], v[0][e], v[1][e], v[2][e], v[3][e]);
+                            else if (kOut == kOutY)
+                                o[e] = ((v[0][e] + v[1][e]) + v[2][e]) + v[3][e];
+                            else
+                                o[e] = v[so][e];
+                        }
                         uint32_t w[8];
 #pragma unroll
                         for (int e = 0; e < kEpiCols; ++e) w[e] = __float_as_uint(o[e]);
-                        if (valid) st_global_v8(out_f32 + (size_t)t * kCols + so * kWidth + c, w);
-                        if (kFused) {
+                        if (valid) st_global_v8(out_f32 + (size_t)t * kRowStride + so * kWidth + c, w);
+                        if (kOut != kOutGated) {
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 bb[so][4 * j + i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
@@ -638,10 +650,10 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     }
                 }
                 if (!ok) break;
-                if (kFused && valid) {
-                    const size_t off = (size_t)t * kCols + ct * kUpCols + k0 * kEpiCols;
+                if (kOut != kOutGated && valid) {
+                    const size_t off = (size_t)t * kRowStride + ct * kUpCols + k0 * kEpiCols;
 #pragma unroll
-                    for (int so = 0; so < kStreams; ++so) {
+                    for (int so = 0; so < kOutStreams; ++so) {
                         st_global_v8(out_bf16 + off + so * kWidth, bb[so]);
                         st_global_v8(out_fp16 + off + so * kWidth, hh[so]);
                     }
@@ -786,13 +798,16 @@ cudaError_t prefill_setup(Ctx& c) {
                         box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
-    e = cudaFuncSetAttribute(upmix_tile_kernel<true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(upmix_tile_kernel<kOutMix, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kUpSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(upmix_tile_kernel<true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(upmix_tile_kernel<kOutMix, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kUpSmem);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(upmix_tile_kernel<false, 2>,
+    e = cudaFuncSetAttribute(upmix_tile_kernel<kOutY, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kUpSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(upmix_tile_kernel<kOutGated, 2>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kUpSmem);
 }
 
@@ -831,7 +846,7 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
     const int has_P = a.P != nullptr;
     switch (mode) {
         case PrefillMode::kFused:
-            upmix_tile_kernel<true, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
+            upmix_tile_kernel<kOutMix, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
                 a.Rmix, c.tm_lo, c.tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16, has_P, a.T,
                 c.s.status);
             break;
@@ -843,13 +858,18 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
             if (!encode_map(&tm_wu_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.W_up, 2, dims, strides,
                             box, CU_TENSOR_MAP_SWIZZLE_128B))
                 return cudaErrorInvalidValue;
-            upmix_tile_kernel<true, 1><<<up_grid, kUpThreads, kUpSmem, st>>>(
+            upmix_tile_kernel<kOutMix, 1><<<up_grid, kUpThreads, kUpSmem, st>>>(
                 a.Rmix, c.tm_lo_bf16, tm_wu_bf16, em, a.out_f32, a.out_bf16, a.out_fp16, has_P,
                 a.T, c.s.status);
             break;
         }
+        case PrefillMode::kReadoutY:
+            upmix_tile_kernel<kOutY, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
+                nullptr, c.tm_lo, c.tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16, has_P, a.T,
+                c.s.status);
+            break;
         case PrefillMode::kUnfused: {
-            upmix_tile_kernel<false, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
+            upmix_tile_kernel<kOutGated, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
                 a.Rmix, c.tm_lo, c.tm_wu, em, c.gated, nullptr, nullptr, has_P, a.T, c.s.status);
             const int n = a.T * (kWidth / 4);
             const int mgrid = (n + 255) / 256 < 8 * c.sm_count ? (n + 255) / 256 : 8 * c.sm_count;

@@ -144,6 +144,21 @@ int hc_read_upmix(int path, int tokens,
                   float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
                   void* stream);
 
+/* The read with a 2560-wide read-out instead of the 4x4 mix: per token and column,
+ * y[c] = gated[0][c] + gated[1][c] + gated[2][c] + gated[3][c] (streams summed in
+ * that order in fp32), written as out_f32 [T][2560] fp32 and its round-to-nearest-
+ * even bf16 / fp16 images out_bf16, out_fp16 [T][2560]. Steps 1-4 are those of
+ * hc_read (tensor-core tile path, fp32-accurate, any T). The pages have no entry
+ * point of this shape: it is the read-out under which "#1370 prefill: opt-in
+ * STRATA_HC_UPMIX=1 on CUDA ...", "Why" (gr_mix_r moving about 102 KB per token)
+ * adds up, 40 KB of gated and 40 KB of residual in and a 2560-wide fp32 + bf16 +
+ * fp16 row out. Same checks and errors as hc_read, with no Rmix. */
+int hc_read_y(int tokens,
+              const float* R, const float* P,
+              const uint16_t* w_norm, const uint16_t* W_down, const uint16_t* W_up,
+              float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
+              void* stream);
+
 /* Copies the bf16 lo ([tokens][320] bf16 bits, row-major) that the most recent
  * HC_PATH_PREFILL_BF16_LO call on this context fed to its up GEMM into lo_out
  * (device memory, 16-byte aligned, caller-owned), asynchronously on `stream`. It is

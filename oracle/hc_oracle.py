@@ -157,6 +157,17 @@ def mix(gated: np.ndarray, Rmix: np.ndarray) -> np.ndarray:
     return out
 
 
+def readout_y(gated: np.ndarray) -> np.ndarray:
+    """The 2560-wide read-out: ``y[c] = sum_q gated[q][c]``, streams in order q =
+    0..3. It is the read-out under which [UPMIX] "Why" (``gr_mix_r`` moving about
+    102 KB per token: gated and residual in, one fp32 + bf16 + fp16 row of width
+    C out) adds up; with it the images are taken of ``y`` as of ``mixed``."""
+    y = gated[:, 0, :].copy()
+    for q in range(1, gated.shape[1]):
+        y = y + gated[:, q, :]
+    return y
+
+
 def images(mixed: np.ndarray):
     """Step 5, outputs: ``mixed`` rounded once to fp32, and the bf16 and fp16
     images of that fp32 value (reading 7). [UPMIX] "What it does" ("writes
@@ -197,6 +208,14 @@ def hc_read_from_lo(R, P, lo, W_up, Rmix):
     Rp = pending_write(R, P)
     u = up(np.asarray(lo, dtype=F64), W_up)
     return images(mix(gate(u, Rp), Rmix))
+
+
+def hc_read_y(R, P, w_norm, W_down, W_up, eps: float = 1e-6):
+    """The read with ``readout_y`` in place of the mix: ``(y_f32, y_bf16, y_fp16)``,
+    each [T][C]."""
+    Rp = pending_write(R, P)
+    lo = down(normalise(Rp, w_norm, rms_scale(Rp, eps)), W_down)
+    return images(readout_y(gate(up(lo, W_up), Rp)))
 
 
 def hc_read_tokens(token_ids, R, P, w_norm, W_down, W_up, Rmix, eps: float = 1e-6):

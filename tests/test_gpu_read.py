@@ -382,3 +382,32 @@ def test_decode_and_prefill_paths_agree(weights):
         p = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL)
         from _hc import rel_diff
         assert rel_diff(d[0], p[0]) <= 2 * TOL_F32
+
+
+@pytest.mark.parametrize("T,with_P,seed", [(1, True, 41), (129, True, 42), (300, False, 43),
+                                           (8192, False, 101)])
+def test_readout_y_against_oracle(weights, T, with_P, seed):
+    """The 2560-wide read-out (y = sum of the gated streams, with its images) through
+    hc_read_y, against the oracle's; long chunks on sampled tokens."""
+    w, W = weights
+    if T == 8192:
+        a = synth.make_prefill_chunk(seed, T)
+        a["P"] = None
+    else:
+        a = synth.make_activations(seed, T, with_P)
+    R, P = dev_f32(a["R"]), dev_f32(a["P"])
+    shape = (T, synth.WIDTH)
+    o = (torch.empty(shape, dtype=torch.float32, device="cuda"),
+         torch.empty(shape, dtype=torch.int16, device="cuda"),
+         torch.empty(shape, dtype=torch.int16, device="cuda"))
+    hc.hc_read_y(T, R, P, W["w_norm"], W["W_down"], W["W_up"], *o)
+    torch.cuda.synchronize()
+    got = _host(o)
+    rng = np.random.default_rng(seed)
+    idx = np.arange(T) if T <= 512 else np.unique(np.concatenate(
+        [np.arange(128), np.arange(T - 128, T), rng.choice(T, 256, replace=False)]))
+    Ps = None if a["P"] is None else a["P"][idx]
+    want = O.hc_read_y(a["R"][idx], Ps, w["w_norm"], w["W_down"], w["W_up"], EPS)
+    assert_matches_oracle(tuple(x[idx] for x in got), want)
+    assert bool(torch.isfinite(o[0]).all())
+    assert hc.hc_read_status() == 0

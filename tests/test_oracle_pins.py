@@ -441,3 +441,25 @@ def test_read_from_lo_is_the_read_after_its_down_projection():
         assert np.array_equal(x, y)
     other = O.hc_read_from_lo(R, P, st["lo"] * 1.5, W_up, Rmix)
     assert not np.array_equal(other[0], st["out_f32"])
+
+
+def test_readout_y_is_the_mix_with_a_row_of_ones():
+    """y = sum of the gated streams equals output stream 0 of the read whose mix
+    matrix has an all-ones first row (the mix is pinned by brute force and by the
+    permutation test), bit for bit: multiplying by 1 is exact and both sum q = 0..3
+    in order."""
+    rng = np.random.default_rng(78)
+    T, n, C, r = 3, 4, 16, 5
+    R = rng.standard_normal((T, n, C)).astype(np.float32)
+    P = (0.1 * rng.standard_normal((T, n, C))).astype(np.float32)
+    w_norm = O.f32_to_bf16_bits((1 + 0.1 * rng.standard_normal((n, C))).astype(np.float32))
+    W_down = O.f32_to_bf16_bits((0.2 * rng.standard_normal((r, n * C))).astype(np.float32))
+    W_up = O.f32_to_bf16_bits((0.2 * rng.standard_normal((n * C, r))).astype(np.float32))
+    ones = np.ones((T, n, n), dtype=np.float32)
+    full = O.hc_read(R, P, w_norm, W_down, W_up, ones, 1e-6)
+    y = O.hc_read_y(R, P, w_norm, W_down, W_up, 1e-6)
+    for a, b in zip(y, full):
+        assert np.array_equal(a, b[:, 0, :])
+    # and it is the plain sum of the gated streams of the staged read
+    st = O.hc_read(R, P, w_norm, W_down, W_up, ones, 1e-6, stages=True)
+    assert np.allclose(O.readout_y(st["gated"]), st["gated"].sum(axis=1), rtol=1e-15, atol=0)
