@@ -411,3 +411,27 @@ def test_readout_y_against_oracle(weights, T, with_P, seed):
     assert_matches_oracle(tuple(x[idx] for x in got), want)
     assert bool(torch.isfinite(o[0]).all())
     assert hc.hc_read_status() == 0
+
+
+def test_back_to_back_tile_reads_do_not_see_each_others_scratch(weights):
+    """Tile-path reads of alternating kinds (bf16 lo, then fp32-accurate) enqueued back
+    to back with no synchronisation: each must give the bits of the same read run
+    alone, so no kernel may read scratch (lo, partials) before the previous kernel
+    has written it or after the next read has overwritten it."""
+    w, W = weights
+    T = 4096
+    c = synth.make_prefill_chunk(102, T)
+    R, M = dev_f32(c["R"]), dev_f32(c["Rmix"])
+    ref = gpu_read(T, R, None, W, M, hc.HC_PATH_PREFILL)
+    ref16 = gpu_read(T, R, None, W, M, hc.HC_PATH_PREFILL_BF16_LO)
+    outs = []
+    for _ in range(6):
+        for path in (hc.HC_PATH_PREFILL_BF16_LO, hc.HC_PATH_PREFILL):
+            o = alloc_out(T)
+            hc.hc_read_path(path, T, R, None, W["w_norm"], W["W_down"], W["W_up"], M, *o)
+            outs.append((path, o))
+    torch.cuda.synchronize()
+    for path, o in outs:
+        want = ref16 if path == hc.HC_PATH_PREFILL_BF16_LO else ref
+        for x, y in zip(want, _host(o)):
+            assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
