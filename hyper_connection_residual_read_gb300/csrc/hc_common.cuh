@@ -16,6 +16,12 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
     return v;
 }
 
+// Asks L2 to fetch the line holding p. It returns nothing, so it may run before the
+// data is final: a later write updates the L2 line and a later load reads it there.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Programmatic dependent launch. A kernel launched with programmatic stream
 // serialisation may start while the previous kernel on the stream is still
 // running; `pdl_wait` blocks until that kernel has completed and its writes are

@@ -97,6 +97,14 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
     // first half of a cluster barrier: the wait before the pushes of step 4 then
     // finds every CTA of the cluster started (their shared memory exists)
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    // the activations into L2 while the previous kernel finishes (read after the wait)
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+        if ((tid & 7) == 0) {   // one prefetch per 128-byte line
+            prefetch_l2(R + (size_t)t * kCols + k0 + 4 * tid);
+            if (P != nullptr) prefetch_l2(P + (size_t)t * kCols + k0 + 4 * tid);
+        }
+    }
     pdl_launch_dependents();
     pdl_wait();
 
@@ -235,6 +243,14 @@ up_mix_kernel(const float* R, const float* P, const uint16_t* __restrict__ W_up,
         const uint16_t* wrow = W_up + (size_t)(st * kWidth + c) * kRank + part * 40;
 #pragma unroll
         for (int q = 0; q < 5; ++q) wv[st][q] = ldg_stream_v4(wrow + 8 * q);
+    }
+    // this lane's residual (and pending write) into L2 while the down kernel runs
+    if (part < 4) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+            prefetch_l2(R + (size_t)t * kCols + sp * kWidth + c);
+            if (P != nullptr) prefetch_l2(P + (size_t)t * kCols + sp * kWidth + c);
+        }
     }
     pdl_launch_dependents();
     pdl_wait();
