@@ -317,7 +317,9 @@ def gpu_arm(args) -> None:
     step_bytes = sum(read_bytes(T, p) for T, p in SWEEP)
 
     # --- per-T times (graph of 48 reads of one T over the 48 sets), for each decode path ---
-    def per_t_times(path, Ts, with_p=(False, True)):
+    def per_t_times(path, Ts, with_p=(False, True), warm=False):
+        """µs per read at each T, 48 reads per graph: weights rotated over the 48 sets
+        (cold, from HBM) or, with ``warm``, one set for every read (L2-resident)."""
         out = {}
         for T in Ts:
             for p in with_p:
@@ -329,7 +331,7 @@ def gpu_arm(args) -> None:
 
                 def enqueue():
                     for i in range(N_SETS):
-                        W = sets[i]
+                        W = sets[0 if warm else i]
                         hc.hc_read_path(path, T, R, Pd, W["w_norm"], W["W_down"], W["W_up"], M,
                                         *o, stream=stream)
                 with torch.cuda.stream(stream):
@@ -344,6 +346,10 @@ def gpu_arm(args) -> None:
         return out
 
     per_t = per_t_times(hc.HC_PATH_AUTO, (1, 4, 8))
+    # the same reads with one weight set (13 MB, resident in L2): the latency floor of
+    # the kernels without the HBM weight stream
+    per_t_warm = {k: round(v["us"], 2)
+                  for k, v in per_t_times(hc.HC_PATH_DECODE, range(1, 9), (True,), warm=True).items()}
     per_t_paths = {name: {k: round(v["us"], 2) for k, v in per_t_times(path, range(1, 9), (True,)).items()}
                    for name, path in (("two_kernels", hc.HC_PATH_DECODE),
                                       ("one_kernel", hc.HC_PATH_DECODE_ONE_KERNEL))}
@@ -503,6 +509,7 @@ def gpu_arm(args) -> None:
         "gpu_launches": kernel_launches_per_step * args.steps,
         "decode_by_T": per_t,
         "decode_paths_us_by_T_with_P": per_t_paths,
+        "decode_warm_weights_us_by_T_with_P": per_t_warm,
         "cold_round_96x_T4_P": cold_round,
         "prefill": prefill,
         "crossover_us_per_read": crossover,

@@ -432,6 +432,7 @@ __global__ void lo_split_kernel(const float* __restrict__ partials, const float*
 // ---------------------------------------------------------------------------
 struct EpiMaps {
     CUtensorMap R, P;
+    CUtensorMap out;   // out_f32 in boxes of 8 columns x 1 stream x 32 tokens (mix only)
 };
 
 // kOut: what the epilogue writes. kOutGated: gated (fp32, the unfused pair's first
@@ -458,6 +459,10 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
     const int n_tiles = ((T + kTileM - 1) / kTileM) * kUpColTiles;
     constexpr int kSteps = kUpCols / kEpiCols;   // 8 epilogue steps per tile
     constexpr int kOutStreams = kOut == kOutY ? 1 : kStreams;   // output rows per token
+    // the mix writes its fp32 rows back into the step's R slot, in place of R, and
+    // stores them from there by TMA (one 1 KB box per stream and warp); the slot is
+    // released once that store has read it
+    constexpr bool kTmaOut = kOut == kOutMix;
     constexpr size_t kRowStride = kOut == kOutY ? kWidth : kCols;   // output floats per token
     // with a pending write a step needs two slots (R, then P)
     const int slots_per_step = has_P ? 2 : 1;
@@ -603,9 +608,11 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     tmem_ld8x4<kUpCols>(tbase + k * kEpiCols, v);
                     // R' of this lane's token: slot layout [stream][128 tokens][8 columns]
                     float rp[kStreams][kEpiCols];
+                    int rslot = 0;
                     for (int which = 0; which < slots_per_step; ++which) {
                         const int u = u_tile + k * slots_per_step + which;
                         const int slot = u % kRSlots;
+                        if (which == 0) rslot = slot;
                         if (!mbar_wait(&r_full[slot], (u / kRSlots) & 1, &abort_flag, status)) { ok = false; break; }
 #pragma unroll
                         for (int s = 0; s < kStreams; ++s) {
@@ -617,7 +624,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                             for (int e = 0; e < kEpiCols; ++e) rp[s][e] = which ? rp[s][e] + x[e] : x[e];
                         }
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&r_empty[slot]);
+                        if (lane == 0 && !(kTmaOut && which == 0)) mbar_arrive(&r_empty[slot]);
                     }
                     if (!ok) break;
 #pragma unroll
@@ -636,10 +643,17 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                             else
                                 o[e] = v[so][e];
                         }
-                        uint32_t w[8];
+                        if (kTmaOut) {
+                            float4* f4 = reinterpret_cast<float4*>(
+                                rring + rslot * kRSlot + so * (kRSlot / kStreams) + row * 32);
+                            f4[0] = make_float4(o[0], o[1], o[2], o[3]);
+                            f4[1] = make_float4(o[4], o[5], o[6], o[7]);
+                        } else {
+                            uint32_t w[8];
 #pragma unroll
-                        for (int e = 0; e < kEpiCols; ++e) w[e] = __float_as_uint(o[e]);
-                        if (valid) st_global_v8(out_f32 + (size_t)t * kRowStride + so * kWidth + c, w);
+                            for (int e = 0; e < kEpiCols; ++e) w[e] = __float_as_uint(o[e]);
+                            if (valid) st_global_v8(out_f32 + (size_t)t * kRowStride + so * kWidth + c, w);
+                        }
                         if (kOut != kOutGated) {
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
@@ -647,6 +661,22 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                                 hh[so][4 * j + i] = pack_f16x2(o[2 * i], o[2 * i + 1]);
                             }
                         }
+                    }
+                    if (kTmaOut) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int t0 = tt * kTileM + q * kEpiRows;
+#pragma unroll
+                            for (int so = 0; so < kStreams; ++so)
+                                tma_store_3d(&em.out, c, so, t0,
+                                             rring + rslot * kRSlot + so * (kRSlot / kStreams) +
+                                                 q * kEpiRows * 32);
+                            bulk_commit();
+                            bulk_wait_read_all();   // the slot may be refilled after this
+                            mbar_arrive(&r_empty[rslot]);
+                        }
+                        __syncwarp();
                     }
                 }
                 if (!ok) break;
@@ -663,6 +693,8 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
             tc_fence_before();
             mbar_arrive(&acc_empty[b]);
         }
+        if (kTmaOut && lane == 0) bulk_wait_all();   // outputs written before the CTA exits
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -842,6 +874,10 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
     bool ok = encode_act(&em.R, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.R, a.T, kEpiCols, kTileM);
     ok = ok && encode_act(&em.P, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.P ? a.P : a.R, a.T,
                           kEpiCols, kTileM);
+    // the mix's fp32 output (any [T][4][2560] fp32 tensor for the other epilogues)
+    const bool mix = mode == PrefillMode::kFused || mode == PrefillMode::kFusedBf16Lo;
+    ok = ok && encode_act(&em.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, mix ? a.out_f32 : a.R, a.T,
+                          kEpiCols, kEpiRows);
     if (!ok) return cudaErrorInvalidValue;
     const int has_P = a.P != nullptr;
     switch (mode) {
