@@ -290,48 +290,66 @@ up_mix_kernel(const float* R, const float* P, const uint16_t* __restrict__ W_up,
         reinterpret_cast<const float4*>(Rmix)[tid];
     __syncthreads();
 
+    // tokens in pairs: each weight is unpacked from bf16 once and feeds both tokens
+    // (every token's dot keeps the same order of fused multiply-adds)
 #pragma unroll
-    for (int t = 0; t < T; ++t) {
-        const float4* l4 = reinterpret_cast<const float4*>(&lo_s[t][part][0]);
-        float acc[kStreams] = {0.f, 0.f, 0.f, 0.f};
+    for (int t0 = 0; t0 < T; t0 += 2) {
+        constexpr int kMax = 2;
+        const int nt = t0 + 1 < T ? 2 : 1;   // a compile-time constant once unrolled
+        float acc[kMax][kStreams] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int q = 0; q < 5; ++q) {
-            const float4 xa = l4[2 * q], xb = l4[2 * q + 1];
+            float x[kMax][8];
+#pragma unroll
+            for (int i = 0; i < kMax; ++i) {
+                if (i < nt) {
+                    const float4* l4 = reinterpret_cast<const float4*>(&lo_s[t0 + i][part][0]);
+                    const float4 xa = l4[2 * q], xb = l4[2 * q + 1];
+                    x[i][0] = xa.x; x[i][1] = xa.y; x[i][2] = xa.z; x[i][3] = xa.w;
+                    x[i][4] = xb.x; x[i][5] = xb.y; x[i][6] = xb.z; x[i][7] = xb.w;
+                }
+            }
 #pragma unroll
             for (int st = 0; st < kStreams; ++st) {
                 const uint4 w = wv[st][q];
-                float v = acc[st];
-                v = fmaf(bf16_lo(w.x), xa.x, v);
-                v = fmaf(bf16_hi(w.x), xa.y, v);
-                v = fmaf(bf16_lo(w.y), xa.z, v);
-                v = fmaf(bf16_hi(w.y), xa.w, v);
-                v = fmaf(bf16_lo(w.z), xb.x, v);
-                v = fmaf(bf16_hi(w.z), xb.y, v);
-                v = fmaf(bf16_lo(w.w), xb.z, v);
-                v = fmaf(bf16_hi(w.w), xb.w, v);
-                acc[st] = v;
+                const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                    bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+                for (int i = 0; i < kMax; ++i) {
+                    if (i < nt) {
+                        float v = acc[i][st];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v = fmaf(f[e], x[i][e], v);
+                        acc[i][st] = v;
+                    }
+                }
             }
         }
 #pragma unroll
-        for (int st = 0; st < kStreams; ++st) {
-            acc[st] += __shfl_xor_sync(0xffffffffu, acc[st], 4);
-            acc[st] += __shfl_xor_sync(0xffffffffu, acc[st], 2);
-            acc[st] += __shfl_xor_sync(0xffffffffu, acc[st], 1);
-        }
-        // lane `part` (0..3) of the column group gates stream `part`
-        const float u = sp == 0 ? acc[0] : sp == 1 ? acc[1] : sp == 2 ? acc[2] : acc[3];
-        const float g = gate_value(u, rp[t]);
-        const int base = lane & ~7;
-        const float g0 = __shfl_sync(0xffffffffu, g, base + 0);
-        const float g1 = __shfl_sync(0xffffffffu, g, base + 1);
-        const float g2 = __shfl_sync(0xffffffffu, g, base + 2);
-        const float g3 = __shfl_sync(0xffffffffu, g, base + 3);
-        if (part < 4) {
-            const float m = mix_row(&m_s[t][part * 4], g0, g1, g2, g3);
-            const size_t off = (size_t)t * kCols + part * kWidth + c;
-            out_f32[off] = m;
-            out_bf16[off] = to_bf16_bits(m);
-            out_fp16[off] = to_fp16_bits(m);
+        for (int i = 0; i < kMax; ++i) {
+            if (i >= nt) continue;
+            const int t = t0 + i;
+#pragma unroll
+            for (int st = 0; st < kStreams; ++st) {
+                acc[i][st] += __shfl_xor_sync(0xffffffffu, acc[i][st], 4);
+                acc[i][st] += __shfl_xor_sync(0xffffffffu, acc[i][st], 2);
+                acc[i][st] += __shfl_xor_sync(0xffffffffu, acc[i][st], 1);
+            }
+            // lane `part` (0..3) of the column group gates stream `part`
+            const float u = sp == 0 ? acc[i][0] : sp == 1 ? acc[i][1] : sp == 2 ? acc[i][2] : acc[i][3];
+            const float g = gate_value(u, rp[t]);
+            const int base = lane & ~7;
+            const float g0 = __shfl_sync(0xffffffffu, g, base + 0);
+            const float g1 = __shfl_sync(0xffffffffu, g, base + 1);
+            const float g2 = __shfl_sync(0xffffffffu, g, base + 2);
+            const float g3 = __shfl_sync(0xffffffffu, g, base + 3);
+            if (part < 4) {
+                const float m = mix_row(&m_s[t][part * 4], g0, g1, g2, g3);
+                const size_t off = (size_t)t * kCols + part * kWidth + c;
+                out_f32[off] = m;
+                out_bf16[off] = to_bf16_bits(m);
+                out_fp16[off] = to_fp16_bits(m);
+            }
         }
     }
 }
