@@ -374,37 +374,52 @@ def gpu_arm(args) -> None:
     cold_round = {"us_per_round": 1e3 * ms_r / 20, "us_per_read": 1e3 * ms_r / 20 / 96,
                   "gbps": 96 * read_bytes(4, True) / (ms_r / 20 * 1e-3) / 1e9}
 
-    # --- e2e: pinned host inputs -> device, 16 reads via the public call, outputs back ---
-    pin_in, pin_out, dev_in = [], [], []
-    h2d = d2h = 0
-    for j, (T, p) in enumerate(SWEEP):
+    # --- e2e: pinned host inputs -> device, 16 reads via the public call, outputs back.
+    #     A step's inputs sit in one pinned buffer and go over in one copy; its outputs
+    #     come back in one copy (how a caller would stage them) ---
+    in_off, out_off = [], []
+    n_in = n_out = 0
+    for T, p in SWEEP:
+        sizes = {"R": T * 10240, "P": T * 10240 if p else 0, "Rmix": T * 16}
+        offs = {}
+        for key, n in sizes.items():
+            offs[key] = (n_in, n) if n else None
+            n_in += n
+        in_off.append(offs)
+        out_off.append((n_out, T))
+        n_out += T * 10240
+    pin_in = torch.empty(n_in, dtype=torch.float32).pin_memory()
+    for j, offs in enumerate(in_off):
         a = acts[j]["host"]
-        hin = {k: torch.from_numpy(a[k]).pin_memory() if a[k] is not None else None
-               for k in ("R", "P", "Rmix")}
-        din = {k: (torch.empty_like(v, device=dev) if v is not None else None)
-               for k, v in hin.items()}
-        hout = tuple(torch.empty((T, 4, 2560), dtype=dt).pin_memory()
-                     for dt in (torch.float32, torch.int16, torch.int16))
-        pin_in.append(hin)
-        dev_in.append(din)
-        pin_out.append(hout)
-        h2d += sum(v.numel() * v.element_size() for v in hin.values() if v is not None)
-        d2h += sum(v.numel() * v.element_size() for v in hout)
+        for key, o in offs.items():
+            if o is not None:
+                pin_in[o[0]:o[0] + o[1]].copy_(torch.from_numpy(np.ascontiguousarray(a[key]).reshape(-1)))
+    dev_in = torch.empty(n_in, dtype=torch.float32, device=dev)
+    # outputs: fp32 region, then the bf16 and fp16 regions, as bytes
+    dev_out = torch.empty(n_out * 8, dtype=torch.uint8, device=dev)
+    pin_out = torch.empty(n_out * 8, dtype=torch.uint8).pin_memory()
+    o32 = dev_out[:n_out * 4].view(torch.float32)
+    o16b = dev_out[n_out * 4:n_out * 6].view(torch.int16)
+    o16h = dev_out[n_out * 6:].view(torch.int16)
+    h2d, d2h = n_in * 4, n_out * 8
+    views = []
+    for j, (T, p) in enumerate(SWEEP):
+        offs, (oo, _) = in_off[j], out_off[j]
+        v = {key: (dev_in[o[0]:o[0] + o[1]] if o is not None else None) for key, o in offs.items()}
+        views.append((v, o32[oo * 1:oo + T * 10240], o16b[oo:oo + T * 10240],
+                      o16h[oo:oo + T * 10240]))
 
     def e2e_step(k):
         g = k % n_groups
         with torch.cuda.stream(stream):
+            dev_in.copy_(pin_in, non_blocking=True)
             for j in range(len(SWEEP)):
                 i = g * len(SWEEP) + j
-                hin, din, hout = pin_in[j], dev_in[j], pin_out[j]
-                for key in ("R", "P", "Rmix"):
-                    if hin[key] is not None:
-                        din[key].copy_(hin[key], non_blocking=True)
+                v, f32, b16, h16 = views[j]
                 W = sets[i]
-                hc.hc_read(SWEEP[j][0], din["R"], din["P"], W["w_norm"], W["W_down"],
-                           W["W_up"], din["Rmix"], *outs[i], stream=stream)
-                for o, ho in zip(outs[i], hout):
-                    ho.copy_(o, non_blocking=True)
+                hc.hc_read(SWEEP[j][0], v["R"], v["P"], W["w_norm"], W["W_down"], W["W_up"],
+                           v["Rmix"], f32, b16, h16, stream=stream)
+            pin_out.copy_(dev_out, non_blocking=True)
 
     e2e_steps = max(10, min(args.steps, 500))
     ms_e = timed(e2e_step, e2e_steps, min(args.warmup, 5) + 3)
