@@ -38,7 +38,6 @@ constexpr int kColGroups = 5;              // down: 5 x 256 columns = 1280
 constexpr int kClusters = kDownRowBlocks;  // 20
 constexpr int kCtas = kDownSlices * kDownRowBlocks;   // 160
 constexpr int kUpColsPerCta = kWidth / kCtas;         // 16
-constexpr int kUpRows = kStreams * kUpColsPerCta;     // 64 rows of W_up per CTA
 constexpr int kParts = 16;                 // up: 16 lanes per column, 20 inputs each
 constexpr int kPartLen = kRank / kParts;   // 20
 constexpr uint64_t kWaitNs = 2000000000ull;
