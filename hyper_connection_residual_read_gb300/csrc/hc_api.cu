@@ -262,8 +262,9 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     ok &= cudaMalloc(&c.s.sync, 2 * sizeof(unsigned)) == cudaSuccess;
     ok &= cudaMalloc(&c.wd16, sizeof(__half) * (size_t)kRank * kCols) == cudaSuccess;
     ok &= cudaMalloc(&c.wu16, sizeof(__half) * (size_t)kCols * kRank) == cudaSuccess;
-    ok &= cudaMalloc(&c.partials, sizeof(float) * (size_t)max_tokens * kStreams * 4 * kRank) == cudaSuccess;
-    ok &= cudaMalloc(&c.ssq, sizeof(float) * (size_t)max_tokens * kStreams * 4) == cudaSuccess;
+    const size_t ts = (size_t)partial_tiles(max_tokens) * 128;
+    ok &= cudaMalloc(&c.partials, sizeof(float) * ts * kStreams * 4 * kRank) == cudaSuccess;
+    ok &= cudaMalloc(&c.ssq, sizeof(float) * ts * kStreams * 4) == cudaSuccess;
     ok &= cudaMalloc(&c.lo16, sizeof(__half) * 2 * (size_t)max_tokens * kRank) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();

@@ -50,8 +50,11 @@ struct Ctx {
     // prefill scratch
     __half* wd16 = nullptr;          // W_down as fp16 [kRank][kCols]
     __half* wu16 = nullptr;          // W_up as fp16 [kCols][kRank]
-    float* partials = nullptr;       // down partials [max_tokens][kStreams][4 K quarters][kRank]
-    float* ssq = nullptr;            // sums of squares of R' [max_tokens][kStreams][4 K quarters]
+    // down partials, tile-blocked and token-minor: [tiles][kStreams][4 K quarters]
+    // [kRank][128 tokens], and the sums of squares of R' [tiles][kStreams][4 K
+    // quarters][128 tokens], tiles = partial_tiles(max_tokens)
+    float* partials = nullptr;
+    float* ssq = nullptr;
     __half* lo16 = nullptr;          // lo as two fp16 terms [2][max_tokens][kRank]
     float* gated = nullptr;          // [max_tokens][kCols], unfused prefill only (lazy)
     CUtensorMap tm_wd;               // TMA maps over wd16, wu16, lo16
@@ -63,6 +66,9 @@ struct Ctx {
     int lo_mode = 0;
     int lo_tokens = 0;
 };
+
+// 128-token tiles of the partials.
+inline int partial_tiles(int max_tokens) { return (max_tokens + 127) / 128; }
 
 struct ReadArgs {
     int T;

@@ -351,26 +351,23 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             const bool valid = t < T;
             if (!mbar_wait(&acc_full, lt & 1, &abort_flag, status)) break;
             tc_fence_after();
-            const size_t prow = ((size_t)t * kStreams + s) * kDownKSplit + kq;
-            float* dst = partials + prow * kRank;
+            // tile-blocked and token-minor: [tile][stream][quarter][column][128 tokens],
+            // so a warp's 32 tokens of one column are 128 contiguous bytes
+            const size_t prow = ((size_t)tt * kStreams + s) * kDownKSplit + kq;
+            float* dst = partials + prow * kRank * kTileM + m;
 #pragma unroll 1
             for (int c0 = 0; c0 < kDownN; c0 += 32) {
                 float v[32];
                 tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
                 if (valid) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        uint32_t w[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(v[8 * g + i]);
-                        st_global_v8(dst + c0 + 8 * g, w);
-                    }
+                    for (int i = 0; i < 32; ++i) dst[(c0 + i) * kTileM] = v[i];
                 }
             }
             tc_fence_before();
             mbar_arrive(&acc_empty);
             if (!mbar_wait(&ss_full[lt & 1], (lt >> 1) & 1, &abort_flag, status)) break;
-            if (valid) ssq[prow] = ss_s[lt & 1][m];
+            if (valid) ssq[prow * kTileM + m] = ss_s[lt & 1][m];
         }
     }
     tc_fence_before();
@@ -382,44 +379,94 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
 }
 
 // ---------------------------------------------------------------------------
-// lo = sum of the 4 stream partials (in stream order), split into two fp16 terms
+// lo = sum over the streams (in order) of rs times the sum of the stream's quarter
+// partials (in order); stored as two fp16 terms, or as one bf16 term in the bf16-lo
+// mode. The partials come tile-blocked and token-minor ([tile][stream][quarter]
+// [column][128 tokens]). A CTA takes one tile's 128 tokens and 32 of the columns:
+// for each (stream, quarter) it reads 32 consecutive 512-byte rows, the tokens
+// across the lanes; shared memory turns the block around so that each token's 32
+// columns leave as whole 32-byte sectors.
 // ---------------------------------------------------------------------------
+constexpr int kLoCols = 32;
+constexpr int kLoThreads = 512;    // 16 warps, two of the 32 columns each
+
 template <bool kBf16>
-__global__ void lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ssq,
-                                __half* __restrict__ lo16, int T, int max_tokens, float eps,
-                                int* __restrict__ status) {
-    const int n4 = T * (kRank / 4);
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += gridDim.x * blockDim.x) {
-        const int t = i / (kRank / 4), j = 4 * (i % (kRank / 4));
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+__global__ void __launch_bounds__(kLoThreads)
+lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ssq,
+                __half* __restrict__ lo16, int T, int max_tokens, float eps,
+                int* __restrict__ status) {
+    __shared__ float lo_s[kTileM][kLoCols + 1];
+    __shared__ float rs_s[kStreams][kTileM];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tt = blockIdx.x / (kRank / kLoCols), cg = blockIdx.x % (kRank / kLoCols);
+    const size_t base = (size_t)tt * kStreams * kDownKSplit;   // first (stream, quarter) row
+    // rs of the tile's tokens: warps 0-3 take a token quarter each
+    if (warp < 4) {
+        const int tr = warp * 32 + lane;
+        const bool valid = tt * kTileM + tr < T;
 #pragma unroll
         for (int s = 0; s < kStreams; ++s) {
-            const size_t row = ((size_t)t * kStreams + s) * kDownKSplit;
-            float ss = ssq[row];
-            float4 d = *reinterpret_cast<const float4*>(partials + row * kRank + j);
+            float ss = 0.f;
+            if (valid) {
+                const float* q4 = ssq + (base + (size_t)s * kDownKSplit) * kTileM + tr;
+                ss = q4[0];
+#pragma unroll
+                for (int q = 1; q < kDownKSplit; ++q) ss += q4[q * kTileM];
+            }
+            rs_s[s][tr] = 1.0f / sqrtf(ss / (float)kWidth + eps);
+        }
+    }
+    __syncthreads();
+    // warp w sums columns w and w + 16 of the group for all 128 tokens: a lane takes
+    // four consecutive tokens, so one load instruction reads a whole 512-byte row
+    const int tr0 = 4 * lane;
+    float rs[4][kStreams];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int s = 0; s < kStreams; ++s) rs[k][s] = rs_s[s][tr0 + k];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int jl = warp + 16 * i, j = cg * kLoCols + jl;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int s = 0; s < kStreams; ++s) {
+            const float* p = partials + ((base + (size_t)s * kDownKSplit) * kRank + j) * kTileM + tr0;
+            float4 d = *reinterpret_cast<const float4*>(p);
 #pragma unroll
             for (int q = 1; q < kDownKSplit; ++q) {
-                ss += ssq[row + q];
-                const float4 w = *reinterpret_cast<const float4*>(partials + (row + q) * kRank + j);
+                const float4 w = *reinterpret_cast<const float4*>(p + (size_t)q * kRank * kTileM);
                 d.x += w.x; d.y += w.y; d.z += w.z; d.w += w.w;
             }
-            const float rs = 1.0f / sqrtf(ss / (float)kWidth + eps);
-            v.x = fmaf(rs, d.x, v.x); v.y = fmaf(rs, d.y, v.y);
-            v.z = fmaf(rs, d.z, v.z); v.w = fmaf(rs, d.w, v.w);
+            v[0] = fmaf(rs[0][s], d.x, v[0]);
+            v[1] = fmaf(rs[1][s], d.y, v[1]);
+            v[2] = fmaf(rs[2][s], d.z, v[2]);
+            v[3] = fmaf(rs[3][s], d.w, v[3]);
         }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) lo_s[tr0 + k][jl] = v[k];
+    }
+    __syncthreads();
+    // out: each token's 32 columns, 4 per lane, 8 lanes per token, 4 tokens per warp
+    // and pass
+    for (int r = warp * 4 + (lane >> 3); r < kTileM; r += (kLoThreads / 32) * 4) {
+        const int trow = tt * kTileM + r;
+        if (trow >= T) continue;
+        const int c4 = 4 * (lane & 7);
+        const float x0 = lo_s[r][c4], x1 = lo_s[r][c4 + 1], x2 = lo_s[r][c4 + 2], x3 = lo_s[r][c4 + 3];
+        const size_t off = (size_t)trow * kRank + cg * kLoCols + c4;
         if (kBf16) {
             // the pages' numerics: lo rounded once to bf16 (nearest even), one term
-            *reinterpret_cast<uint2*>(lo16 + (size_t)t * kRank + j) =
-                make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+            *reinterpret_cast<uint2*>(lo16 + off) = make_uint2(pack_bf16x2(x0, x1), pack_bf16x2(x2, x3));
             continue;
         }
-        if (fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))) >= 65504.f)
+        if (fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))) >= 65504.f)
             atomicOr(status, kStatusRange);
         uint32_t h0, l0, h1, l1;
-        split2(v.x, v.y, h0, l0);
-        split2(v.z, v.w, h1, l1);
-        *reinterpret_cast<uint2*>(lo16 + (size_t)t * kRank + j) = make_uint2(h0, h1);
-        *reinterpret_cast<uint2*>(lo16 + ((size_t)max_tokens + t) * kRank + j) = make_uint2(l0, l1);
+        split2(x0, x1, h0, l0);
+        split2(x2, x3, h1, l1);
+        *reinterpret_cast<uint2*>(lo16 + off) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2*>(lo16 + (size_t)max_tokens * kRank + off) = make_uint2(l0, l1);
     }
 }
 
@@ -855,14 +902,13 @@ cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, PrefillMode mod
     if (!encode_down_r(&tm_r, a.R, a.T)) return cudaErrorInvalidValue;
     down_tile_kernel<<<down_grid, kDownThreads, kDownSmem, st>>>(
         a.R, a.P, a.w_norm, c.tm_wd, tm_r, c.partials, c.ssq, a.T, c.s.status);
-    const int n4 = a.T * (kRank / 4);
-    const int rgrid = (n4 + 255) / 256 < 8 * c.sm_count ? (n4 + 255) / 256 : 8 * c.sm_count;
+    const int rgrid = ((a.T + kTileM - 1) / kTileM) * (kRank / kLoCols);
     if (mode == PrefillMode::kFusedBf16Lo)
-        lo_split_kernel<true><<<rgrid, 256, 0, st>>>(c.partials, c.ssq, c.lo16, a.T, c.max_tokens,
-                                                     c.eps, c.s.status);
+        lo_split_kernel<true><<<rgrid, kLoThreads, 0, st>>>(c.partials, c.ssq, c.lo16, a.T,
+                                                            c.max_tokens, c.eps, c.s.status);
     else
-        lo_split_kernel<false><<<rgrid, 256, 0, st>>>(c.partials, c.ssq, c.lo16, a.T, c.max_tokens,
-                                                      c.eps, c.s.status);
+        lo_split_kernel<false><<<rgrid, kLoThreads, 0, st>>>(c.partials, c.ssq, c.lo16, a.T,
+                                                             c.max_tokens, c.eps, c.s.status);
     return cudaGetLastError();
 }
 
