@@ -16,7 +16,7 @@ from hyper_connection_residual_read_gb300 import synth
 from oracle import hc_oracle as O
 
 from _hc import (EPS, MAX_TOKENS, TOL_F32, alloc_out, assert_matches_oracle, dev_f32,
-                 dev_weights, gpu_read)
+                 dev_u16, dev_weights, gpu_read, rel_diff)
 
 pytestmark = pytest.mark.gpu
 
@@ -435,3 +435,23 @@ def test_back_to_back_tile_reads_do_not_see_each_others_scratch(weights):
         want = ref16 if path == hc.HC_PATH_PREFILL_BF16_LO else ref
         for x, y in zip(want, _host(o)):
             assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+
+
+@pytest.mark.parametrize("T,path", [(3, hc.HC_PATH_DECODE), (4, hc.HC_PATH_DECODE_ONE_KERNEL),
+                                    (200, hc.HC_PATH_PREFILL)])
+def test_stream_permutation_equivariance(weights, T, path):
+    """Relabelling the four streams consistently (residual and pending write, w_norm
+    rows, W_down column blocks, W_up row blocks, the mix's rows and columns) relabels
+    the output streams. The GPU sums streams in a fixed order, so the two reads agree
+    to the fp32 tolerance, not bit for bit."""
+    w, W = weights
+    a = synth.make_activations(61 + T, T, True)
+    C = synth.WIDTH
+    perm = np.array([2, 0, 3, 1])
+    kperm = (perm[:, None] * C + np.arange(C)[None, :]).reshape(-1)
+    base = gpu_read(T, dev_f32(a["R"]), dev_f32(a["P"]), W, dev_f32(a["Rmix"]), path)
+    Wp = {"w_norm": dev_u16(w["w_norm"][perm]), "W_down": dev_u16(w["W_down"][:, kperm]),
+          "W_up": dev_u16(w["W_up"][kperm])}
+    moved = gpu_read(T, dev_f32(a["R"][:, perm]), dev_f32(a["P"][:, perm]), Wp,
+                     dev_f32(a["Rmix"][:, perm][:, :, perm]), path)
+    assert rel_diff(moved[0], base[0][:, perm]) <= TOL_F32
