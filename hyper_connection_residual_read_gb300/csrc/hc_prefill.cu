@@ -74,7 +74,14 @@ constexpr int kUpColTiles = kWidth / kUpCols;     // 40
 // stream per step, and 16 columns of each 16-bit image per pair of steps, so
 // every store fills whole DRAM sectors and no output passes through shared memory.
 constexpr int kUpEpiWarps = 8;
-constexpr int kUpThreads = 96 + 32 * kUpEpiWarps; // operand TMA, MMA, R TMA, epilogue warps
+// Warpgroup 0: operand TMA, MMA issuer, R TMA and one idle warp; warpgroups 1-2: the
+// epilogue. The block is launched with kUpRegsLaunch registers a thread; warpgroup 0
+// then gives registers up and the epilogue takes them (setmaxnreg):
+// 128 x (kUpRegsLaunch - kUpRegsLow) = 256 x (kUpRegsHigh - kUpRegsLaunch).
+constexpr int kUpThreads = 128 + 32 * kUpEpiWarps;
+constexpr int kUpRegsLaunch = 168, kUpRegsLow = 40, kUpRegsHigh = 232;
+static_assert(128 * (kUpRegsLaunch - kUpRegsLow) == 256 * (kUpRegsHigh - kUpRegsLaunch),
+              "the epilogue may take only what warpgroup 0 gives up");
 constexpr int kEpiCols = 8;
 constexpr int kEpiRows = 32;
 constexpr int kRSlot = kStreams * kTileM * kEpiCols * 4;        // 16 KB
@@ -541,6 +548,8 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
     auto sB = [&](int slot) { return smem + slot * kUpStageBytes + 2 * kTileBytes16; };
     uint8_t* rring = smem + kUpStages * kUpStageBytes;
 
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kUpRegsLow));
     if (warp == 0) {
         // operand producer: lo terms and W_up rows, K blocks of 64
         if (lane == 0) {
@@ -613,10 +622,12 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                 }
             }
         }
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kUpRegsHigh));
         // epilogue warp: TMEM lane quarter q = tokens q*32..q*32+31 of the tile; group
         // g takes the step pairs {2g, 2g+1} and {4+2g, 5+2g}
-        const int ew = warp - 3, q = warp & 3, g = ew >> 2;
+        const int ew = warp - 4, q = warp & 3, g = ew >> 2;
         const int row = q * kEpiRows + lane;         // this lane's token within the tile
         int lt = 0;
         for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
@@ -876,6 +887,20 @@ cudaError_t prefill_setup(Ctx& c) {
         if (!encode_map(&c.tm_lo_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.lo16, 3, dims, strides,
                         box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
+    }
+    // the register split of the up tile assumes the launch register count it was
+    // written for: refuse to run a build whose count differs (the epilogue's
+    // setmaxnreg.inc would wait for registers that are never given up)
+    {
+        cudaFuncAttributes fa;
+        const void* ks[] = {reinterpret_cast<const void*>(upmix_tile_kernel<kOutMix, 2>),
+                            reinterpret_cast<const void*>(upmix_tile_kernel<kOutMix, 1>),
+                            reinterpret_cast<const void*>(upmix_tile_kernel<kOutY, 2>),
+                            reinterpret_cast<const void*>(upmix_tile_kernel<kOutGated, 2>)};
+        for (const void* k : ks) {
+            if ((e = cudaFuncGetAttributes(&fa, k)) != cudaSuccess) return e;
+            if (fa.numRegs != kUpRegsLaunch) return cudaErrorInvalidConfiguration;
+        }
     }
     e = cudaFuncSetAttribute(upmix_tile_kernel<kOutMix, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kUpSmem);
