@@ -79,7 +79,7 @@ constexpr int kUpEpiWarps = 8;
 // then gives registers up and the epilogue takes them (setmaxnreg):
 // 128 x (kUpRegsLaunch - kUpRegsLow) = 256 x (kUpRegsHigh - kUpRegsLaunch).
 constexpr int kUpThreads = 128 + 32 * kUpEpiWarps;
-constexpr int kUpRegsLaunch = 168, kUpRegsLow = 40, kUpRegsHigh = 232;
+constexpr int kUpRegsLaunch = 168, kUpRegsLow = 56, kUpRegsHigh = 224;
 static_assert(128 * (kUpRegsLaunch - kUpRegsLow) == 256 * (kUpRegsHigh - kUpRegsLaunch),
               "the epilogue may take only what warpgroup 0 gives up");
 constexpr int kEpiCols = 8;
