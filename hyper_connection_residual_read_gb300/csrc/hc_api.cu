@@ -38,6 +38,7 @@ void free_ctx(Ctx& c) {
     cudaFree(c.s.lo);
     cudaFree(c.s.status);
     cudaFree(c.s.sync);
+    cudaFree(c.s.sched);
     cudaFree(c.wd16);
     cudaFree(c.wu16);
     cudaFree(c.partials);
@@ -260,6 +261,7 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     ok &= cudaMalloc(&c.s.lo, sizeof(float) * (size_t)max_tokens * kRank) == cudaSuccess;
     ok &= cudaMalloc(&c.s.status, sizeof(int)) == cudaSuccess;
     ok &= cudaMalloc(&c.s.sync, 2 * sizeof(unsigned)) == cudaSuccess;
+    ok &= cudaMalloc(&c.s.sched, 2 * kSchedPairs * sizeof(int)) == cudaSuccess;
     ok &= cudaMalloc(&c.wd16, sizeof(__half) * (size_t)kRank * kCols) == cudaSuccess;
     ok &= cudaMalloc(&c.wu16, sizeof(__half) * (size_t)kCols * kRank) == cudaSuccess;
     const size_t ts = (size_t)partial_tiles(max_tokens) * 128;
@@ -273,6 +275,7 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     }
     if (cudaMemset(c.s.status, 0, sizeof(int)) != cudaSuccess ||
         cudaMemset(c.s.sync, 0, 2 * sizeof(unsigned)) != cudaSuccess ||
+        cudaMemset(c.s.sched, 0, 2 * kSchedPairs * sizeof(int)) != cudaSuccess ||
         decode_fused_setup(&c.fused_decode) != cudaSuccess ||
         cudaMemset(c.lo16, 0, sizeof(__half) * 2 * (size_t)max_tokens * kRank) != cudaSuccess ||
         prefill_setup(c) != cudaSuccess ||
@@ -372,7 +375,11 @@ extern "C" int hc_read_status(void* stream) {
     if (cudaMemcpy(&word, c->s.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
         cudaMemset(c->s.status, 0, sizeof(int)) != cudaSuccess)
         return HC_ERR_CUDA;
-    if (word & kStatusTimeout) return HC_ERR_TIMEOUT;
+    if (word & kStatusTimeout) {
+        // a kernel that gave up may have left its scheduler pair mid-count
+        if (cudaMemset(c->s.sched, 0, 2 * kSchedPairs * sizeof(int)) != cudaSuccess) return HC_ERR_CUDA;
+        return HC_ERR_TIMEOUT;
+    }
     return (word & kStatusRangeBit) ? HC_ERR_RANGE : HC_OK;
 }
 

@@ -27,6 +27,10 @@ constexpr int kDownRowBlocks = kRank / kDownRowsPerCta;  // 20
 // path 54.4 us at 32 tokens, 78.4 vs 57.8 at 48.
 constexpr int kAutoDecodeMaxT = 32;
 
+// Scheduler pairs in Scratch::sched.
+constexpr int kSchedUp = 0;
+constexpr int kSchedPairs = 2;
+
 // Device status word bits.
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusRangeBit = 2;   // a prefill activation did not fit fp16
@@ -34,6 +38,9 @@ constexpr int kStatusRangeBit = 2;   // a prefill activation did not fit fp16
 struct Scratch {
     float* lo = nullptr;             // [max_tokens][kRank], the down projection's output
     int* status = nullptr;           // device status word
+    // tile-path schedulers: per kernel kind a pair {next tile, CTAs finished}; the
+    // last CTA of a launch resets its pair to 0 for the next launch
+    int* sched = nullptr;
     unsigned* sync = nullptr;        // fused decode: [0] clusters that published lo,
                                      // [1] CTAs that have read it (both reset per call)
 };

@@ -83,9 +83,22 @@ constexpr int kUpRegsLaunch = 168, kUpRegsLow = 56, kUpRegsHigh = 224;
 static_assert(128 * (kUpRegsLaunch - kUpRegsLow) == 256 * (kUpRegsHigh - kUpRegsLaunch),
               "the epilogue may take only what warpgroup 0 gives up");
 constexpr int kEpiCols = 8;
+// Tiles are handed out at run time: a CTA's first tile is its block index, the
+// rest come from a global counter in index order, so a CTA that runs fast takes
+// more tiles and all CTAs finish within about one tile of each other. The fetching
+// thread passes each index through a small queue in shared memory to the CTA's
+// other roles (MMA issuer, two R producers, 8 epilogue warps).
+constexpr int kTileQ = 4;
+constexpr int kTileQConsumers = 3 + kUpEpiWarps;
 constexpr int kEpiRows = 32;
 constexpr int kRSlot = kStreams * kTileM * kEpiCols * 4;        // 16 KB
-constexpr int kRSlots = 6;
+// Each epilogue group has its own ring of R slots and its own producer, so every
+// warp that waits on a slot's barrier consumes every fill of that slot. (With one
+// ring shared by both groups a warp a tile ahead of the other group could wait on
+// a slot whose previous fill, for the other group, was still in flight, and its
+// parity wait would take the fill before that one as complete.)
+constexpr int kRSlotsPerGroup = 3;
+constexpr int kRSlots = 2 * kRSlotsPerGroup;
 constexpr int kUpSmem = kUpStages * kUpStageBytes + kRSlots * kRSlot + 1024;
 
 constexpr int kStatusRange = kStatusRangeBit;
@@ -500,12 +513,15 @@ __global__ void __launch_bounds__(kUpThreads, 1)
 upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtensorMap tm_lo,
                   const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ EpiMaps em,
                   float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16,
-                  uint16_t* __restrict__ out_fp16, int has_P, int T, int* __restrict__ status) {
+                  uint16_t* __restrict__ out_fp16, int has_P, int T, int* __restrict__ status,
+                  int* __restrict__ sched) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[kUpStages], empty_bar[kUpStages];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
     __shared__ __align__(8) uint64_t r_full[kRSlots], r_empty[kRSlots];
+    __shared__ __align__(8) uint64_t tq_full[kTileQ], tq_empty[kTileQ];
+    __shared__ int tile_q[kTileQ];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
 
@@ -535,6 +551,10 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
             mbar_init(&r_full[i], 1);
             mbar_init(&r_empty[i], 4);
         }
+        for (int i = 0; i < kTileQ; ++i) {
+            mbar_init(&tq_full[i], 1);
+            mbar_init(&tq_empty[i], kTileQConsumers);
+        }
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -547,14 +567,30 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
     auto sA = [&](int slot, int term) { return smem + slot * kUpStageBytes + term * kTileBytes16; };
     auto sB = [&](int slot) { return smem + slot * kUpStageBytes + 2 * kTileBytes16; };
     uint8_t* rring = smem + kUpStages * kUpStageBytes;
+    // the CTA's i-th tile from the queue (n_tiles: no more tiles, or the CTA gave up)
+    auto take_tile = [&](int i) -> int {
+        if (!mbar_wait(&tq_full[i % kTileQ], (i / kTileQ) & 1, &abort_flag, status)) return n_tiles;
+        return tile_q[i % kTileQ];
+    };
 
     if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kUpRegsLow));
     if (warp == 0) {
         // operand producer: lo terms and W_up rows, K blocks of 64
         if (lane == 0) {
+            // lo and W_up tiles are read again by the other CTAs of their token and
+            // column tiles: keep them in L2 (evict_last) against the stream of R and
+            // outputs. R and the outputs keep the default policy: a 32-byte box row
+            // shares its 128-byte line with the next three steps, which find it in L2.
+            const uint64_t keep = l2_policy_evict_last();
             int it = 0;
-            for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
+            for (int i = 0; !abort_flag; ++i) {
+                // fetch the next tile and publish it to the other roles
+                if (!mbar_wait(&tq_empty[i % kTileQ], ((i / kTileQ) & 1) ^ 1, &abort_flag, status)) break;
+                const int tile = i == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(sched, 1);
+                tile_q[i % kTileQ] = tile;
+                mbar_arrive(&tq_full[i % kTileQ]);
+                if (tile >= n_tiles) break;
                 const int tt = tile / kUpColTiles, ct = tile % kUpColTiles;
                 for (int kb = 0; kb < kUpKBlocks; ++kb, ++it) {
                     const int slot = it % kUpStages;
@@ -563,19 +599,23 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     mbar_arrive_expect_tx(&full_bar[slot], kTerms * kTileBytes16 + kUpBBytes);
 #pragma unroll
                     for (int term = 0; term < kTerms; ++term)
-                        tma_load_3d(sA(slot, term), &tm_lo, kb * kBK, tt * kTileM, term, &full_bar[slot]);
+                        tma_load_3d_hint(sA(slot, term), &tm_lo, kb * kBK, tt * kTileM, term,
+                                         &full_bar[slot], keep);
 #pragma unroll
                     for (int s = 0; s < kStreams; ++s)
-                        tma_load_2d(sB(slot) + s * (kUpBBytes / kStreams), &tm_wu, kb * kBK,
-                                    s * kWidth + ct * kUpCols, &full_bar[slot]);
+                        tma_load_2d_hint(sB(slot) + s * (kUpBBytes / kStreams), &tm_wu, kb * kBK,
+                                         s * kWidth + ct * kUpCols, &full_bar[slot], keep);
                 }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = kTerms == 2 ? idesc_f16_f32(kTileM, kUpN) : idesc_bf16_f32(kTileM, kUpN);
-            int it = 0, lt = 0;
-            for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
+            int it = 0;
+            for (int lt = 0; !abort_flag; ++lt) {
+                const int tile = take_tile(lt);
+                mbar_arrive(&tq_empty[lt % kTileQ]);
+                if (tile >= n_tiles) break;
                 const int b = lt & 1;
                 if (!mbar_wait(&acc_empty[b], ((lt >> 1) & 1) ^ 1, &abort_flag, status)) break;
                 tc_fence_after();
@@ -600,17 +640,24 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                 mma_commit(&acc_full[b]);
             }
         }
-    } else if (warp == 2) {
-        // R (and P) producer: one slot per step (two with P), 4 streams per slot,
-        // in step order
+    } else {
+        // R (and P) producers, warp 2 for epilogue group 0 and warp 3 for group 1:
+        // one slot of the group's ring per step (two with P), 4 streams per slot, in
+        // the group's step order {2g, 2g+1, 4+2g, 5+2g}
+        const int rg = warp - 2;
         if (lane == 0) {
-            int u = 0;   // slot uses
-            for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
+            int u = 0;   // uses of this group's ring
+            for (int i = 0; !abort_flag; ++i) {
+                const int tile = take_tile(i);
+                mbar_arrive(&tq_empty[i % kTileQ]);
+                if (tile >= n_tiles) break;
                 const int tt = tile / kUpColTiles, ct = tile % kUpColTiles;
-                for (int k = 0; k < kSteps; ++k) {
+                for (int sg = 0; sg < kSteps / 2; ++sg) {
+                    const int k = 4 * (sg >> 1) + 2 * rg + (sg & 1);
                     for (int which = 0; which < slots_per_step; ++which, ++u) {
-                        const int slot = u % kRSlots;
-                        if (!mbar_wait(&r_empty[slot], ((u / kRSlots) & 1) ^ 1, &abort_flag, status))
+                        const int slot = rg * kRSlotsPerGroup + u % kRSlotsPerGroup;
+                        if (!mbar_wait(&r_empty[slot], ((u / kRSlotsPerGroup) & 1) ^ 1, &abort_flag,
+                                       status))
                             break;
                         mbar_arrive_expect_tx(&r_full[slot], kRSlot);
                         const CUtensorMap* map = which ? &em.P : &em.R;
@@ -629,8 +676,11 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
         // g takes the step pairs {2g, 2g+1} and {4+2g, 5+2g}
         const int ew = warp - 4, q = warp & 3, g = ew >> 2;
         const int row = q * kEpiRows + lane;         // this lane's token within the tile
-        int lt = 0;
-        for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
+        for (int lt = 0; !abort_flag; ++lt) {
+            const int tile = take_tile(lt);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tq_empty[lt % kTileQ]);
+            if (tile >= n_tiles) break;
             const int tt = tile / kUpColTiles, ct = tile % kUpColTiles;
             const int b = lt & 1;
             const int t = tt * kTileM + row;
@@ -652,7 +702,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
             if (!mbar_wait(&acc_full[b], (lt >> 1) & 1, &abort_flag, status)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * kUpN;
-            const int u_tile = lt * kSteps * slots_per_step;
+            const int u_tile = lt * (kSteps / 2) * slots_per_step;   // uses of group g's ring
             bool ok = true;
 #pragma unroll 1
             for (int pi = 0; pi < 2 && ok; ++pi) {
@@ -668,10 +718,13 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     float rp[kStreams][kEpiCols];
                     int rslot = 0;
                     for (int which = 0; which < slots_per_step; ++which) {
-                        const int u = u_tile + k * slots_per_step + which;
-                        const int slot = u % kRSlots;
+                        const int u = u_tile + (2 * pi + j) * slots_per_step + which;
+                        const int slot = g * kRSlotsPerGroup + u % kRSlotsPerGroup;
                         if (which == 0) rslot = slot;
-                        if (!mbar_wait(&r_full[slot], (u / kRSlots) & 1, &abort_flag, status)) { ok = false; break; }
+                        if (!mbar_wait(&r_full[slot], (u / kRSlotsPerGroup) & 1, &abort_flag, status)) {
+                            ok = false;
+                            break;
+                        }
 #pragma unroll
                         for (int s = 0; s < kStreams; ++s) {
                             const float4* r4 = reinterpret_cast<const float4*>(
@@ -759,6 +812,14 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+    if (threadIdx.x == 0) {
+        // every fetch of this CTA is done; the last CTA to finish resets the pair
+        __threadfence();
+        if (atomicAdd(sched + 1, 1) == (int)gridDim.x - 1) {
+            atomicExch(sched, 0);
+            atomicExch(sched + 1, 0);
+        }
     }
 }
 
@@ -955,7 +1016,7 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
         case PrefillMode::kFused:
             upmix_tile_kernel<kOutMix, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
                 a.Rmix, c.tm_lo, c.tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16, has_P, a.T,
-                c.s.status);
+                c.s.status, c.s.sched + 2 * kSchedUp);
             break;
         case PrefillMode::kFusedBf16Lo: {
             CUtensorMap tm_wu_bf16;   // over the caller's W_up [kCols][kRank] bf16
@@ -967,17 +1028,18 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
                 return cudaErrorInvalidValue;
             upmix_tile_kernel<kOutMix, 1><<<up_grid, kUpThreads, kUpSmem, st>>>(
                 a.Rmix, c.tm_lo_bf16, tm_wu_bf16, em, a.out_f32, a.out_bf16, a.out_fp16, has_P,
-                a.T, c.s.status);
+                a.T, c.s.status, c.s.sched + 2 * kSchedUp);
             break;
         }
         case PrefillMode::kReadoutY:
             upmix_tile_kernel<kOutY, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
                 nullptr, c.tm_lo, c.tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16, has_P, a.T,
-                c.s.status);
+                c.s.status, c.s.sched + 2 * kSchedUp);
             break;
         case PrefillMode::kUnfused: {
             upmix_tile_kernel<kOutGated, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
-                a.Rmix, c.tm_lo, c.tm_wu, em, c.gated, nullptr, nullptr, has_P, a.T, c.s.status);
+                a.Rmix, c.tm_lo, c.tm_wu, em, c.gated, nullptr, nullptr, has_P, a.T, c.s.status,
+                c.s.sched + 2 * kSchedUp);
             const int n = a.T * (kWidth / 4);
             const int mgrid = (n + 255) / 256 < 8 * c.sm_count ? (n + 255) / 256 : 8 * c.sm_count;
             mix_gated_kernel<<<mgrid, 256, 0, st>>>(c.gated, a.Rmix, a.out_f32, a.out_bf16,

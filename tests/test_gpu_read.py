@@ -437,6 +437,39 @@ def test_back_to_back_tile_reads_do_not_see_each_others_scratch(weights):
             assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
 
 
+def _poisoned_out(T):
+    """Output tensors filled with NaN / all-ones bits, so a value that no kernel wrote
+    cannot pass for a correct one left over from an earlier run."""
+    shape = (T, synth.N_STREAMS, synth.WIDTH)
+    return (torch.full(shape, float("nan"), dtype=torch.float32, device="cuda"),
+            torch.full(shape, -1, dtype=torch.int16, device="cuda"),
+            torch.full(shape, -1, dtype=torch.int16, device="cuda"))
+
+
+def test_up_tile_repeats_bitwise_into_poisoned_outputs(weights):
+    """The up tile's epilogue groups each stream R through their own ring of slots and
+    tiles are handed out at run time, so which CTA takes which tile, and how far one
+    epilogue group runs ahead of the other, change from run to run. Every run of the
+    up + gate + mix stage, fused and unfused, into fresh poisoned outputs must give
+    the bits of the first read (a group that read a slot before its data landed
+    would differ in that step's columns)."""
+    w, W = weights
+    T = 8192
+    c = synth.make_prefill_chunk(100, T)
+    R, M = dev_f32(c["R"]), dev_f32(c["Rmix"])
+    o = _poisoned_out(T)
+    hc.hc_read_path(hc.HC_PATH_PREFILL, T, R, None, W["w_norm"], W["W_down"], W["W_up"], M, *o)
+    ref = o
+    for rep in range(8):
+        path = hc.HC_PATH_PREFILL_UNFUSED if rep % 2 == 0 else hc.HC_PATH_PREFILL
+        o = _poisoned_out(T)
+        hc.hc_read_upmix(path, T, R, None, None, M, *o)
+        for x, y in zip(ref, o):
+            assert bool(torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x,
+                                    y.view(torch.int32) if y.dtype == torch.float32 else y)), rep
+    assert hc.hc_read_status() == 0
+
+
 @pytest.mark.parametrize("T,path", [(3, hc.HC_PATH_DECODE), (4, hc.HC_PATH_DECODE_ONE_KERNEL),
                                     (200, hc.HC_PATH_PREFILL)])
 def test_stream_permutation_equivariance(weights, T, path):
