@@ -29,6 +29,7 @@ constexpr int kAutoDecodeMaxT = 32;
 
 // Scheduler pairs in Scratch::sched.
 constexpr int kSchedUp = 0;
+constexpr int kSchedDown = 1;
 constexpr int kSchedPairs = 2;
 
 // Device status word bits.

@@ -56,6 +56,10 @@ constexpr int kDownKBlocksPerTile = kDownKBlocks / kDownKSplit;   // 10
 // TMA, MMA, 8 converter warps, 4 epilogue warps (one per TMEM lane quarter): the
 // epilogue of one tile runs while the converters already produce the next tile's A
 constexpr int kDownThreads = 448;
+// tiles from a run-time counter, as in the up tile below; the queue's consumers are
+// the MMA issuer, 8 converter warps and 4 epilogue warps
+constexpr int kDownTileQ = 4;
+constexpr int kDownTileQConsumers = 1 + 8 + 4;
 constexpr int kDownSmem = kDownStages * kDownStageBytes + 1024;
 
 // upmix_tile
@@ -172,11 +176,13 @@ __global__ void __launch_bounds__(kDownThreads, 1)
 down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                  const uint16_t* __restrict__ w_norm, const __grid_constant__ CUtensorMap tm_wd,
                  const __grid_constant__ CUtensorMap tm_r, float* __restrict__ partials,
-                 float* __restrict__ ssq, int T, int* __restrict__ status) {
+                 float* __restrict__ ssq, int T, int* __restrict__ status, int* __restrict__ sched) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[kDownStages], empty_bar[kDownStages];
     __shared__ __align__(8) uint64_t r_full[kDownStages];
+    __shared__ __align__(8) uint64_t tq_full[kDownTileQ], tq_empty[kDownTileQ];
+    __shared__ int tile_q[kDownTileQ];
     __shared__ __align__(8) uint64_t acc_full, acc_empty, ss_full[2];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
@@ -195,6 +201,10 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         mbar_init(&acc_empty, 128);
         mbar_init(&ss_full[0], 256);
         mbar_init(&ss_full[1], 256);
+        for (int i = 0; i < kDownTileQ; ++i) {
+            mbar_init(&tq_full[i], 1);
+            mbar_init(&tq_empty[i], kDownTileQConsumers);
+        }
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -206,13 +216,30 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
 
     auto sA = [&](int slot, int term) { return smem + slot * kDownStageBytes + term * kTileBytes16; };
     auto sB = [&](int slot) { return smem + slot * kDownStageBytes + 2 * kTileBytes16; };
+    // the CTA's i-th tile from the queue (n_tiles: no more tiles, or the CTA gave up),
+    // taken by a whole warp (its lane 0 releases the entry once every lane has read
+    // it) or by one thread
+    auto take_tile = [&](int i, bool whole_warp) -> int {
+        const int tile = mbar_wait(&tq_full[i % kDownTileQ], (i / kDownTileQ) & 1, &abort_flag, status)
+                             ? tile_q[i % kDownTileQ]
+                             : n_tiles;
+        if (whole_warp) __syncwarp();
+        if (!whole_warp || lane == 0) mbar_arrive(&tq_empty[i % kDownTileQ]);
+        return tile;
+    };
 
     if (warp == 0) {
-        // producer: the stream's W_down columns (320 rows as two boxes of 160) and,
-        // for a full tile, the R block
+        // producer: fetches the CTA's tiles; the stream's W_down columns (320 rows as
+        // two boxes of 160) and, for a full tile, the R block
         if (lane == 0) {
             int it = 0;
-            for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
+            for (int i = 0; !abort_flag; ++i) {
+                if (!mbar_wait(&tq_empty[i % kDownTileQ], ((i / kDownTileQ) & 1) ^ 1, &abort_flag, status))
+                    break;
+                const int tile = i == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(sched, 1);
+                tile_q[i % kDownTileQ] = tile;
+                mbar_arrive(&tq_full[i % kDownTileQ]);
+                if (tile >= n_tiles) break;
                 const int tt = tile / (kStreams * kDownKSplit);
                 const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
                 const bool full = (tt + 1) * kTileM <= T;
@@ -238,8 +265,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         // MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32(kTileM, kDownN / 2);
-            int it = 0, lt = 0;
-            for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
+            int it = 0;
+            for (int lt = 0; !abort_flag; ++lt) {
+                if (take_tile(lt, false) >= n_tiles) break;
                 if (!mbar_wait(&acc_empty, (lt & 1) ^ 1, &abort_flag, status)) break;
                 tc_fence_after();
                 bool ok = true;
@@ -272,8 +300,10 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         // lanes 0-15 and 16-31 take two rows at a time, 4 columns each
         const int cw = warp - 2;
         const int kc = 4 * (lane & 15);                 // this lane's 4 columns in a K block
-        int it = 0, lt = 0;
-        for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
+        int it = 0;
+        for (int lt = 0; !abort_flag; ++lt) {
+            const int tile = take_tile(lt, true);
+            if (tile >= n_tiles) break;
             const int tt = tile / (kStreams * kDownKSplit);
             const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
             const bool full = (tt + 1) * kTileM <= T;
@@ -363,8 +393,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         // store this quarter's partial dots and its sums of squares
         const int q = warp & 3;
         const int m = q * 32 + lane;
-        int lt = 0;
-        for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x, ++lt) {
+        for (int lt = 0; !abort_flag; ++lt) {
+            const int tile = take_tile(lt, true);
+            if (tile >= n_tiles) break;
             const int tt = tile / (kStreams * kDownKSplit);
             const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
             const int t = tt * kTileM + m;
@@ -395,6 +426,14 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+    if (threadIdx.x == 0) {
+        // every fetch of this CTA is done; the last CTA to finish resets the pair
+        __threadfence();
+        if (atomicAdd(sched + 1, 1) == (int)gridDim.x - 1) {
+            atomicExch(sched, 0);
+            atomicExch(sched + 1, 0);
+        }
     }
 }
 
@@ -987,7 +1026,8 @@ cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, PrefillMode mod
     CUtensorMap tm_r;
     if (!encode_down_r(&tm_r, a.R, a.T)) return cudaErrorInvalidValue;
     down_tile_kernel<<<down_grid, kDownThreads, kDownSmem, st>>>(
-        a.R, a.P, a.w_norm, c.tm_wd, tm_r, c.partials, c.ssq, a.T, c.s.status);
+        a.R, a.P, a.w_norm, c.tm_wd, tm_r, c.partials, c.ssq, a.T, c.s.status,
+        c.s.sched + 2 * kSchedDown);
     const int rgrid = ((a.T + kTileM - 1) / kTileM) * (kRank / kLoCols);
     if (mode == PrefillMode::kFusedBf16Lo)
         lo_split_kernel<true><<<rgrid, kLoThreads, 0, st>>>(c.partials, c.ssq, c.lo16, a.T,
