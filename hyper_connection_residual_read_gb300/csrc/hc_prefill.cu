@@ -59,6 +59,8 @@ constexpr int kDownThreads = 448;
 // tiles from a run-time counter, as in the up tile below; the queue's consumers are
 // the MMA issuer, 8 converter warps and 4 epilogue warps
 constexpr int kDownTileQ = 4;
+// R blocks are asked into L2 this many K blocks before their TMA load
+constexpr int kDownPrefetch = 3;
 constexpr int kDownTileQConsumers = 1 + 8 + 4;
 constexpr int kDownSmem = kDownStages * kDownStageBytes + 1024;
 
@@ -233,16 +235,23 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         // two boxes of 160) and, for a full tile, the R block
         if (lane == 0) {
             int it = 0;
+            // the tile after the current one is fetched one tile early, so that its
+            // first R blocks can be asked into L2 while the current tile is loaded
+            int next = blockIdx.x;
             for (int i = 0; !abort_flag; ++i) {
                 if (!mbar_wait(&tq_empty[i % kDownTileQ], ((i / kDownTileQ) & 1) ^ 1, &abort_flag, status))
                     break;
-                const int tile = i == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(sched, 1);
+                const int tile = next;
                 tile_q[i % kDownTileQ] = tile;
                 mbar_arrive(&tq_full[i % kDownTileQ]);
                 if (tile >= n_tiles) break;
+                next = (int)gridDim.x + atomicAdd(sched, 1);
                 const int tt = tile / (kStreams * kDownKSplit);
                 const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
                 const bool full = (tt + 1) * kTileM <= T;
+                const int ntt = next / (kStreams * kDownKSplit);
+                const int ns = (next / kDownKSplit) % kStreams, nkq = next % kDownKSplit;
+                const bool next_full = next < n_tiles && (ntt + 1) * kTileM <= T;
                 for (int kb = kq * kDownKBlocksPerTile; kb < (kq + 1) * kDownKBlocksPerTile; ++kb, ++it) {
                     const int slot = it % kDownStages;
                     const uint32_t ph = (it / kDownStages) & 1;
@@ -257,6 +266,17 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                         tma_load_5d(sA(slot, 1), &tm_r, kb * kBK, s, 0, 1, tt * 8, &r_full[slot]);
                     } else {
                         mbar_arrive(&r_full[slot]);
+                    }
+                    // R of the block kDownPrefetch stages ahead into L2: later in this
+                    // tile, or at the start of the next one
+                    const int pk = kb - kq * kDownKBlocksPerTile + kDownPrefetch;
+                    if (pk < kDownKBlocksPerTile) {
+                        if (full)
+                            for (int h = 0; h < 2; ++h)
+                                tma_prefetch_5d(&tm_r, (kb + kDownPrefetch) * kBK, s, 0, h, tt * 8);
+                    } else if (next_full) {
+                        const int nkb = nkq * kDownKBlocksPerTile + pk - kDownKBlocksPerTile;
+                        for (int h = 0; h < 2; ++h) tma_prefetch_5d(&tm_r, nkb * kBK, ns, 0, h, ntt * 8);
                     }
                 }
             }
@@ -310,6 +330,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             float ss[8], amax = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss[i] = 0.f;
+            // w_norm of this lane's 4 columns, loaded one K block ahead
+            uint2 wv_next = *reinterpret_cast<const uint2*>(
+                w_norm + s * kWidth + kq * kDownKBlocksPerTile * kBK + kc);
             for (int kb = kq * kDownKBlocksPerTile; kb < (kq + 1) * kDownKBlocksPerTile; ++kb, ++it) {
                 const int slot = it % kDownStages;
                 const uint32_t ph = (it / kDownStages) & 1;
@@ -329,7 +352,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                         }
                     }
                 }
-                const uint2 wv = *reinterpret_cast<const uint2*>(w_norm + k);
+                const uint2 wv = wv_next;
+                if (kb + 1 < (kq + 1) * kDownKBlocksPerTile)
+                    wv_next = *reinterpret_cast<const uint2*>(w_norm + k + kBK);
                 const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x), w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
                 if (!mbar_wait(&r_full[slot], ph, &abort_flag, status)) break;
                 uint8_t* ahi = sA(slot, 0);

@@ -150,6 +150,17 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// Asks L2 to fetch a 5D tile of a tensor map (no shared memory, no completion):
+// a later TMA load of the same tile then finds it in L2.
+__device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
+
 // TMA tile store from shared memory, tracked as a bulk async group of this thread.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z,
                                              const void* src) {
