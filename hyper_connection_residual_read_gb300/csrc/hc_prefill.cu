@@ -453,8 +453,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         tmem_dealloc(tmem, 512);
     }
     if (threadIdx.x == 0) {
-        // every fetch of this CTA is done; the last CTA to finish resets the pair
-        __threadfence();
+        // every fetch of this CTA has returned its tile (the fetch loop ended on the
+        // value it returned), so no fetch of this CTA can be performed after this
+        // count; the last CTA to count resets the pair for the next launch
         if (atomicAdd(sched + 1, 1) == (int)gridDim.x - 1) {
             atomicExch(sched, 0);
             atomicExch(sched + 1, 0);
@@ -878,8 +879,9 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
         tmem_dealloc(tmem, 512);
     }
     if (threadIdx.x == 0) {
-        // every fetch of this CTA is done; the last CTA to finish resets the pair
-        __threadfence();
+        // every fetch of this CTA has returned its tile (the fetch loop ended on the
+        // value it returned), so no fetch of this CTA can be performed after this
+        // count; the last CTA to count resets the pair for the next launch
         if (atomicAdd(sched + 1, 1) == (int)gridDim.x - 1) {
             atomicExch(sched, 0);
             atomicExch(sched + 1, 0);
