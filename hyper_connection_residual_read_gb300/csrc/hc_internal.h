@@ -58,9 +58,9 @@ struct Ctx {
     // prefill scratch
     __half* wd16 = nullptr;          // W_down as fp16 [kRank][kCols]
     __half* wu16 = nullptr;          // W_up as fp16 [kCols][kRank]
-    // down partials, tile-blocked and token-minor: [tiles][kStreams][4 K quarters]
-    // [kRank][128 tokens], and the sums of squares of R' [tiles][kStreams][4 K
-    // quarters][128 tokens], tiles = partial_tiles(max_tokens)
+    // down partials, tile-blocked, in column quads, token-minor: [tiles][kStreams]
+    // [4 K quarters][kRank / 4][128 tokens][4], and the sums of squares of R'
+    // [tiles][kStreams][4 K quarters][128 tokens], tiles = partial_tiles(max_tokens)
     float* partials = nullptr;
     float* ssq = nullptr;
     __half* lo16 = nullptr;          // lo as two fp16 terms [2][max_tokens][kRank]

@@ -429,15 +429,18 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             tc_fence_after();
             // tile-blocked and token-minor: [tile][stream][quarter][column][128 tokens],
             // so a warp's 32 tokens of one column are 128 contiguous bytes
+            // column quads, token-minor: [tile][stream][quarter][column / 4][128 tokens]
+            // [4 columns], so a lane stores 16 bytes and a warp 512 contiguous bytes
             const size_t prow = ((size_t)tt * kStreams + s) * kDownKSplit + kq;
-            float* dst = partials + prow * kRank * kTileM + m;
+            float4* dst = reinterpret_cast<float4*>(partials + prow * kRank * kTileM) + m;
 #pragma unroll 1
             for (int c0 = 0; c0 < kDownN; c0 += 32) {
                 float v[32];
                 tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
                 if (valid) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) dst[(c0 + i) * kTileM] = v[i];
+                    for (int i = 0; i < 8; ++i)
+                        dst[(c0 / 4 + i) * kTileM] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                 }
             }
             tc_fence_before();
@@ -466,11 +469,12 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
 // ---------------------------------------------------------------------------
 // lo = sum over the streams (in order) of rs times the sum of the stream's quarter
 // partials (in order); stored as two fp16 terms, or as one bf16 term in the bf16-lo
-// mode. The partials come tile-blocked and token-minor ([tile][stream][quarter]
-// [column][128 tokens]). A CTA takes one tile's 128 tokens and 32 of the columns:
-// for each (stream, quarter) it reads 32 consecutive 512-byte rows, the tokens
-// across the lanes; shared memory turns the block around so that each token's 32
-// columns leave as whole 32-byte sectors.
+// mode. The partials come tile-blocked, in column quads, token-minor ([tile][stream]
+// [quarter][column / 4][128 tokens][4 columns]). A CTA takes one tile's 128 tokens
+// and 32 of the columns (8 quads): for each (stream, quarter) these are 16 KB in one
+// piece, and a lane reads one token's quad, a warp 512 contiguous bytes; shared
+// memory turns the block around so that each token's 32 columns leave as whole
+// 32-byte sectors.
 // ---------------------------------------------------------------------------
 constexpr int kLoCols = 32;
 constexpr int kLoThreads = 512;    // 16 warps, two of the 32 columns each
@@ -502,34 +506,32 @@ lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ss
         }
     }
     __syncthreads();
-    // warp w sums columns w and w + 16 of the group for all 128 tokens: a lane takes
-    // four consecutive tokens, so one load instruction reads a whole 512-byte row
-    const int tr0 = 4 * lane;
-    float rs[4][kStreams];
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-#pragma unroll
-        for (int s = 0; s < kStreams; ++s) rs[k][s] = rs_s[s][tr0 + k];
+    // a thread takes (token, column quad) pairs: tokens across the lanes, so each load
+    // instruction of a warp reads 512 contiguous bytes; two pairs per thread
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        const int jl = warp + 16 * i, j = cg * kLoCols + jl;
+        const int pidx = threadIdx.x + i * kLoThreads;
+        const int tr = pidx & (kTileM - 1), jq = pidx >> 7;     // token, quad 0..7
+        const float4* p = reinterpret_cast<const float4*>(partials) +
+                          (base * (kRank / 4) + (size_t)cg * (kLoCols / 4) + jq) * kTileM + tr;
         float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int s = 0; s < kStreams; ++s) {
-            const float* p = partials + ((base + (size_t)s * kDownKSplit) * kRank + j) * kTileM + tr0;
-            float4 d = *reinterpret_cast<const float4*>(p);
+            const float4* ps = p + (size_t)s * kDownKSplit * (kRank / 4) * kTileM;
+            float4 d = ps[0];
 #pragma unroll
             for (int q = 1; q < kDownKSplit; ++q) {
-                const float4 w = *reinterpret_cast<const float4*>(p + (size_t)q * kRank * kTileM);
+                const float4 w = ps[(size_t)q * (kRank / 4) * kTileM];
                 d.x += w.x; d.y += w.y; d.z += w.z; d.w += w.w;
             }
-            v[0] = fmaf(rs[0][s], d.x, v[0]);
-            v[1] = fmaf(rs[1][s], d.y, v[1]);
-            v[2] = fmaf(rs[2][s], d.z, v[2]);
-            v[3] = fmaf(rs[3][s], d.w, v[3]);
+            const float r = rs_s[s][tr];
+            v[0] = fmaf(r, d.x, v[0]);
+            v[1] = fmaf(r, d.y, v[1]);
+            v[2] = fmaf(r, d.z, v[2]);
+            v[3] = fmaf(r, d.w, v[3]);
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) lo_s[tr0 + k][jl] = v[k];
+        for (int k = 0; k < 4; ++k) lo_s[tr][4 * jq + k] = v[k];
     }
     __syncthreads();
     // out: each token's 32 columns, 4 per lane, 8 lanes per token, 4 tokens per warp
