@@ -59,6 +59,11 @@ constexpr int kDownThreads = 448;
 // tiles from a run-time counter, as in the up tile below; the queue's consumers are
 // the MMA issuer, 8 converter warps and 4 epilogue warps
 constexpr int kDownTileQ = 4;
+// The 320-column accumulator as two halves of 160 columns, rotating through three
+// half-buffers of TMEM (480 of its 512 columns): tile lt writes half-buffer uses 2 lt
+// and 2 lt + 1, so its MMAs need only the first half of the previous tile drained.
+constexpr int kDownHalf = kDownN / 2;
+constexpr int kDownHalfBufs = 3;
 // R blocks are asked into L2 this many K blocks before their TMA load
 constexpr int kDownPrefetch = 3;
 constexpr int kDownTileQConsumers = 1 + 8 + 4;
@@ -185,7 +190,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
     __shared__ __align__(8) uint64_t r_full[kDownStages];
     __shared__ __align__(8) uint64_t tq_full[kDownTileQ], tq_empty[kDownTileQ];
     __shared__ int tile_q[kDownTileQ];
-    __shared__ __align__(8) uint64_t acc_full, acc_empty, ss_full[2];
+    __shared__ __align__(8) uint64_t acc_full, acc_empty[kDownHalfBufs], ss_full[2];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
     __shared__ float ss_s[2][kTileM];   // per-row sums of squares, by tile parity
@@ -200,7 +205,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             mbar_init(&r_full[i], 1);
         }
         mbar_init(&acc_full, 1);
-        mbar_init(&acc_empty, 128);
+        for (int i = 0; i < kDownHalfBufs; ++i) mbar_init(&acc_empty[i], 128);
         mbar_init(&ss_full[0], 256);
         mbar_init(&ss_full[1], 256);
         for (int i = 0; i < kDownTileQ; ++i) {
@@ -286,9 +291,17 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         if (lane == 0) {
             const uint32_t idesc = idesc_f16_f32(kTileM, kDownN / 2);
             int it = 0;
+            // waits until half-buffer use u may be written: its previous use drained
+            auto half_free = [&](int u) {
+                return mbar_wait(&acc_empty[u % kDownHalfBufs], ((u / kDownHalfBufs) & 1) ^ 1,
+                                 &abort_flag, status);
+            };
             for (int lt = 0; !abort_flag; ++lt) {
                 if (take_tile(lt, false) >= n_tiles) break;
-                if (!mbar_wait(&acc_empty, (lt & 1) ^ 1, &abort_flag, status)) break;
+                // the tile's two halves go to half-buffer uses 2 lt and 2 lt + 1
+                const uint32_t d0 = tmem + ((2 * lt) % kDownHalfBufs) * kDownHalf;
+                const uint32_t d1 = tmem + ((2 * lt + 1) % kDownHalfBufs) * kDownHalf;
+                if (!half_free(2 * lt)) break;
                 tc_fence_after();
                 bool ok = true;
                 for (int kl = 0; kl < kDownKBlocksPerTile; ++kl, ++it) {
@@ -297,18 +310,27 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     if (!mbar_wait(&full_bar[slot], ph, &abort_flag, status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t b0 = smem_u32(sB(slot));
+                    // first half, then second half: each half accumulates in the same
+                    // (K block, term, K step) order. The second half-buffer is usually
+                    // the one the epilogue is draining first from the previous tile, so
+                    // the first K block's first-half MMAs are issued before waiting on it.
 #pragma unroll
-                    for (int term = 0; term < 2; ++term) {
-                        const uint32_t a0 = smem_u32(sA(slot, term));
+                    for (int h = 0; h < 2; ++h) {
+                        if (h == 1 && kl == 0) {
+                            if (!half_free(2 * lt + 1)) { ok = false; break; }
+                            tc_fence_after();
+                        }
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                        for (int term = 0; term < 2; ++term) {
+                            const uint32_t a0 = smem_u32(sA(slot, term));
 #pragma unroll
-                            for (int h = 0; h < 2; ++h)
-                                mma_f16(tmem + h * (kDownN / 2), desc_sw128(a0 + kk * 32),
+                            for (int kk = 0; kk < kBK / 16; ++kk)
+                                mma_f16(h ? d1 : d0, desc_sw128(a0 + kk * 32),
                                         desc_sw128(b0 + h * (kDownBBytes / 2) + kk * 32), idesc,
                                         (kl | term | kk) != 0);
                         }
                     }
+                    if (!ok) break;
                     mma_commit(&empty_bar[slot]);
                 }
                 if (!ok) break;
@@ -401,7 +423,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             if (amax >= 65504.f) atomicOr(status, kStatusRange);
             // sums of squares per row: the 16 lanes that share a row, in a fixed order.
             // The buffer of this parity was last read by the epilogue two tiles ago,
-            // which has finished: the MMAs of this tile could not start before it.
+            // before it released that tile's second half-buffer; this tile's MMAs,
+            // which the conversions run at most three stages ahead of, waited for
+            // that release.
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 float v = ss[i];
@@ -427,26 +451,33 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             const bool valid = t < T;
             if (!mbar_wait(&acc_full, lt & 1, &abort_flag, status)) break;
             tc_fence_after();
-            // tile-blocked and token-minor: [tile][stream][quarter][column][128 tokens],
-            // so a warp's 32 tokens of one column are 128 contiguous bytes
-            // column quads, token-minor: [tile][stream][quarter][column / 4][128 tokens]
-            // [4 columns], so a lane stores 16 bytes and a warp 512 contiguous bytes
             const size_t prow = ((size_t)tt * kStreams + s) * kDownKSplit + kq;
-            float4* dst = reinterpret_cast<float4*>(partials + prow * kRank * kTileM) + m;
-#pragma unroll 1
-            for (int c0 = 0; c0 < kDownN; c0 += 32) {
-                float v[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
-                if (valid) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[(c0 / 4 + i) * kTileM] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&acc_empty);
+            // the sums of squares first: the converters finished them before the last
+            // MMA of the tile, and their buffer is rewritten two tiles later, which
+            // cannot start before this tile's second half is drained below
             if (!mbar_wait(&ss_full[lt & 1], (lt >> 1) & 1, &abort_flag, status)) break;
             if (valid) ssq[prow * kTileM + m] = ss_s[lt & 1][m];
+            // column quads, token-minor: [tile][stream][quarter][column / 4][128 tokens]
+            // [4 columns], so a lane stores 16 bytes and a warp 512 contiguous bytes;
+            // each half-buffer is released as soon as it has been read
+            float4* dst = reinterpret_cast<float4*>(partials + prow * kRank * kTileM) + m;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                const int hb = (2 * lt + h) % kDownHalfBufs;
+#pragma unroll 1
+                for (int c0 = 0; c0 < kDownHalf; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + hb * kDownHalf + c0, v);
+                    if (valid) {
+                        const int cq = (h * kDownHalf + c0) / 4;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[(cq + i) * kTileM] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&acc_empty[hb]);
+            }
         }
     }
     tc_fence_before();
