@@ -7,9 +7,10 @@ without a pending write, every read on a different weight set out of a rotation
 of 48 sets (630 MB of bf16 weights, larger than the 129 MB L2), so every read
 streams its 13 MB of weights from HBM. ``value`` = microseconds per read, device
 time from CUDA events around K steps (each step replayed as one CUDA graph;
-inputs resident in HBM). ``e2e`` = the same reads through the public call with
-the inputs copied from pinned host memory and the outputs copied back inside
-the timed region. Extra keys carry the 96-read cold round, per-T times and the
+inputs resident in HBM). ``e2e`` = the same reads through the public call (each
+step's 16 calls captured as one CUDA graph) with each step's inputs copied from
+pinned host memory and its outputs copied back inside the timed region; the copies
+of neighbouring steps run on two copy streams beside the reads. Extra keys carry the 96-read cold round, per-T times and the
 8K / 32K-token prefill chunks.
 
 ``--impl reference`` times the CPU oracle (float64, single thread) on a bounded
@@ -376,7 +377,10 @@ def gpu_arm(args) -> None:
 
     # --- e2e: pinned host inputs -> device, 16 reads via the public call, outputs back.
     #     A step's inputs sit in one pinned buffer and go over in one copy; its outputs
-    #     come back in one copy (how a caller would stage them) ---
+    #     come back in one copy (how a caller would stage them). Two device buffer sets
+    #     alternate between steps: step k+1's inputs go over on a copy stream while step
+    #     k computes, and step k's outputs come back on another while step k+1 computes.
+    #     Each step's reads are one CUDA graph of the public calls. ---
     in_off, out_off = [], []
     n_in = n_out = 0
     for T, p in SWEEP:
@@ -394,35 +398,101 @@ def gpu_arm(args) -> None:
         for key, o in offs.items():
             if o is not None:
                 pin_in[o[0]:o[0] + o[1]].copy_(torch.from_numpy(np.ascontiguousarray(a[key]).reshape(-1)))
-    dev_in = torch.empty(n_in, dtype=torch.float32, device=dev)
-    # outputs: fp32 region, then the bf16 and fp16 regions, as bytes
-    dev_out = torch.empty(n_out * 8, dtype=torch.uint8, device=dev)
     pin_out = torch.empty(n_out * 8, dtype=torch.uint8).pin_memory()
-    o32 = dev_out[:n_out * 4].view(torch.float32)
-    o16b = dev_out[n_out * 4:n_out * 6].view(torch.int16)
-    o16h = dev_out[n_out * 6:].view(torch.int16)
     h2d, d2h = n_in * 4, n_out * 8
-    views = []
-    for j, (T, p) in enumerate(SWEEP):
-        offs, (oo, _) = in_off[j], out_off[j]
-        v = {key: (dev_in[o[0]:o[0] + o[1]] if o is not None else None) for key, o in offs.items()}
-        views.append((v, o32[oo * 1:oo + T * 10240], o16b[oo:oo + T * 10240],
-                      o16h[oo:oo + T * 10240]))
+    dev_in = [torch.empty(n_in, dtype=torch.float32, device=dev) for _ in range(2)]
+    # outputs: fp32 region, then the bf16 and fp16 regions, as bytes
+    dev_out = [torch.empty(n_out * 8, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+    def step_views(b):
+        o32 = dev_out[b][:n_out * 4].view(torch.float32)
+        o16b = dev_out[b][n_out * 4:n_out * 6].view(torch.int16)
+        o16h = dev_out[b][n_out * 6:].view(torch.int16)
+        views = []
+        for j, (T, p) in enumerate(SWEEP):
+            offs, (oo, _) = in_off[j], out_off[j]
+            v = {key: (dev_in[b][o[0]:o[0] + o[1]] if o is not None else None)
+                 for key, o in offs.items()}
+            views.append((v, o32[oo:oo + T * 10240], o16b[oo:oo + T * 10240],
+                          o16h[oo:oo + T * 10240]))
+        return views
+
+    e2e_views = [step_views(b) for b in range(2)]
+
+    def enqueue_reads(g, b):
+        for j in range(len(SWEEP)):
+            v, f32, b16, h16 = e2e_views[b][j]
+            W = sets[g * len(SWEEP) + j]
+            hc.hc_read(SWEEP[j][0], v["R"], v["P"], W["w_norm"], W["W_down"], W["W_up"],
+                       v["Rmix"], f32, b16, h16, stream=stream)
+
+    e2e_graphs = {}
+    with torch.cuda.stream(stream):
+        for g in range(n_groups):
+            for b in range(2):
+                enqueue_reads(g, b)
+        stream.synchronize()
+        for g in range(n_groups):
+            for b in range(2):
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=stream):
+                    enqueue_reads(g, b)
+                e2e_graphs[(g, b)] = gr
+    h2d_stream = torch.cuda.Stream(device=dev)
+    d2h_stream = torch.cuda.Stream(device=dev)
+    ev = {(kind, b): torch.cuda.Event() for kind in ("in", "done", "out") for b in range(2)}
+    for b in range(2):   # every buffer starts free
+        for kind in ("done", "out"):
+            ev[(kind, b)].record(stream)
 
     def e2e_step(k):
-        g = k % n_groups
-        with torch.cuda.stream(stream):
-            dev_in.copy_(pin_in, non_blocking=True)
-            for j in range(len(SWEEP)):
-                i = g * len(SWEEP) + j
-                v, f32, b16, h16 = views[j]
-                W = sets[i]
-                hc.hc_read(SWEEP[j][0], v["R"], v["P"], W["w_norm"], W["W_down"], W["W_up"],
-                           v["Rmix"], f32, b16, h16, stream=stream)
-            pin_out.copy_(dev_out, non_blocking=True)
+        b = k % 2
+        # inputs of this step into buffer b once the step that last read it is done
+        h2d_stream.wait_event(ev[("done", b)])
+        with torch.cuda.stream(h2d_stream):
+            dev_in[b].copy_(pin_in, non_blocking=True)
+        ev[("in", b)].record(h2d_stream)
+        # the reads, once the inputs are over and buffer b's last outputs have left
+        stream.wait_event(ev[("in", b)])
+        stream.wait_event(ev[("out", b)])
+        with torch.cuda.stream(stream):   # a graph replays on the current stream
+            e2e_graphs[(k % n_groups, b)].replay()
+        ev[("done", b)].record(stream)
+        # the outputs back while the next step computes
+        d2h_stream.wait_event(ev[("done", b)])
+        with torch.cuda.stream(d2h_stream):
+            pin_out.copy_(dev_out[b], non_blocking=True)
+        ev[("out", b)].record(d2h_stream)
+
+    def e2e_run(steps, warmup):
+        """Device time of `steps` pipelined steps, from the first copy to the last
+        output back on the host, after `warmup` steps."""
+        for k in range(warmup):
+            e2e_step(k)
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        h2d_stream.wait_event(e0)
+        d2h_stream.wait_event(e0)
+        for k in range(warmup, warmup + steps):
+            e2e_step(k)
+        stream.wait_stream(d2h_stream)
+        e1.record(stream)
+        barrier()
+        return reduce_max(e0.elapsed_time(e1), world, dev)
 
     e2e_steps = max(10, min(args.steps, 500))
-    ms_e = timed(e2e_step, e2e_steps, min(args.warmup, 5) + 3)
+    ms_e = e2e_run(e2e_steps, min(args.warmup, 5) + 3)
+
+    def e2e_serial_step(k):
+        # the same step with copies and reads in order on one stream: no overlap
+        with torch.cuda.stream(stream):
+            dev_in[0].copy_(pin_in, non_blocking=True)
+            e2e_graphs[(k % n_groups, 0)].replay()
+            pin_out.copy_(dev_out[0], non_blocking=True)
+
+    ms_e_serial = timed(e2e_serial_step, e2e_steps, 3)
     e2e_us = us_per_unit(ms_e, e2e_steps * reads_per_step, world)
 
     # --- prefill chunks: the whole read, and the fused up + gate + mix stage alone
@@ -529,7 +599,10 @@ def gpu_arm(args) -> None:
                      "bytes_per_step": step_bytes},
         "clocks": clocks,
         "e2e": {"value": e2e_us, "unit": "us/read", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "pipelining": "step k+1's inputs and step k-1's outputs cross on two copy "
+                              "streams while step k computes",
+                "serial_us": us_per_unit(ms_e_serial, e2e_steps * reads_per_step, world)},
         "gpu_launches": kernel_launches_per_step * args.steps,
         "decode_by_T": per_t,
         "decode_paths_us_by_T_with_P": per_t_paths,
