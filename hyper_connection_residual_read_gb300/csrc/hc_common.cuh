@@ -51,6 +51,16 @@ __device__ __forceinline__ float gate_value(float u, float rp) {
     return rp * __fdividef(1.0f, 1.0f + expf(-u));
 }
 
+// The RMS-norm scale 1 / sqrt(a) of a stream, a = mean(R'^2) + eps. The hardware
+// reciprocal square root (rsqrtf, within 2 ulp) refined by one step of Newton's method
+// for f(y) = 1/y^2 - a, y <- y (3 - a y^2) / 2, which about doubles its correct bits:
+// within about 1 ulp, as close as 1 / sqrtf(a) with its two roundings, but without the
+// IEEE square root and division, whose latency sat on the decode read's critical path.
+__device__ __forceinline__ float inv_rms(float a) {
+    const float y = rsqrtf(a);
+    return y * fmaf(-0.5f * a, y * y, 1.5f);
+}
+
 // Row s of the token's 4x4 mix applied to the 4 gated values (q = 0..3 in order).
 __device__ __forceinline__ float mix_row(const float* m_row, float g0, float g1, float g2,
                                          float g3) {

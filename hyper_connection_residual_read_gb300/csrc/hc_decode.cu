@@ -212,7 +212,7 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
 #pragma unroll
         for (int st = 0; st < kStreams; ++st) {
             const float ss = inbox[2 * st][t][2] + inbox[2 * st + 1][t][2];
-            const float rs = 1.0f / sqrtf(ss / (float)kWidth + eps);
+            const float rs = inv_rms(fmaf(ss, 1.0f / (float)kWidth, eps));
             const float d = inbox[2 * st][t][jj] + inbox[2 * st + 1][t][jj];
             v = fmaf(rs, d, v);
         }

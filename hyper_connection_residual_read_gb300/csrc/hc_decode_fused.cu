@@ -233,7 +233,7 @@ decode_fused_kernel(const float* R, const float* P, const uint16_t* __restrict__
 #pragma unroll
         for (int st = 0; st < kStreams; ++st) {
             const float ss = ssv[2 * st] + ssv[2 * st + 1];
-            const float rs = 1.0f / sqrtf(ss / (float)kWidth + eps);
+            const float rs = inv_rms(fmaf(ss, 1.0f / (float)kWidth, eps));
             const float d = pv[2 * st] + pv[2 * st + 1];
             v = fmaf(rs, d, v);
         }

@@ -533,7 +533,7 @@ lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ss
 #pragma unroll
                 for (int q = 1; q < kDownKSplit; ++q) ss += q4[q * kTileM];
             }
-            rs_s[s][tr] = 1.0f / sqrtf(ss / (float)kWidth + eps);
+            rs_s[s][tr] = inv_rms(fmaf(ss, 1.0f / (float)kWidth, eps));
         }
     }
     __syncthreads();
