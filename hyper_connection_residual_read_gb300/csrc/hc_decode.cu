@@ -32,6 +32,8 @@
 // stream, so their loads must stay after the wait.
 #include <cooperative_groups.h>
 
+#include <atomic>
+
 #include "hc_common.cuh"
 #include "hc_internal.h"
 
@@ -41,8 +43,16 @@ namespace {
 
 constexpr int kDownThreads = 320;   // 10 warps: 2 row groups x 5 column groups
 constexpr int kDownColGroups = 5;   // 5 x 256 columns = 1280
-constexpr int kUpWarps = 4;         // 4 columns per warp, 16 per CTA
-constexpr int kUpThreads = 32 * kUpWarps;
+// The up kernel: a warp owns 4 output columns. Chunks of up to 4 tokens use 128 CTAs
+// of 5 warps and reserve enough shared memory that an SM holds at most one of them
+// (the down kernel of the same or the next read still fits beside it); chunks of 5-8
+// tokens use 160 CTAs of 4 warps with no reservation. Launched early by programmatic
+// dependent launch, up CTAs otherwise land up to four on one SM while others have
+// none. Measured: T = 1 6.10 -> 5.00 us per read, T = 2-4 0.2-0.6 us faster; at
+// T = 5-8 one CTA per SM did not pay.
+template <int T> constexpr int kUpWarpsT = T <= 4 ? 5 : 4;
+template <int T> constexpr int kUpThreadsT = 32 * kUpWarpsT<T>;
+template <int T> constexpr int kUpReserveT = T <= 4 ? 120 * 1024 : 0;   // dynamic shared bytes
 
 // Sum over the 32 lanes of eight per-lane values, one per row. On return the
 // lanes whose bits (4,3,2) equal the row's index hold that row's full sum:
@@ -225,7 +235,7 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
 constexpr int kLoPart = 44;
 
 template <int T>
-__global__ void __launch_bounds__(kUpThreads)
+__global__ void __launch_bounds__(kUpThreadsT<T>)
 up_mix_kernel(const float* R, const float* P, const uint16_t* __restrict__ W_up,
               const float* lo, const float* Rmix, float* out_f32, uint16_t* out_bf16,
               uint16_t* out_fp16) {
@@ -233,7 +243,7 @@ up_mix_kernel(const float* R, const float* P, const uint16_t* __restrict__ W_up,
     const int warp = tid >> 5, lane = tid & 31;
     const int cc = lane >> 3;                  // which of the warp's 4 columns
     const int part = lane & 7;                 // which 40 of the 320 inputs
-    const int c = (blockIdx.x * kUpWarps + warp) * 4 + cc;   // output column 0..2559
+    const int c = (blockIdx.x * kUpWarpsT<T> + warp) * 4 + cc;   // output column 0..2559
     const int sp = part & 3;                   // stream gated by this lane (lanes 0..3)
 
     // 1. the 4 up rows of column c (one per stream), this lane's 40 inputs each
@@ -271,16 +281,16 @@ up_mix_kernel(const float* R, const float* P, const uint16_t* __restrict__ W_up,
     // lo of the chunk ([T][320], contiguous): every load is issued before the first
     // store, so the staging costs one round trip whatever T is
     constexpr int kLoVec = T * kRank / 4;
-    constexpr int kLoIter = (kLoVec + kUpThreads - 1) / kUpThreads;
+    constexpr int kLoIter = (kLoVec + kUpThreadsT<T> - 1) / kUpThreadsT<T>;
     float4 lv[kLoIter];
 #pragma unroll
     for (int i = 0; i < kLoIter; ++i) {
-        const int e = tid + i * kUpThreads;
+        const int e = tid + i * kUpThreadsT<T>;
         if (e < kLoVec) lv[i] = reinterpret_cast<const float4*>(lo)[e];
     }
 #pragma unroll
     for (int i = 0; i < kLoIter; ++i) {
-        const int e = tid + i * kUpThreads;
+        const int e = tid + i * kUpThreadsT<T>;
         if (e < kLoVec) {
             const int t = e / (kRank / 4), j = 4 * (e % (kRank / 4));
             *reinterpret_cast<float4*>(&lo_s[t][j / 40][j % 40]) = lv[i];
@@ -356,12 +366,12 @@ up_mix_kernel(const float* R, const float* P, const uint16_t* __restrict__ W_up,
 
 // Launch with programmatic stream serialisation (see pdl_wait).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t st,
-                       Args... args) {
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -371,18 +381,34 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStre
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Allows up_mix_kernel<T> its shared-memory reservation on this device, once.
+template <int T>
+cudaError_t allow_up_reserve(int device) {
+    static std::atomic<unsigned long long> done{0};
+    if (kUpReserveT<T> == 0) return cudaSuccess;
+    const unsigned long long bit = device >= 0 && device < 64 ? 1ull << device : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(
+        up_mix_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUpReserveT<T>);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 template <int T>
 cudaError_t launch_chunk(const Ctx& ctx, const ReadArgs& a, int t0, cudaStream_t st) {
     const size_t off = (size_t)t0 * kCols;
     const float* R = a.R + off;
     const float* P = a.P ? a.P + off : nullptr;
     float* lo = ctx.s.lo + (size_t)t0 * kRank;
-    cudaError_t e = launch_pdl(down_slice_kernel<T>, dim3(kDownSlices, kDownRowBlocks),
-                               dim3(kDownThreads), st, R, P, a.w_norm, a.W_down, lo, ctx.eps);
+    cudaError_t e = allow_up_reserve<T>(ctx.device);
     if (e != cudaSuccess) return e;
-    return launch_pdl(up_mix_kernel<T>, dim3(kWidth / (4 * kUpWarps)), dim3(kUpThreads), st,
-                      R, P, a.W_up, (const float*)lo, a.Rmix + (size_t)t0 * 16,
-                      a.out_f32 + off, a.out_bf16 + off, a.out_fp16 + off);
+    e = launch_pdl(down_slice_kernel<T>, dim3(kDownSlices, kDownRowBlocks), dim3(kDownThreads), 0,
+                   st, R, P, a.w_norm, a.W_down, lo, ctx.eps);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(up_mix_kernel<T>, dim3(kWidth / (4 * kUpWarpsT<T>)), dim3(kUpThreadsT<T>),
+                      (size_t)kUpReserveT<T>, st, R, P, a.W_up, (const float*)lo,
+                      a.Rmix + (size_t)t0 * 16, a.out_f32 + off, a.out_bf16 + off,
+                      a.out_fp16 + off);
 }
 
 }  // namespace
