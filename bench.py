@@ -41,11 +41,11 @@ N_SETS = 48
 EPS = float(np.float32(1e-6))
 
 # DRAM bytes (read + write) that ncu counted for one 4-token read with a pending
-# write, both decode kernels together (down_slice_kernel<4> 6,924,058 B,
-# up_mix_kernel<4> 6,910,490 B; 48 rotated weight sets, so the weights come from
+# write, both decode kernels together (down_slice_kernel<4> 6,918,733 B,
+# up_mix_kernel<4> 6,911,232 B; 48 rotated weight sets, so the weights come from
 # DRAM). The sweep's traffic is taken as its algorithmic bytes times the ratio of
 # this figure to the same read's algorithmic bytes.
-NCU_TRAFFIC_T4_P = 13834547
+NCU_TRAFFIC_T4_P = 13829965
 
 
 def read_bytes(T: int, with_P: bool) -> int:
