@@ -36,6 +36,7 @@
 
 #include "hc_common.cuh"
 #include "hc_internal.h"
+#include "hc_tc.cuh"
 
 namespace hc {
 
@@ -364,6 +365,196 @@ up_mix_kernel(const float* R, const float* P, const uint16_t* __restrict__ W_up,
     }
 }
 
+// ---------------------------------------------------------------------------
+// up_mix_tc_kernel - the up projection of a decode chunk on the tcgen05 tensor
+// cores: all of the chunk's tokens in one pass of MMAs instead of a loop over them.
+// A CTA owns 32 output columns: A = their 128 W_up rows (4 streams x 32 columns,
+// bf16 as stored, loaded by TMA before the dependency wait). B = lo of the chunk's
+// tokens as three bf16 terms hi + mid + low (x - hi and x - hi - mid are exact in
+// fp32, so the three carry x to about 2^-27 of its size), the terms side by side as
+// B rows term * T + t, so that one MMA takes all three: N = 16 up to 5 tokens, 32
+// above. D = 128 x N fp32 in TMEM; each bf16 product is exact in fp32 and each term
+// accumulates 20 MMAs deep; the epilogue adds a token's three columns, smallest
+// first. TMEM lane = row, so warp w holds stream w and lane l column l; the gate is
+// applied there, the four streams of a column meet in shared memory, and the mix
+// writes each output row with stores that are contiguous across the warp.
+// ---------------------------------------------------------------------------
+constexpr int kTcCols = 32;                          // output columns per CTA
+constexpr int kTcRows = kStreams * kTcCols;          // 128 W_up rows: MMA M
+constexpr int kTcKB = 64;                            // K per 128-byte swizzle row
+constexpr int kTcKBlocks = kRank / kTcKB;            // 5
+template <int T> constexpr int kTcN = 3 * T <= 16 ? 16 : 32;   // MMA N: 3 terms x T tokens
+constexpr int kTcABytes = kTcRows * kTcKB * 2;       // 16 KB per K block
+constexpr int kTcBBytesMax = 32 * kTcKB * 2;         // 4 KB per K block at N = 32
+constexpr int kTcThreads = 128;
+constexpr int kTcSmem = kTcKBlocks * kTcABytes + kTcKBlocks * kTcBBytesMax + 1024;
+constexpr int kTcTmemCols = 32;                      // the smallest TMEM allocation
+
+// A bounded wait on an mbarrier phase: false after 2 s, with the timeout recorded in
+// the status word when there is one (the allocation-free entry has none).
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int* status) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait_suspend(bar, parity, tc::kSuspendHintNs)) {
+        if (tc::globaltimer() - t0 > tc::kWaitLimitNs) {
+            if (status != nullptr) atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+// x as the sum of three bf16 terms, packed in pairs: (x0, x1) -> hi, mid, low words.
+__device__ __forceinline__ void split3_bf16(float x0, float x1, uint32_t& hi, uint32_t& mid,
+                                            uint32_t& low) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float r0 = x0 - __low2float(h), r1 = x1 - __high2float(h);
+    const __nv_bfloat162 m = __floats2bfloat162_rn(r0, r1);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(r0 - __low2float(m), r1 - __high2float(m));
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    mid = *reinterpret_cast<const uint32_t*>(&m);
+    low = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+template <int T>
+__global__ void __launch_bounds__(kTcThreads, 1)
+up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, const float* P,
+                 const float* lo, const float* Rmix, float* out_f32, uint16_t* out_bf16,
+                 uint16_t* out_fp16, int* status) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned: the 128-byte swizzle pattern repeats every 8 rows of 128 B
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int kN = kTcN<T>, kBBytes = kN * kTcKB * 2;
+    uint8_t* sA = smem;                                  // [K block][128 rows][128 B]
+    uint8_t* sB = smem + kTcKBlocks * kTcABytes;         // [K block][N rows][128 B]
+    __shared__ __align__(8) uint64_t w_full, mma_done;
+    __shared__ uint32_t tmem_slot;
+    __shared__ float g_s[T][kStreams][kTcCols];
+    __shared__ __align__(16) float m_s[T][16];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x * kTcCols + lane;           // this thread's output column
+
+    if (tid == 0) {
+        tc::mbar_init(&w_full, 1);
+        tc::mbar_init(&mma_done, 1);
+        tc::fence_barrier_init();
+    }
+    if (warp == 0) tc::tmem_alloc(&tmem_slot, kTcTmemCols);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    // 1. the CTA's W_up rows (layer parameters, read before the wait): per K block
+    //    one 32-row box per stream
+    if (tid == 0) {
+        tc::mbar_arrive_expect_tx(&w_full, kTcKBlocks * kTcABytes);
+#pragma unroll
+        for (int kb = 0; kb < kTcKBlocks; ++kb)
+#pragma unroll
+            for (int s = 0; s < kStreams; ++s)
+                tc::tma_load_2d(sA + kb * kTcABytes + s * (kTcABytes / kStreams), &tm_wu, kb * kTcKB,
+                                s * kWidth + blockIdx.x * kTcCols, &w_full);
+    }
+    // this thread's residual (and pending write) into L2 while the down kernel runs:
+    // a warp's 32 columns of a stream are one 128-byte line
+    if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+            prefetch_l2(R + (size_t)t * kCols + warp * kWidth + c);
+            if (P != nullptr) prefetch_l2(P + (size_t)t * kCols + warp * kWidth + c);
+        }
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // 2. lo of the chunk as three bf16 terms in the B tiles (K-major, 128-byte
+    //    swizzled, tokens as rows), R' of this thread's (stream, column), the mix
+    float rp[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) rp[t] = R[(size_t)t * kCols + warp * kWidth + c];
+    if (P != nullptr) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) rp[t] += P[(size_t)t * kCols + warp * kWidth + c];
+    }
+    // (rows past 3 T stay unwritten: they only feed D columns nobody reads)
+    constexpr int kQuads = T * kRank / 4;                // float4 granules of lo
+    constexpr int kIters = (kQuads + kTcThreads - 1) / kTcThreads;
+    float4 xq[kIters];
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {                   // every load in flight at once
+        const int e = tid + i * kTcThreads;
+        if (e < kQuads) xq[i] = reinterpret_cast<const float4*>(lo)[e];
+    }
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {
+        const int e = tid + i * kTcThreads;
+        if (e >= kQuads) continue;
+        const int t = e / (kRank / 4), k = 4 * (e % (kRank / 4));
+        uint32_t h0, m0, l0, h1, m1, l1;
+        split3_bf16(xq[i].x, xq[i].y, h0, m0, l0);
+        split3_bf16(xq[i].z, xq[i].w, h1, m1, l1);
+        uint8_t* b = sB + (k / kTcKB) * kBBytes;
+        const int kin = k % kTcKB;
+        *reinterpret_cast<uint2*>(b + tc::sw128_offset(t, kin)) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2*>(b + tc::sw128_offset(T + t, kin)) = make_uint2(m0, m1);
+        *reinterpret_cast<uint2*>(b + tc::sw128_offset(2 * T + t, kin)) = make_uint2(l0, l1);
+    }
+    if (tid < T * 4) reinterpret_cast<float4*>(&m_s[0][0])[tid] = reinterpret_cast<const float4*>(Rmix)[tid];
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+
+    // 3. the MMAs, issued by one thread once the weights have landed
+    __shared__ int ok_s;
+    if (tid == 0) {
+        bool ok = tc_wait(&w_full, 0, status);
+        if (!ok) ok = tc_wait(&w_full, 0, status);   // give the copies in flight one more limit
+        if (ok) {
+            tc::tc_fence_after();
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(kTcRows, kN);
+#pragma unroll
+            for (int kb = 0; kb < kTcKBlocks; ++kb)
+#pragma unroll
+                for (int kk = 0; kk < kTcKB / 16; ++kk)
+                    tc::mma_f16(tmem, tc::desc_sw128(tc::smem_u32(sA + kb * kTcABytes) + kk * 32),
+                                tc::desc_sw128(tc::smem_u32(sB + kb * kBBytes) + kk * 32), idesc,
+                                (kb | kk) != 0);
+            tc::mma_commit(&mma_done);
+        }
+        ok_s = ok;
+    }
+    __syncthreads();
+    const bool ok = ok_s && tc_wait(&mma_done, 0, status);
+
+    // 4. gate in place (warp = stream, lane = column), the streams meet in shared
+    //    memory, then the mix and the three images
+    if (ok) {
+        tc::tc_fence_after();
+        float u[32];
+        tc::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16), u);
+#pragma unroll
+        for (int t = 0; t < T; ++t)
+            g_s[t][warp][lane] = gate_value((u[2 * T + t] + u[T + t]) + u[t], rp[t]);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (ok) {
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+            const float m = mix_row(&m_s[t][warp * 4], g_s[t][0][lane], g_s[t][1][lane],
+                                    g_s[t][2][lane], g_s[t][3][lane]);
+            const size_t off = (size_t)t * kCols + warp * kWidth + c;
+            out_f32[off] = m;
+            out_bf16[off] = to_bf16_bits(m);
+            out_fp16[off] = to_fp16_bits(m);
+        }
+    }
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTcTmemCols);
+    }
+}
+
 // Launch with programmatic stream serialisation (see pdl_wait).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -381,17 +572,33 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Allows up_mix_kernel<T> its shared-memory reservation on this device, once.
+// Which up kernel a chunk of T tokens runs. Measured, µs per read with P: the
+// tcgen05 kernel 6.13, 6.14, 6.67, 7.21, 7.94, 8.68, 9.63, 10.20 for T = 1..8; the
+// CUDA-core kernel 5.0, 6.1, 7.1, 7.9, 8.8, 9.7, 10.8, 12.2. The tcgen05 kernel runs
+// every T, so that a token's bits do not depend on the other tokens of its call.
+template <int T> constexpr bool kUpTcT = true;
+
+// Allows `kernel` `bytes` of dynamic shared memory on this device, once per device.
+template <typename K>
+cudaError_t allow_smem(K kernel, int bytes, int device, std::atomic<unsigned long long>& done) {
+    if (bytes == 0) return cudaSuccess;
+    const unsigned long long bit = device >= 0 && device < 64 ? 1ull << device : 0;
+    if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 template <int T>
 cudaError_t allow_up_reserve(int device) {
     static std::atomic<unsigned long long> done{0};
-    if (kUpReserveT<T> == 0) return cudaSuccess;
-    const unsigned long long bit = device >= 0 && device < 64 ? 1ull << device : 0;
-    if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(
-        up_mix_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kUpReserveT<T>);
-    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
-    return e;
+    return allow_smem(up_mix_kernel<T>, kUpReserveT<T>, device, done);
+}
+
+template <int T>
+cudaError_t allow_up_tc(int device) {
+    static std::atomic<unsigned long long> done{0};
+    return allow_smem(up_mix_tc_kernel<T>, kTcSmem, device, done);
 }
 
 template <int T>
@@ -400,11 +607,18 @@ cudaError_t launch_chunk(const Ctx& ctx, const ReadArgs& a, int t0, cudaStream_t
     const float* R = a.R + off;
     const float* P = a.P ? a.P + off : nullptr;
     float* lo = ctx.s.lo + (size_t)t0 * kRank;
-    cudaError_t e = allow_up_reserve<T>(ctx.device);
+    CUtensorMap tm_wu;
+    if (kUpTcT<T> && !encode_w_up_bf16(&tm_wu, a.W_up, kTcCols)) return cudaErrorInvalidValue;
+    cudaError_t e = kUpTcT<T> ? allow_up_tc<T>(ctx.device) : allow_up_reserve<T>(ctx.device);
     if (e != cudaSuccess) return e;
     e = launch_pdl(down_slice_kernel<T>, dim3(kDownSlices, kDownRowBlocks), dim3(kDownThreads), 0,
                    st, R, P, a.w_norm, a.W_down, lo, ctx.eps);
     if (e != cudaSuccess) return e;
+    if (kUpTcT<T>)
+        return launch_pdl(up_mix_tc_kernel<T>, dim3(kWidth / kTcCols), dim3(kTcThreads),
+                          (size_t)kTcSmem, st, tm_wu, R, P, (const float*)lo,
+                          a.Rmix + (size_t)t0 * 16, a.out_f32 + off, a.out_bf16 + off,
+                          a.out_fp16 + off, ctx.s.status);
     return launch_pdl(up_mix_kernel<T>, dim3(kWidth / (4 * kUpWarpsT<T>)), dim3(kUpThreadsT<T>),
                       (size_t)kUpReserveT<T>, st, R, P, a.W_up, (const float*)lo,
                       a.Rmix + (size_t)t0 * 16, a.out_f32 + off, a.out_bf16 + off,

@@ -92,6 +92,10 @@ struct ReadArgs {
     int out_cols = kCols;            // output floats per token (kWidth for the y read-out)
 };
 
+// A TMA map over the caller's W_up [kCols][kRank] bf16, in boxes of 64 K x box_rows
+// rows with the 128-byte swizzle (the K-major layout of a tcgen05 operand).
+bool encode_w_up_bf16(CUtensorMap* map, const uint16_t* W_up, int box_rows);
+
 // Decode kernels for any T: launched in chunks of kDecodeMaxT tokens.
 cudaError_t launch_decode(const Ctx& ctx, const ReadArgs& a, cudaStream_t st);
 
