@@ -17,11 +17,17 @@
 //      to finish; a cluster needs no global counter), so the result is bitwise
 //      repeatable.
 //
-//  up_mix_kernel - a warp owns 4 output columns; 8 lanes per column each sum 40
-//      of the 320 inputs for all 4 up rows i = s*2560 + c of that column, an xor
-//      tree finishes the dots, then the gate and the 4x4 mix run in registers
-//      ("#1370 prefill: opt-in STRATA_HC_UPMIX=1 on CUDA ...", "What it does":
-//      the mix in registers, writing mixed with its BF16 / FP16 images).
+//  up_mix_tc_kernel - the up projection of all the chunk's tokens at once on the
+//      tcgen05 tensor cores (W_up rows as A, lo as three bf16 terms as B, D in
+//      TMEM), then the gate and the 4x4 mix in its epilogue ("#1370 prefill:
+//      opt-in STRATA_HC_UPMIX=1 on CUDA ...", "What it does": the mix fused into
+//      the up projection, writing mixed with its BF16 / FP16 images). The launcher
+//      uses it for every T.
+//
+//  up_mix_kernel - the same step on CUDA cores, not launched by default: a warp
+//      owns 4 output columns; 8 lanes per column each sum 40 of the 320 inputs for
+//      all 4 up rows i = s*2560 + c of that column, an xor tree finishes the dots,
+//      then the gate and the 4x4 mix run in registers.
 //
 // Weights are loaded straight into registers with 16-byte streaming loads issued
 // before anything else, so a kernel's whole weight matrix is in flight at once.
