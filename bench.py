@@ -41,11 +41,11 @@ N_SETS = 48
 EPS = float(np.float32(1e-6))
 
 # DRAM bytes (read + write) that ncu counted for one 4-token read with a pending
-# write, both decode kernels together (down_slice_kernel<4> 6,918,733 B,
-# up_mix_kernel<4> 6,911,232 B; 48 rotated weight sets, so the weights come from
+# write, both decode kernels together (down_slice_kernel<4> 6,918,707 B,
+# up_mix_tc_kernel<4> 6,910,515 B; 48 rotated weight sets, so the weights come from
 # DRAM). The sweep's traffic is taken as its algorithmic bytes times the ratio of
 # this figure to the same read's algorithmic bytes.
-NCU_TRAFFIC_T4_P = 13829965
+NCU_TRAFFIC_T4_P = 13829222
 
 
 def read_bytes(T: int, with_P: bool) -> int:
@@ -590,7 +590,7 @@ def gpu_arm(args) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": workload_config(),
-        "roofline": {"bound": "hbm", "kernel": "decode read (down_slice + up_mix kernels)",
+        "roofline": {"bound": "hbm", "kernel": "decode read (down_slice + up_mix_tc kernels)",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "traffic_basis": "ncu DRAM bytes of one T=4 read with P, scaled to the "
