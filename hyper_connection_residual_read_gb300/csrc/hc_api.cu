@@ -258,11 +258,7 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     c.sm_count = prop.multiProcessorCount;
     strncpy(c.name, prop.name, sizeof(c.name) - 1);
     bool ok = true;
-    // lo: [max_tokens][kRank] for the one-kernel decode, and at least the four stream
-    // parts of one chunk ([4][kDecodeMaxT][kRank]) for the two-kernel decode
-    const size_t lo_rows = (size_t)max_tokens > (size_t)kStreams * kDecodeMaxT
-                               ? (size_t)max_tokens : (size_t)kStreams * kDecodeMaxT;
-    ok &= cudaMalloc(&c.s.lo, sizeof(float) * lo_rows * kRank) == cudaSuccess;
+    ok &= cudaMalloc(&c.s.lo, sizeof(float) * (size_t)max_tokens * kRank) == cudaSuccess;
     ok &= cudaMalloc(&c.s.status, sizeof(int)) == cudaSuccess;
     ok &= cudaMalloc(&c.s.sync, 2 * sizeof(unsigned)) == cudaSuccess;
     ok &= cudaMalloc(&c.s.sched, 2 * kSchedPairs * sizeof(int)) == cudaSuccess;

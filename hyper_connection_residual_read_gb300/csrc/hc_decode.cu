@@ -388,7 +388,6 @@ up_mix_kernel(const float* R, const float* P, const uint16_t* __restrict__ W_up,
 constexpr int kTcCols = 32;                          // output columns per CTA
 constexpr int kTcRows = kStreams * kTcCols;          // 128 W_up rows: MMA M
 constexpr int kTcKB = 64;                            // K per 128-byte swizzle row
-constexpr int kLoPartStride = kDecodeMaxT * kRank;   // floats per stream part of lo
 constexpr int kTcKBlocks = kRank / kTcKB;            // 5
 template <int T> constexpr int kTcN = 3 * T <= 16 ? 16 : 32;   // MMA N: 3 terms x T tokens
 constexpr int kTcABytes = kTcRows * kTcKB * 2;       // 16 KB per K block
@@ -423,9 +422,7 @@ __device__ __forceinline__ void split3_bf16(float x0, float x1, uint32_t& hi, ui
     low = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// kParts: lo comes as the four streams' parts from down_tc_kernel, added here in
-// stream order ([4][8 tokens][320]); otherwise as one [T][320] array.
-template <int T, bool kParts>
+template <int T>
 __global__ void __launch_bounds__(kTcThreads, 1)
 up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, const float* P,
                  const float* lo, const float* Rmix, float* out_f32, uint16_t* out_bf16,
@@ -493,17 +490,7 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {                   // every load in flight at once
         const int e = tid + i * kTcThreads;
-        if (e >= kQuads) continue;
-        if (kParts) {
-            float4 q[kStreams];
-#pragma unroll
-            for (int st = 0; st < kStreams; ++st)
-                q[st] = reinterpret_cast<const float4*>(lo + (size_t)st * kLoPartStride)[e];
-            xq[i] = make_float4(((q[0].x + q[1].x) + q[2].x) + q[3].x, ((q[0].y + q[1].y) + q[2].y) + q[3].y,
-                                ((q[0].z + q[1].z) + q[2].z) + q[3].z, ((q[0].w + q[1].w) + q[2].w) + q[3].w);
-        } else {
-            xq[i] = reinterpret_cast<const float4*>(lo)[e];
-        }
+        if (e < kQuads) xq[i] = reinterpret_cast<const float4*>(lo)[e];
     }
 #pragma unroll
     for (int i = 0; i < kIters; ++i) {
@@ -574,202 +561,6 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
     }
 }
 
-// ---------------------------------------------------------------------------
-// down_tc_kernel - the down projection of a decode chunk on the tcgen05 tensor
-// cores, all of the chunk's tokens in one pass. A CTA takes a 128-row tile of
-// W_down (rows 256-383 of the last tile read as zero past row 320) over one
-// 320-column slice of one stream: A = those weights, bf16 as stored, by TMA before
-// the dependency wait; B = the slice's activations R'·w_norm as three bf16 terms
-// side by side (rows term * T + t), as in up_mix_tc_kernel; D = 128 x N fp32 in
-// TMEM, 20 MMAs deep per term. The 8 slices of a stream form one thread-block
-// cluster: each CTA pushes its partial dots (its three term columns added, smallest
-// first) and its slice's sums of squares of R' into the CTA that finishes 16 of
-// the tile's rows, one cluster barrier publishes them, and that CTA sums the 8
-// slices in order and applies the stream's rs ("#2488 sycl/A770: faster hyper-
-// connection read on Arc A-series", Summary, change 4: the norm folded into the
-// down projection). Each stream's contribution rs_s * d_s goes to global memory
-// ([4 streams][8 tokens][320]); up_mix_tc_kernel adds the four in stream order as
-// it stages lo. R is read by the 3 row tiles only, not by every row block.
-// ---------------------------------------------------------------------------
-constexpr int kDtRows = 128;                          // W_down rows per CTA: MMA M
-constexpr int kDtRowTiles = (kRank + kDtRows - 1) / kDtRows;   // 3
-constexpr int kDtSliceCols = 320;                     // K per CTA
-constexpr int kDtSlices = kWidth / kDtSliceCols;      // 8 per stream: one cluster
-constexpr int kDtKBlocks = kDtSliceCols / kTcKB;      // 5
-constexpr int kDtThreads = 128;
-constexpr int kDtOwnRows = kDtRows / kDtSlices;       // 16 rows finished per CTA
-constexpr int kDtQuads = kDtSliceCols / 4;            // 80 column quads per token
-constexpr int kDtSmem = kDtKBlocks * kTcABytes + kDtKBlocks * kTcBBytesMax + 1024;
-
-template <int T>
-__global__ void __cluster_dims__(kDtSlices, 1, 1) __launch_bounds__(kDtThreads, 1)
-down_tc_kernel(const __grid_constant__ CUtensorMap tm_wd, const float* R, const float* P,
-               const uint16_t* __restrict__ w_norm, float* lo_parts, float eps, int* status) {
-    namespace cg = cooperative_groups;
-    extern __shared__ uint8_t smem_raw[];
-    // 1024-byte aligned: the 128-byte swizzle pattern repeats every 8 rows of 128 B
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int kN = kTcN<T>, kBBytes = kN * kTcKB * 2;
-    uint8_t* sA = smem;                                   // [K block][128 rows][128 B]
-    uint8_t* sB = smem + kDtKBlocks * kTcABytes;          // [K block][N rows][128 B]
-    __shared__ __align__(8) uint64_t w_full, mma_done;
-    __shared__ uint32_t tmem_slot;
-    __shared__ float ss_part[kDtThreads / 32][T];         // per warp: sums of squares of R'
-    __shared__ float inbox[kDtSlices][kDtOwnRows][T];     // pushed by each slice: partial dots
-    __shared__ float ss_in[kDtSlices][T];                 // pushed by each slice: its sums of squares
-    __shared__ int ok_s;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int sl = blockIdx.x;                            // slice == rank in the cluster
-    const int r0 = blockIdx.y * kDtRows;                  // first W_down row of the tile
-    const int s = blockIdx.z;                             // stream
-    const int k0 = s * kWidth + sl * kDtSliceCols;        // first column on the 10240 axis
-
-    if (tid == 0) {
-        tc::mbar_init(&w_full, 1);
-        tc::mbar_init(&mma_done, 1);
-        tc::fence_barrier_init();
-    }
-    if (warp == 0) tc::tmem_alloc(&tmem_slot, kTcTmemCols);
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = tmem_slot;
-
-    // 1. the tile's weights (layer parameters, read before the wait): one 128-row box
-    //    per K block; and this thread's w_norm quad
-    if (tid == 0) {
-        tc::mbar_arrive_expect_tx(&w_full, kDtKBlocks * kTcABytes);
-#pragma unroll
-        for (int kb = 0; kb < kDtKBlocks; ++kb)
-            tc::tma_load_2d(sA + kb * kTcABytes, &tm_wd, k0 + kb * kTcKB, r0, &w_full);
-    }
-    const bool stager = tid < kDtQuads;                   // thread tid stages column quad tid
-    uint2 wn = make_uint2(0u, 0u);
-    if (stager) wn = *reinterpret_cast<const uint2*>(w_norm + k0 + 4 * tid);
-    // first half of a cluster barrier: the wait before the pushes then finds every CTA
-    // of the cluster started (their shared memory exists)
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-    // the slice's activations into L2 while the previous kernel finishes
-    if (tid < 10 * T) {
-        const int t = tid / 10, line = tid % 10;
-        prefetch_l2(R + (size_t)t * kCols + k0 + line * 32);
-        if (P != nullptr) prefetch_l2(P + (size_t)t * kCols + k0 + line * 32);
-    }
-    pdl_launch_dependents();
-    pdl_wait();
-
-    // 2. R' of the slice, its sums of squares, and a = R' * w_norm as three bf16 terms
-    //    in the B tiles (K-major, 128-byte swizzled, rows term * T + t)
-    float4 x[T];
-    if (stager) {
-#pragma unroll
-        for (int t = 0; t < T; ++t) x[t] = *reinterpret_cast<const float4*>(R + (size_t)t * kCols + k0 + 4 * tid);
-        if (P != nullptr) {
-#pragma unroll
-            for (int t = 0; t < T; ++t) {
-                const float4 p = *reinterpret_cast<const float4*>(P + (size_t)t * kCols + k0 + 4 * tid);
-                x[t].x += p.x; x[t].y += p.y; x[t].z += p.z; x[t].w += p.w;
-            }
-        }
-    }
-    const float w0 = bf16_lo(wn.x), w1 = bf16_hi(wn.x), w2 = bf16_lo(wn.y), w3 = bf16_hi(wn.y);
-    const int kq = 4 * tid;                               // this thread's first column in the slice
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-        float ss = 0.f;
-        if (stager) {
-            ss = x[t].x * x[t].x;
-            ss = fmaf(x[t].y, x[t].y, ss);
-            ss = fmaf(x[t].z, x[t].z, ss);
-            ss = fmaf(x[t].w, x[t].w, ss);
-            uint32_t h0, m0, l0, h1, m1, l1;
-            split3_bf16(x[t].x * w0, x[t].y * w1, h0, m0, l0);
-            split3_bf16(x[t].z * w2, x[t].w * w3, h1, m1, l1);
-            uint8_t* b = sB + (kq / kTcKB) * kBBytes;
-            const int kin = kq % kTcKB;
-            *reinterpret_cast<uint2*>(b + tc::sw128_offset(t, kin)) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2*>(b + tc::sw128_offset(T + t, kin)) = make_uint2(m0, m1);
-            *reinterpret_cast<uint2*>(b + tc::sw128_offset(2 * T + t, kin)) = make_uint2(l0, l1);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) ss_part[warp][t] = ss;
-    }
-    tc::fence_proxy_async_smem();
-    __syncthreads();
-
-    // 3. the MMAs, issued by one thread once the weights have landed
-    if (tid == 0) {
-        bool ok = tc_wait(&w_full, 0, status);
-        if (!ok) ok = tc_wait(&w_full, 0, status);   // give the copies in flight one more limit
-        if (ok) {
-            tc::tc_fence_after();
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(kDtRows, kN);
-#pragma unroll
-            for (int kb = 0; kb < kDtKBlocks; ++kb)
-#pragma unroll
-                for (int kk = 0; kk < kTcKB / 16; ++kk)
-                    tc::mma_f16(tmem, tc::desc_sw128(tc::smem_u32(sA + kb * kTcABytes) + kk * 32),
-                                tc::desc_sw128(tc::smem_u32(sB + kb * kBBytes) + kk * 32), idesc,
-                                (kb | kk) != 0);
-            tc::mma_commit(&mma_done);
-        }
-        ok_s = ok;
-    }
-    __syncthreads();
-    const bool ok = ok_s && tc_wait(&mma_done, 0, status);
-
-    // 4. partial dots of this thread's row (TMEM lane = row of the tile), pushed with
-    //    the slice's sums of squares into the CTA that finishes the row
-    float d[T];
-#pragma unroll
-    for (int t = 0; t < T; ++t) d[t] = 0.f;
-    if (ok) {
-        tc::tc_fence_after();
-        float u[32];
-        tc::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16), u);
-#pragma unroll
-        for (int t = 0; t < T; ++t) d[t] = (u[2 * T + t] + u[T + t]) + u[t];
-    }
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-    cg::cluster_group cluster = cg::this_cluster();
-    {
-        const int rl = warp * 32 + lane;                   // row within the tile
-        float* dst = cluster.map_shared_rank(&inbox[sl][rl % kDtOwnRows][0], rl / kDtOwnRows);
-#pragma unroll
-        for (int t = 0; t < T; ++t) dst[t] = d[t];
-        if (tid < kDtSlices * T) {
-            const int q = tid % kDtSlices, t = tid / kDtSlices;
-            const float ss = (ss_part[0][t] + ss_part[1][t]) + (ss_part[2][t] + ss_part[3][t]);
-            *cluster.map_shared_rank(&ss_in[sl][t], q) = ss;
-        }
-    }
-    cluster.sync();
-
-    // 5. rows sl*16 .. sl*16+15 of the tile: the 8 slices summed in order, times the
-    //    stream's rs; this stream's part of lo
-    if (tid < kDtOwnRows * T) {
-        const int j = tid % kDtOwnRows, t = tid / kDtOwnRows;
-        const int row = r0 + sl * kDtOwnRows + j;
-        if (row < kRank) {
-            float v = inbox[0][j][t], ss = ss_in[0][t];
-#pragma unroll
-            for (int i = 1; i < kDtSlices; ++i) {
-                v += inbox[i][j][t];
-                ss += ss_in[i][t];
-            }
-            const float rs = inv_rms(fmaf(ss, 1.0f / (float)kWidth, eps));
-            lo_parts[(size_t)s * kLoPartStride + t * kRank + row] = rs * v;
-        }
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, kTcTmemCols);
-    }
-}
-
 // Launch with programmatic stream serialisation (see pdl_wait).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
@@ -810,25 +601,12 @@ cudaError_t allow_up_reserve(int device) {
     return allow_smem(up_mix_kernel<T>, kUpReserveT<T>, device, done);
 }
 
-template <int T, bool kParts>
+template <int T>
 cudaError_t allow_up_tc(int device) {
     static std::atomic<unsigned long long> done{0};
-    return allow_smem(up_mix_tc_kernel<T, kParts>, kTcSmem, device, done);
+    return allow_smem(up_mix_tc_kernel<T>, kTcSmem, device, done);
 }
 
-template <int T>
-cudaError_t allow_down_tc(int device) {
-    static std::atomic<unsigned long long> done{0};
-    return allow_smem(down_tc_kernel<T>, kDtSmem, device, done);
-}
-
-// Which down kernel a chunk of T tokens runs: the tcgen05 one (with the up kernel
-// adding its four stream parts of lo) or the CUDA-core one. The tcgen05 pair passes
-// the same parity tests but measured slower, µs per read with P: 6.06, 6.38, 6.81,
-// 7.44, 8.41, 9.23, 10.22, 10.73 for T = 1..8 (sweep 8.41) against 6.15, 6.14, 6.67,
-// 7.21, 7.94, 8.68, 9.63, 10.20 (sweep 7.99) with the CUDA-core down kernel: its
-// dots were not what grows with T.
-template <int T> constexpr bool kDownTcT = false;
 
 template <int T>
 cudaError_t launch_chunk(const Ctx& ctx, const ReadArgs& a, int t0, cudaStream_t st) {
@@ -838,32 +616,13 @@ cudaError_t launch_chunk(const Ctx& ctx, const ReadArgs& a, int t0, cudaStream_t
     float* lo = ctx.s.lo + (size_t)t0 * kRank;
     CUtensorMap tm_wu;
     if (kUpTcT<T> && !encode_w_up_bf16(&tm_wu, a.W_up, kTcCols)) return cudaErrorInvalidValue;
-    if constexpr (kDownTcT<T>) {
-        // the tcgen05 pair; lo holds the four stream parts of one chunk (the chunks of a
-        // call reuse it: a chunk's down kernel writes lo only after its wait, when the
-        // previous chunk's up kernel has finished)
-        static_assert(kUpTcT<T> || !kDownTcT<T>, "the tcgen05 down kernel feeds the tcgen05 up kernel");
-        float* parts = ctx.s.lo;
-        CUtensorMap tm_wd;
-        if (!encode_w_down_bf16(&tm_wd, a.W_down, kDtRows)) return cudaErrorInvalidValue;
-        cudaError_t e = allow_down_tc<T>(ctx.device);
-        if (e == cudaSuccess) e = allow_up_tc<T, true>(ctx.device);
-        if (e != cudaSuccess) return e;
-        e = launch_pdl(down_tc_kernel<T>, dim3(kDtSlices, kDtRowTiles, kStreams), dim3(kDtThreads),
-                       (size_t)kDtSmem, st, tm_wd, R, P, a.w_norm, parts, ctx.eps, ctx.s.status);
-        if (e != cudaSuccess) return e;
-        return launch_pdl(up_mix_tc_kernel<T, true>, dim3(kWidth / kTcCols), dim3(kTcThreads),
-                          (size_t)kTcSmem, st, tm_wu, R, P, (const float*)parts,
-                          a.Rmix + (size_t)t0 * 16, a.out_f32 + off, a.out_bf16 + off,
-                          a.out_fp16 + off, ctx.s.status);
-    }
-    cudaError_t e = kUpTcT<T> ? allow_up_tc<T, false>(ctx.device) : allow_up_reserve<T>(ctx.device);
+    cudaError_t e = kUpTcT<T> ? allow_up_tc<T>(ctx.device) : allow_up_reserve<T>(ctx.device);
     if (e != cudaSuccess) return e;
     e = launch_pdl(down_slice_kernel<T>, dim3(kDownSlices, kDownRowBlocks), dim3(kDownThreads), 0,
                    st, R, P, a.w_norm, a.W_down, lo, ctx.eps);
     if (e != cudaSuccess) return e;
     if (kUpTcT<T>)
-        return launch_pdl(up_mix_tc_kernel<T, false>, dim3(kWidth / kTcCols), dim3(kTcThreads),
+        return launch_pdl(up_mix_tc_kernel<T>, dim3(kWidth / kTcCols), dim3(kTcThreads),
                           (size_t)kTcSmem, st, tm_wu, R, P, (const float*)lo,
                           a.Rmix + (size_t)t0 * 16, a.out_f32 + off, a.out_bf16 + off,
                           a.out_fp16 + off, ctx.s.status);

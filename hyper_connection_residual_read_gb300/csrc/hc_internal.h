@@ -95,8 +95,6 @@ struct ReadArgs {
 // A TMA map over the caller's W_up [kCols][kRank] bf16, in boxes of 64 K x box_rows
 // rows with the 128-byte swizzle (the K-major layout of a tcgen05 operand).
 bool encode_w_up_bf16(CUtensorMap* map, const uint16_t* W_up, int box_rows);
-// The same over the caller's W_down [kRank][kCols] bf16 (rows past kRank read as zero).
-bool encode_w_down_bf16(CUtensorMap* map, const uint16_t* W_down, int box_rows);
 
 // Decode kernels for any T: launched in chunks of kDecodeMaxT tokens.
 cudaError_t launch_decode(const Ctx& ctx, const ReadArgs& a, cudaStream_t st);

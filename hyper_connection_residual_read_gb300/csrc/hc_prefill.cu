@@ -1158,14 +1158,6 @@ bool encode_w_up_bf16(CUtensorMap* map, const uint16_t* W_up, int box_rows) {
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-bool encode_w_down_bf16(CUtensorMap* map, const uint16_t* W_down, int box_rows) {
-    const cuuint64_t dims[2] = {kCols, kRank};
-    const cuuint64_t strides[1] = {kCols * 2};
-    const cuuint32_t box[2] = {kBK, (cuuint32_t)box_rows};
-    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W_down, 2, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
 cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, PrefillMode mode, cudaStream_t st) {
     cudaError_t e = launch_prefill_down(c, a, mode, st);
     if (e != cudaSuccess) return e;
