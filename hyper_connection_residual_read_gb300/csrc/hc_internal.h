@@ -112,7 +112,9 @@ cudaError_t launch_prefill(const Ctx& ctx, const ReadArgs& a, PrefillMode mode, 
 // The two halves of the tile path: weights to fp16, down GEMM and lo split; then the
 // up GEMM with its gate + mix epilogue (fused) or writing gated + the mix (unfused).
 cudaError_t launch_prefill_down(const Ctx& ctx, const ReadArgs& a, PrefillMode mode, cudaStream_t st);
+// pdl: launched with programmatic dependent launch right after lo_split (inside a
+// read); the stage run alone is an ordinary launch (its predecessor may write R).
 cudaError_t launch_prefill_upmix(const Ctx& ctx, const ReadArgs& a, PrefillMode mode,
-                                 cudaStream_t st);
+                                 cudaStream_t st, bool pdl = false);
 
 }  // namespace hc

@@ -515,6 +515,10 @@ __global__ void __launch_bounds__(kLoThreads)
 lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ssq,
                 __half* __restrict__ lo16, int T, int max_tokens, float eps,
                 int* __restrict__ status) {
+    // the up tile after it (launched with programmatic dependent launch inside a read)
+    // may start its prologue, R stream and weight loads now; it waits for this grid
+    // before it loads lo
+    pdl_launch_dependents();
     __shared__ float lo_s[kTileM][kLoCols + 1];
     __shared__ float rs_s[kStreams][kTileM];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -612,7 +616,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                   const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ EpiMaps em,
                   float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16,
                   uint16_t* __restrict__ out_fp16, int has_P, int T, int* __restrict__ status,
-                  int* __restrict__ sched) {
+                  int* __restrict__ sched, int pdl) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[kUpStages], empty_bar[kUpStages];
@@ -681,6 +685,9 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
             // outputs. R and the outputs keep the default policy: a 32-byte box row
             // shares its 128-byte line with the next three steps, which find it in L2.
             const uint64_t keep = l2_policy_evict_last();
+            // launched with programmatic dependent launch (inside a read, after lo_split):
+            // W_up and R were final before lo_split started, lo only once it has ended
+            bool lo_ready = !pdl;
             int it = 0;
             for (int i = 0; !abort_flag; ++i) {
                 // fetch the next tile and publish it to the other roles
@@ -696,13 +703,19 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
                     mbar_arrive_expect_tx(&full_bar[slot], kTerms * kTileBytes16 + kUpBBytes);
 #pragma unroll
-                    for (int term = 0; term < kTerms; ++term)
-                        tma_load_3d_hint(sA(slot, term), &tm_lo, kb * kBK, tt * kTileM, term,
-                                         &full_bar[slot], keep);
-#pragma unroll
                     for (int s = 0; s < kStreams; ++s)
                         tma_load_2d_hint(sB(slot) + s * (kUpBBytes / kStreams), &tm_wu, kb * kBK,
                                          s * kWidth + ct * kUpCols, &full_bar[slot], keep);
+                    if (!lo_ready) {
+                        pdl_wait();
+                        // lo was written by lo_split's ordinary stores; TMA reads it
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        lo_ready = true;
+                    }
+#pragma unroll
+                    for (int term = 0; term < kTerms; ++term)
+                        tma_load_3d_hint(sA(slot, term), &tm_lo, kb * kBK, tt * kTileM, term,
+                                         &full_bar[slot], keep);
                 }
             }
         }
@@ -1098,7 +1111,24 @@ cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, PrefillMode mod
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mode, cudaStream_t st) {
+// An up tile launch, with programmatic stream serialisation when `pdl`.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_up(void (*kernel)(KArgs...), int grid, bool pdl, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kUpThreads);
+    cfg.dynamicSmemBytes = kUpSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mode, cudaStream_t st,
+                                 bool pdl) {
     const int n_tt = (a.T + kTileM - 1) / kTileM;
     const int up_tiles = n_tt * kUpColTiles;
     const int up_grid = up_tiles < c.sm_count ? up_tiles : c.sm_count;
@@ -1114,9 +1144,10 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
     const int has_P = a.P != nullptr;
     switch (mode) {
         case PrefillMode::kFused:
-            upmix_tile_kernel<kOutMix, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
-                a.Rmix, c.tm_lo, c.tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16, has_P, a.T,
-                c.s.status, c.s.sched + 2 * kSchedUp);
+            if (cudaError_t e = launch_up(upmix_tile_kernel<kOutMix, 2>, up_grid, pdl, st, a.Rmix,
+                                          c.tm_lo, c.tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16,
+                                          has_P, a.T, c.s.status, c.s.sched + 2 * kSchedUp, (int)pdl))
+                return e;
             break;
         case PrefillMode::kFusedBf16Lo: {
             CUtensorMap tm_wu_bf16;   // over the caller's W_up [kCols][kRank] bf16
@@ -1126,20 +1157,26 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
             if (!encode_map(&tm_wu_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.W_up, 2, dims, strides,
                             box, CU_TENSOR_MAP_SWIZZLE_128B))
                 return cudaErrorInvalidValue;
-            upmix_tile_kernel<kOutMix, 1><<<up_grid, kUpThreads, kUpSmem, st>>>(
-                a.Rmix, c.tm_lo_bf16, tm_wu_bf16, em, a.out_f32, a.out_bf16, a.out_fp16, has_P,
-                a.T, c.s.status, c.s.sched + 2 * kSchedUp);
+            if (cudaError_t e = launch_up(upmix_tile_kernel<kOutMix, 1>, up_grid, pdl, st, a.Rmix,
+                                          c.tm_lo_bf16, tm_wu_bf16, em, a.out_f32, a.out_bf16,
+                                          a.out_fp16, has_P, a.T, c.s.status,
+                                          c.s.sched + 2 * kSchedUp, (int)pdl))
+                return e;
             break;
         }
         case PrefillMode::kReadoutY:
-            upmix_tile_kernel<kOutY, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
-                nullptr, c.tm_lo, c.tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16, has_P, a.T,
-                c.s.status, c.s.sched + 2 * kSchedUp);
+            if (cudaError_t e = launch_up(upmix_tile_kernel<kOutY, 2>, up_grid, pdl, st,
+                                          (const float*)nullptr, c.tm_lo, c.tm_wu, em, a.out_f32,
+                                          a.out_bf16, a.out_fp16, has_P, a.T, c.s.status,
+                                          c.s.sched + 2 * kSchedUp, (int)pdl))
+                return e;
             break;
         case PrefillMode::kUnfused: {
-            upmix_tile_kernel<kOutGated, 2><<<up_grid, kUpThreads, kUpSmem, st>>>(
-                a.Rmix, c.tm_lo, c.tm_wu, em, c.gated, nullptr, nullptr, has_P, a.T, c.s.status,
-                c.s.sched + 2 * kSchedUp);
+            if (cudaError_t e = launch_up(upmix_tile_kernel<kOutGated, 2>, up_grid, pdl, st, a.Rmix,
+                                          c.tm_lo, c.tm_wu, em, c.gated, (uint16_t*)nullptr,
+                                          (uint16_t*)nullptr, has_P, a.T, c.s.status,
+                                          c.s.sched + 2 * kSchedUp, (int)pdl))
+                return e;
             const int n = a.T * (kWidth / 4);
             const int mgrid = (n + 255) / 256 < 8 * c.sm_count ? (n + 255) / 256 : 8 * c.sm_count;
             mix_gated_kernel<<<mgrid, 256, 0, st>>>(c.gated, a.Rmix, a.out_f32, a.out_bf16,
@@ -1161,7 +1198,7 @@ bool encode_w_up_bf16(CUtensorMap* map, const uint16_t* W_up, int box_rows) {
 cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, PrefillMode mode, cudaStream_t st) {
     cudaError_t e = launch_prefill_down(c, a, mode, st);
     if (e != cudaSuccess) return e;
-    return launch_prefill_upmix(c, a, mode, st);
+    return launch_prefill_upmix(c, a, mode, st, true);
 }
 
 }  // namespace hc
