@@ -149,6 +149,9 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __global__ void convert_weights_kernel(const uint16_t* __restrict__ wd, const uint16_t* __restrict__ wu,
                                        __half* __restrict__ wd16, __half* __restrict__ wu16,
                                        int n8_each, bool down_only) {
+    // the down tile after it (launched with programmatic dependent launch) may start
+    // its prologue and R stream now; it waits for this grid before loading W_down
+    pdl_launch_dependents();
     const int n = down_only ? n8_each : 2 * n8_each;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const bool up = i >= n8_each;
@@ -183,7 +186,8 @@ __global__ void __launch_bounds__(kDownThreads, 1)
 down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                  const uint16_t* __restrict__ w_norm, const __grid_constant__ CUtensorMap tm_wd,
                  const __grid_constant__ CUtensorMap tm_r, float* __restrict__ partials,
-                 float* __restrict__ ssq, int T, int* __restrict__ status, int* __restrict__ sched) {
+                 float* __restrict__ ssq, int T, int* __restrict__ status, int* __restrict__ sched,
+                 int pdl) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[kDownStages], empty_bar[kDownStages];
@@ -243,6 +247,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             // the tile after the current one is fetched one tile early, so that its
             // first R blocks can be asked into L2 while the current tile is loaded
             int next = blockIdx.x;
+            bool wd_ready = !pdl;
             for (int i = 0; !abort_flag; ++i) {
                 if (!mbar_wait(&tq_empty[i % kDownTileQ], ((i / kDownTileQ) & 1) ^ 1, &abort_flag, status))
                     break;
@@ -261,10 +266,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     const int slot = it % kDownStages;
                     const uint32_t ph = (it / kDownStages) & 1;
                     if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
-                    mbar_arrive_expect_tx(&full_bar[slot], kDownBBytes);
-                    const int x = s * kWidth + kb * kBK;
-                    tma_load_2d(sB(slot), &tm_wd, x, 0, &full_bar[slot]);
-                    tma_load_2d(sB(slot) + kDownBBytes / 2, &tm_wd, x, kDownN / 2, &full_bar[slot]);
+                    // R (final before the read began) first; W_down's fp16 copy is written
+                    // by the conversion kernel before this one, so with programmatic
+                    // dependent launch it waits for that grid
                     if (full) {
                         mbar_arrive_expect_tx(&r_full[slot], 2 * kTileBytes16);
                         tma_load_5d(sA(slot, 0), &tm_r, kb * kBK, s, 0, 0, tt * 8, &r_full[slot]);
@@ -272,6 +276,15 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     } else {
                         mbar_arrive(&r_full[slot]);
                     }
+                    if (!wd_ready) {
+                        pdl_wait();
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        wd_ready = true;
+                    }
+                    mbar_arrive_expect_tx(&full_bar[slot], kDownBBytes);
+                    const int x = s * kWidth + kb * kBK;
+                    tma_load_2d(sB(slot), &tm_wd, x, 0, &full_bar[slot]);
+                    tma_load_2d(sB(slot) + kDownBBytes / 2, &tm_wd, x, kDownN / 2, &full_bar[slot]);
                     // R of the block kDownPrefetch stages ahead into L2: later in this
                     // tile, or at the start of the next one
                     const int pk = kb - kq * kDownKBlocksPerTile + kDownPrefetch;
@@ -1098,9 +1111,24 @@ cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, PrefillMode mod
     const int down_grid = down_tiles < c.sm_count ? down_tiles : c.sm_count;
     CUtensorMap tm_r;
     if (!encode_down_r(&tm_r, a.R, a.T)) return cudaErrorInvalidValue;
-    down_tile_kernel<<<down_grid, kDownThreads, kDownSmem, st>>>(
-        a.R, a.P, a.w_norm, c.tm_wd, tm_r, c.partials, c.ssq, a.T, c.s.status,
-        c.s.sched + 2 * kSchedDown);
+    {
+        // programmatic dependent launch after the conversion kernel: the prologue and
+        // the first R blocks overlap its end
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(down_grid);
+        cfg.blockDim = dim3(kDownThreads);
+        cfg.dynamicSmemBytes = kDownSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, down_tile_kernel, a.R, a.P, a.w_norm, c.tm_wd,
+                                           tm_r, c.partials, c.ssq, a.T, c.s.status,
+                                           c.s.sched + 2 * kSchedDown, 1);
+        if (e != cudaSuccess) return e;
+    }
     const int rgrid = ((a.T + kTileM - 1) / kTileM) * (kRank / kLoCols);
     if (mode == PrefillMode::kFusedBf16Lo)
         lo_split_kernel<true><<<rgrid, kLoThreads, 0, st>>>(c.partials, c.ssq, c.lo16, a.T,
