@@ -29,8 +29,9 @@
 //      all 4 up rows i = s*2560 + c of that column, an xor tree finishes the dots,
 //      then the gate and the 4x4 mix run in registers.
 //
-// Weights are loaded straight into registers with 16-byte streaming loads issued
-// before anything else, so a kernel's whole weight matrix is in flight at once.
+// Weights are requested before anything else, so a kernel's whole weight matrix is in
+// flight at once: the down kernel loads its slice straight into registers with
+// 16-byte streaming loads, the up kernel its 128 W_up rows into shared memory by TMA.
 //
 // Only the weight pointers carry __restrict__. A load through a const __restrict__
 // pointer may be treated as invariant and moved above griddepcontrol.wait; the
@@ -50,7 +51,7 @@ namespace {
 
 constexpr int kDownThreads = 320;   // 10 warps: 2 row groups x 5 column groups
 constexpr int kDownColGroups = 5;   // 5 x 256 columns = 1280
-// The up kernel: a warp owns 4 output columns. Chunks of up to 4 tokens use 128 CTAs
+// The CUDA-core up kernel (up_mix_kernel): a warp owns 4 output columns. Chunks of up to 4 tokens use 128 CTAs
 // of 5 warps and reserve enough shared memory that an SM holds at most one of them
 // (the down kernel of the same or the next read still fits beside it); chunks of 5-8
 // tokens use 160 CTAs of 4 warps with no reservation. Launched early by programmatic
