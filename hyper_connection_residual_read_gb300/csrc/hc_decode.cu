@@ -51,8 +51,9 @@ namespace {
 
 constexpr int kDownThreads = 320;   // 10 warps: 2 row groups x 5 column groups
 constexpr int kDownColGroups = 5;   // 5 x 256 columns = 1280
-// The CUDA-core up kernel (up_mix_kernel): a warp owns 4 output columns. Chunks of up to 4 tokens use 128 CTAs
-// of 5 warps and reserve enough shared memory that an SM holds at most one of them
+// The CUDA-core up kernel (up_mix_kernel): a warp owns 4 output columns. Chunks of
+// up to 4 tokens use 128 CTAs of 5 warps and reserve enough shared memory that an SM
+// holds at most one of them
 // (the down kernel of the same or the next read still fits beside it); chunks of 5-8
 // tokens use 160 CTAs of 4 warps with no reservation. Launched early by programmatic
 // dependent launch, up CTAs otherwise land up to four on one SM while others have
