@@ -256,6 +256,7 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     c.max_tokens = max_tokens;
     c.eps = eps > 0.f ? eps : 1e-6f;
     c.sm_count = prop.multiProcessorCount;
+    decode_forget_smem(device);
     strncpy(c.name, prop.name, sizeof(c.name) - 1);
     bool ok = true;
     ok &= cudaMalloc(&c.s.lo, sizeof(float) * (size_t)max_tokens * kRank) == cudaSuccess;

@@ -586,6 +586,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // every T, so that a token's bits do not depend on the other tokens of its call.
 template <int T> constexpr bool kUpTcT = true;
 
+// Devices (bits) on which each up kernel has been allowed its dynamic shared memory:
+// [0][T] the tcgen05 kernel, [1][T] the CUDA-core one. hc_read_init clears a device's
+// bits (decode_forget_smem), so the attributes are set again after a device reset.
+std::atomic<unsigned long long> g_smem_set[2][kDecodeMaxT + 1];
+
 // Allows `kernel` `bytes` of dynamic shared memory on this device, once per device.
 template <typename K>
 cudaError_t allow_smem(K kernel, int bytes, int device, std::atomic<unsigned long long>& done) {
@@ -599,14 +604,12 @@ cudaError_t allow_smem(K kernel, int bytes, int device, std::atomic<unsigned lon
 
 template <int T>
 cudaError_t allow_up_reserve(int device) {
-    static std::atomic<unsigned long long> done{0};
-    return allow_smem(up_mix_kernel<T>, kUpReserveT<T>, device, done);
+    return allow_smem(up_mix_kernel<T>, kUpReserveT<T>, device, g_smem_set[1][T]);
 }
 
 template <int T>
 cudaError_t allow_up_tc(int device) {
-    static std::atomic<unsigned long long> done{0};
-    return allow_smem(up_mix_tc_kernel<T>, kTcSmem, device, done);
+    return allow_smem(up_mix_tc_kernel<T>, kTcSmem, device, g_smem_set[0][T]);
 }
 
 
@@ -635,6 +638,12 @@ cudaError_t launch_chunk(const Ctx& ctx, const ReadArgs& a, int t0, cudaStream_t
 }
 
 }  // namespace
+
+void decode_forget_smem(int device) {
+    if (device < 0 || device >= 64) return;
+    for (auto& row : g_smem_set)
+        for (auto& bits : row) bits.fetch_and(~(1ull << device), std::memory_order_acq_rel);
+}
 
 cudaError_t launch_decode(const Ctx& ctx, const ReadArgs& a, cudaStream_t st) {
     for (int t0 = 0; t0 < a.T; t0 += kDecodeMaxT) {
