@@ -87,7 +87,8 @@ enum hc_status {
  * (tests, bench). */
 enum hc_path {
     HC_PATH_AUTO = 0,
-    HC_PATH_DECODE = 1,            /* per 8 tokens: sliced down kernel, then up/gate/mix kernel */
+    HC_PATH_DECODE = 1,            /* per 8 tokens: sliced down kernel (CUDA cores, clusters),
+                                      then the up + gate + mix kernel (tcgen05) */
     HC_PATH_PREFILL = 2,           /* tile down, fused up + gate + mix epilogue */
     HC_PATH_PREFILL_UNFUSED = 3,   /* tile down, up GEMM writing gated, then the mix */
     HC_PATH_DECODE_ONE_KERNEL = 4, /* per 8 tokens: one kernel with an in-kernel lo exchange
@@ -218,7 +219,8 @@ void hc_read_shutdown(void);
  * pointer errors hc_read refuses, HC_ERR_ARCH off sm_103, HC_ERR_CUDA otherwise.
  *
  * The first call on a device (with that device current) looks up the array's
- * device address; make that first call before any stream capture. Every call
+ * device address and sets the decode kernels' shared-memory attributes for each
+ * token count it meets; make those first calls before any stream capture. Every call
  * on a device shares the one array: calls that may overlap on the GPU (on
  * different streams without ordering between them) race and must not be made. */
 int hc_read_noalloc(int tokens,
