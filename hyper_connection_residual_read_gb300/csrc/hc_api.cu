@@ -256,7 +256,6 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     c.max_tokens = max_tokens;
     c.eps = eps > 0.f ? eps : 1e-6f;
     c.sm_count = prop.multiProcessorCount;
-    decode_forget_smem(device);
     strncpy(c.name, prop.name, sizeof(c.name) - 1);
     bool ok = true;
     ok &= cudaMalloc(&c.s.lo, sizeof(float) * (size_t)max_tokens * kRank) == cudaSuccess;
@@ -277,6 +276,7 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     if (cudaMemset(c.s.status, 0, sizeof(int)) != cudaSuccess ||
         cudaMemset(c.s.sync, 0, 2 * sizeof(unsigned)) != cudaSuccess ||
         cudaMemset(c.s.sched, 0, 2 * kSchedPairs * sizeof(int)) != cudaSuccess ||
+        decode_setup(device) != cudaSuccess ||
         decode_fused_setup(&c.fused_decode) != cudaSuccess ||
         cudaMemset(c.lo16, 0, sizeof(__half) * 2 * (size_t)max_tokens * kRank) != cudaSuccess ||
         prefill_setup(c) != cudaSuccess ||

@@ -645,6 +645,26 @@ void decode_forget_smem(int device) {
         for (auto& bits : row) bits.fetch_and(~(1ull << device), std::memory_order_acq_rel);
 }
 
+namespace {
+template <int T>
+cudaError_t allow_chunk(int device) {
+    return kUpTcT<T> ? allow_up_tc<T>(device) : allow_up_reserve<T>(device);
+}
+}  // namespace
+
+cudaError_t decode_setup(int device) {
+    decode_forget_smem(device);
+    cudaError_t e = allow_chunk<1>(device);
+    if (e == cudaSuccess) e = allow_chunk<2>(device);
+    if (e == cudaSuccess) e = allow_chunk<3>(device);
+    if (e == cudaSuccess) e = allow_chunk<4>(device);
+    if (e == cudaSuccess) e = allow_chunk<5>(device);
+    if (e == cudaSuccess) e = allow_chunk<6>(device);
+    if (e == cudaSuccess) e = allow_chunk<7>(device);
+    if (e == cudaSuccess) e = allow_chunk<8>(device);
+    return e;
+}
+
 cudaError_t launch_decode(const Ctx& ctx, const ReadArgs& a, cudaStream_t st) {
     for (int t0 = 0; t0 < a.T; t0 += kDecodeMaxT) {
         const int n = a.T - t0 < kDecodeMaxT ? a.T - t0 : kDecodeMaxT;

@@ -96,9 +96,12 @@ struct ReadArgs {
 // rows with the 128-byte swizzle (the K-major layout of a tcgen05 operand).
 bool encode_w_up_bf16(CUtensorMap* map, const uint16_t* W_up, int box_rows);
 
-// Forgets which decode kernels were allowed their shared memory on `device` (called by
-// hc_read_init, so that the attributes are set again after a device reset).
+// Forgets which decode kernels were allowed their shared memory on `device`, then
+// sets those attributes for every chunk size, so that no launch inside a stream
+// capture needs to (hc_read_init calls it; the attributes also survive a device
+// reset that is followed by a new hc_read_init).
 void decode_forget_smem(int device);
+cudaError_t decode_setup(int device);
 
 // Decode kernels for any T: launched in chunks of kDecodeMaxT tokens.
 cudaError_t launch_decode(const Ctx& ctx, const ReadArgs& a, cudaStream_t st);
