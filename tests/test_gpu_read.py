@@ -437,6 +437,33 @@ def test_back_to_back_tile_reads_do_not_see_each_others_scratch(weights):
             assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
 
 
+@pytest.mark.parametrize("T", [3, 300])
+def test_reads_captured_in_a_cuda_graph(weights, T):
+    """A read captured in a CUDA graph (how a serving step calls it) and replayed gives
+    the bits of the same read called directly: the launch needs no host work that a
+    capture cannot hold, decode (T = 3) and tile path (T = 300) alike."""
+    w, W = weights
+    a = synth.make_activations(77 + T, T, True)
+    R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+    ref = gpu_read(T, R, P, W, M)
+    o = _poisoned_out(T)
+    st = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        hc.hc_read(T, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o, stream=st)
+        st.synchronize()
+        with torch.cuda.graph(g, stream=st):
+            hc.hc_read(T, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o, stream=st)
+    for _ in range(2):
+        for x in o:
+            x.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        for x, y in zip(ref, _host(o)):
+            assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    assert hc.hc_read_status() == 0
+
+
 def _poisoned_out(T):
     """Output tensors filled with NaN / all-ones bits, so a value that no kernel wrote
     cannot pass for a correct one left over from an earlier run."""
