@@ -8,7 +8,8 @@
 * invariants: pending write == pre-added residual, token independence, stream
   permutation equivariance, exact power-of-two scaling with eps = 0;
 * textbook routines from another library: torch's ``rms_norm``, float64 matmul,
-  ``sigmoid`` and ``einsum``; the converters against torch's casts.
+  ``sigmoid`` and ``einsum``; the converters against torch's casts (the bf16
+  encoder on all 2^32 fp32 patterns, the bf16 decoder on all 2^16).
 
 A final test plants mistakes in the oracle (transposed operands, a flipped sign,
 a dropped factor, eps outside the root, the mix read the wrong way round) and
@@ -331,6 +332,35 @@ def test_bf16_encoder_against_torch():
     assert np.array_equal(mine[~nan], ref[~nan])
     back = O.bf16_bits_to_f64(mine[nan])
     assert np.all(np.isnan(back))
+
+
+def test_bf16_encoder_exhaustive():
+    """All 2^32 fp32 bit patterns through the oracle's bf16 encoder, against
+    torch's cast, in blocks of 2^24 over a spawn pool (about half a minute on
+    eight cores)."""
+    import multiprocessing as mp
+
+    import _converter_sweep as S
+
+    blocks = range(1 << (32 - S.BLOCK_BITS))
+    workers = max(1, min(16, os.cpu_count() or 1))
+    with mp.get_context("spawn").Pool(workers) as pool:
+        results = pool.map(S.check_block, blocks, chunksize=1)
+    bad = [(k, n, hex(first)) for k, n, first in results if n]
+    assert len(results) == len(blocks) and not bad, bad[:4]
+
+
+def test_bf16_decoder_exhaustive():
+    """All 2^16 bf16 bit patterns through the oracle's decoder, against torch's
+    bfloat16 -> float64 cast (NaNs compared as NaNs)."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):   # signalling NaNs quieted by the widening
+        mine = O.bf16_bits_to_f64(bits)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(mine[~nan]), np.signbit(ref[~nan]))
 
 
 def test_fp16_encoder_against_torch():
