@@ -22,6 +22,7 @@ HC_ERR_CUDA = -4
 HC_ERR_TIMEOUT = -5
 HC_ERR_CHECK = -6
 HC_ERR_NOMEM = -7
+HC_ERR_RANGE = -8
 
 HC_PATH_AUTO = 0
 HC_PATH_DECODE = 1

@@ -37,9 +37,23 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_strerror(lib):
     assert hc.hc_read_version() == 100
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         assert hc.strerror(code) != "unknown status"
     assert hc.strerror(-99) == "unknown status"
+
+
+def test_binding_constants_match_the_header():
+    """Every enumerator and size macro of include/hc_read.h has the same value in
+    the binding (parsed from the header text, so a renumbering on either side fails)."""
+    from hyper_connection_residual_read_gb300 import _lib
+    text = open(os.path.join(ROOT, "include", "hc_read.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    enums = dict((k, int(v)) for k, v in re.findall(r"\b(HC_(?:OK|ERR_\w+|PATH_\w+))\s*=\s*(-?\d+)", text))
+    assert len(enums) == 15, sorted(enums)
+    for name, value in enums.items():
+        assert getattr(_lib, name) == value, name
+    macros = dict((k, int(v)) for k, v in re.findall(r"#define\s+HC_READ_(\w+)\s+(\d+)", text))
+    assert (macros["STREAMS"], macros["WIDTH"], macros["RANK"]) == (_lib.STREAMS, _lib.WIDTH, _lib.RANK)
 
 
 def test_calls_without_a_device_fail_cleanly(lib):
