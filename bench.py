@@ -41,11 +41,16 @@ N_SETS = 48
 EPS = float(np.float32(1e-6))
 
 # DRAM bytes (read + write) that ncu counted for one 4-token read with a pending
-# write, both decode kernels together (down_slice_kernel<4> 6,918,707 B,
+# write, both decode kernels together, on the current kernels; None when the
+# kernels changed after the last capture. The sweep's traffic is taken as its
+# algorithmic bytes times the ratio of this figure to the same read's algorithmic
+# bytes. The last capture (13,829,222 B: down_slice_kernel<4> 6,918,707 B,
 # up_mix_tc_kernel<4> 6,910,515 B; 48 rotated weight sets, so the weights come from
-# DRAM). The sweep's traffic is taken as its algorithmic bytes times the ratio of
-# this figure to the same read's algorithmic bytes.
-NCU_TRAFFIC_T4_P = 13829222
+# DRAM) predates the down kernel's one-pass sum-of-squares reduction, a change of
+# shuffles only.
+NCU_TRAFFIC_T4_P = None
+NCU_TRAFFIC_LAST = "13,829,222 B per T=4 read with P (13,783,296 algorithmic), before the " \
+                   "down kernel's one-pass sum-of-squares reduction"
 
 
 def read_bytes(T: int, with_P: bool) -> int:
@@ -582,7 +587,8 @@ def gpu_arm(args) -> None:
     del Rc, Mc, Pc
 
     achieved = step_bytes / (ms / args.steps * 1e-3) / 1e9
-    traffic = step_bytes * NCU_TRAFFIC_T4_P / read_bytes(4, True)
+    traffic = (None if NCU_TRAFFIC_T4_P is None
+               else step_bytes * NCU_TRAFFIC_T4_P / read_bytes(4, True))
     kernel_launches_per_step = sum(2 * ((T + 7) // 8) for T, _ in SWEEP)
 
     line = {
@@ -593,8 +599,10 @@ def gpu_arm(args) -> None:
         "roofline": {"bound": "hbm", "kernel": "decode read (down_slice + up_mix_tc kernels)",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "traffic_basis": "ncu DRAM bytes of one T=4 read with P, scaled to the "
-                                      "sweep by algorithmic bytes",
+                     "traffic_basis": ("ncu DRAM bytes of one T=4 read with P, scaled to the "
+                                       "sweep by algorithmic bytes" if traffic is not None else
+                                       "null: the kernels changed after the last ncu capture; "
+                                       "that capture: " + NCU_TRAFFIC_LAST),
                      "peak_source": peaks["source"],
                      "bytes_per_step": step_bytes},
         "clocks": clocks,
