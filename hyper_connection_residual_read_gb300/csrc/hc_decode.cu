@@ -24,14 +24,13 @@
 //      the up projection, writing mixed with its BF16 / FP16 images). The launcher
 //      uses it for every T.
 //
-//  up_mix_kernel - the same step on CUDA cores, not launched by default: a warp
-//      owns 4 output columns; 8 lanes per column each sum 40 of the 320 inputs for
-//      all 4 up rows i = s*2560 + c of that column, an xor tree finishes the dots,
-//      then the gate and the 4x4 mix run in registers.
-//
 // Weights are requested before anything else, so a kernel's whole weight matrix is in
 // flight at once: the down kernel loads its slice straight into registers with
 // 16-byte streaming loads, the up kernel its 128 W_up rows into shared memory by TMA.
+//
+// A CUDA-core up kernel (a warp per 4 output columns, 8 lanes per column, an xor
+// tree for the dots) came before the tcgen05 one; its measured times are given at
+// the launcher below.
 //
 // Only the weight pointers carry __restrict__. A load through a const __restrict__
 // pointer may be treated as invariant and moved above griddepcontrol.wait; the
@@ -51,17 +50,6 @@ namespace {
 
 constexpr int kDownThreads = 320;   // 10 warps: 2 row groups x 5 column groups
 constexpr int kDownColGroups = 5;   // 5 x 256 columns = 1280
-// The CUDA-core up kernel (up_mix_kernel): a warp owns 4 output columns. Chunks of
-// up to 4 tokens use 128 CTAs of 5 warps and reserve enough shared memory that an SM
-// holds at most one of them
-// (the down kernel of the same or the next read still fits beside it); chunks of 5-8
-// tokens use 160 CTAs of 4 warps with no reservation. Launched early by programmatic
-// dependent launch, up CTAs otherwise land up to four on one SM while others have
-// none. Measured: T = 1 6.10 -> 5.00 us per read, T = 2-4 0.2-0.6 us faster; at
-// T = 5-8 one CTA per SM did not pay.
-template <int T> constexpr int kUpWarpsT = T <= 4 ? 5 : 4;
-template <int T> constexpr int kUpThreadsT = 32 * kUpWarpsT<T>;
-template <int T> constexpr int kUpReserveT = T <= 4 ? 120 * 1024 : 0;   // dynamic shared bytes
 
 // Sum over the 32 lanes of eight per-lane values, one per row. On return the
 // lanes whose bits (4,3,2) equal the row's index hold that row's full sum:
@@ -244,140 +232,6 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
             v = fmaf(rs, d, v);
         }
         lo[t * kRank + rb * kDownRowsPerCta + 2 * sl + jj] = v;
-    }
-}
-
-// lo in shared memory: each token's 320 values as 8 parts of 40, padded to 44
-// floats so that the 8 parts a warp reads at once fall in distinct banks.
-constexpr int kLoPart = 44;
-
-template <int T>
-__global__ void __launch_bounds__(kUpThreadsT<T>)
-up_mix_kernel(const float* R, const float* P, const uint16_t* __restrict__ W_up,
-              const float* lo, const float* Rmix, float* out_f32, uint16_t* out_bf16,
-              uint16_t* out_fp16) {
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int cc = lane >> 3;                  // which of the warp's 4 columns
-    const int part = lane & 7;                 // which 40 of the 320 inputs
-    const int c = (blockIdx.x * kUpWarpsT<T> + warp) * 4 + cc;   // output column 0..2559
-    const int sp = part & 3;                   // stream gated by this lane (lanes 0..3)
-
-    // 1. the 4 up rows of column c (one per stream), this lane's 40 inputs each
-    uint4 wv[kStreams][5];
-#pragma unroll
-    for (int st = 0; st < kStreams; ++st) {
-        const uint16_t* wrow = W_up + (size_t)(st * kWidth + c) * kRank + part * 40;
-#pragma unroll
-        for (int q = 0; q < 5; ++q) wv[st][q] = ldg_stream_v4(wrow + 8 * q);
-    }
-    // this lane's residual (and pending write) into L2 while the down kernel runs
-    if (part < 4) {
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-            prefetch_l2(R + (size_t)t * kCols + sp * kWidth + c);
-            if (P != nullptr) prefetch_l2(P + (size_t)t * kCols + sp * kWidth + c);
-        }
-    }
-    pdl_launch_dependents();
-    pdl_wait();
-
-    // 2. everything the token loop needs, requested at once: lo, R' and the mix
-    __shared__ __align__(16) float lo_s[T][8][kLoPart];
-    __shared__ __align__(16) float m_s[T][16];
-    float rp[T];
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-        const size_t off = (size_t)t * kCols + sp * kWidth + c;
-        rp[t] = R[off];
-    }
-    if (P != nullptr) {
-#pragma unroll
-        for (int t = 0; t < T; ++t) rp[t] += P[(size_t)t * kCols + sp * kWidth + c];
-    }
-    // lo of the chunk ([T][320], contiguous): every load is issued before the first
-    // store, so the staging costs one round trip whatever T is
-    constexpr int kLoVec = T * kRank / 4;
-    constexpr int kLoIter = (kLoVec + kUpThreadsT<T> - 1) / kUpThreadsT<T>;
-    float4 lv[kLoIter];
-#pragma unroll
-    for (int i = 0; i < kLoIter; ++i) {
-        const int e = tid + i * kUpThreadsT<T>;
-        if (e < kLoVec) lv[i] = reinterpret_cast<const float4*>(lo)[e];
-    }
-#pragma unroll
-    for (int i = 0; i < kLoIter; ++i) {
-        const int e = tid + i * kUpThreadsT<T>;
-        if (e < kLoVec) {
-            const int t = e / (kRank / 4), j = 4 * (e % (kRank / 4));
-            *reinterpret_cast<float4*>(&lo_s[t][j / 40][j % 40]) = lv[i];
-        }
-    }
-    if (tid < T * 4) reinterpret_cast<float4*>(&m_s[0][0])[tid] =
-        reinterpret_cast<const float4*>(Rmix)[tid];
-    __syncthreads();
-
-    // tokens in pairs: each weight is unpacked from bf16 once and feeds both tokens
-    // (every token's dot keeps the same order of fused multiply-adds)
-#pragma unroll
-    for (int t0 = 0; t0 < T; t0 += 2) {
-        constexpr int kMax = 2;
-        const int nt = t0 + 1 < T ? 2 : 1;   // a compile-time constant once unrolled
-        float acc[kMax][kStreams] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int q = 0; q < 5; ++q) {
-            float x[kMax][8];
-#pragma unroll
-            for (int i = 0; i < kMax; ++i) {
-                if (i < nt) {
-                    const float4* l4 = reinterpret_cast<const float4*>(&lo_s[t0 + i][part][0]);
-                    const float4 xa = l4[2 * q], xb = l4[2 * q + 1];
-                    x[i][0] = xa.x; x[i][1] = xa.y; x[i][2] = xa.z; x[i][3] = xa.w;
-                    x[i][4] = xb.x; x[i][5] = xb.y; x[i][6] = xb.z; x[i][7] = xb.w;
-                }
-            }
-#pragma unroll
-            for (int st = 0; st < kStreams; ++st) {
-                const uint4 w = wv[st][q];
-                const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                                    bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
-#pragma unroll
-                for (int i = 0; i < kMax; ++i) {
-                    if (i < nt) {
-                        float v = acc[i][st];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v = fmaf(f[e], x[i][e], v);
-                        acc[i][st] = v;
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kMax; ++i) {
-            if (i >= nt) continue;
-            const int t = t0 + i;
-#pragma unroll
-            for (int st = 0; st < kStreams; ++st) {
-                acc[i][st] += __shfl_xor_sync(0xffffffffu, acc[i][st], 4);
-                acc[i][st] += __shfl_xor_sync(0xffffffffu, acc[i][st], 2);
-                acc[i][st] += __shfl_xor_sync(0xffffffffu, acc[i][st], 1);
-            }
-            // lane `part` (0..3) of the column group gates stream `part`
-            const float u = sp == 0 ? acc[i][0] : sp == 1 ? acc[i][1] : sp == 2 ? acc[i][2] : acc[i][3];
-            const float g = gate_value(u, rp[t]);
-            const int base = lane & ~7;
-            const float g0 = __shfl_sync(0xffffffffu, g, base + 0);
-            const float g1 = __shfl_sync(0xffffffffu, g, base + 1);
-            const float g2 = __shfl_sync(0xffffffffu, g, base + 2);
-            const float g3 = __shfl_sync(0xffffffffu, g, base + 3);
-            if (part < 4) {
-                const float m = mix_row(&m_s[t][part * 4], g0, g1, g2, g3);
-                const size_t off = (size_t)t * kCols + part * kWidth + c;
-                out_f32[off] = m;
-                out_bf16[off] = to_bf16_bits(m);
-                out_fp16[off] = to_fp16_bits(m);
-            }
-        }
     }
 }
 
@@ -588,16 +442,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Which up kernel a chunk of T tokens runs. Measured, µs per read with P: the
-// tcgen05 kernel 6.13, 6.14, 6.67, 7.21, 7.94, 8.68, 9.63, 10.20 for T = 1..8; the
-// CUDA-core kernel 5.0, 6.1, 7.1, 7.9, 8.8, 9.7, 10.8, 12.2. The tcgen05 kernel runs
-// every T, so that a token's bits do not depend on the other tokens of its call.
-template <int T> constexpr bool kUpTcT = true;
+// The up kernel of every chunk is the tcgen05 one. Measured, µs per read with P, for
+// T = 1..8: 6.13, 6.14, 6.67, 7.21, 7.94, 8.68, 9.63, 10.20, against 5.0, 6.1, 7.1,
+// 7.9, 8.8, 9.7, 10.8, 12.2 with the CUDA-core up kernel it replaced. One kernel for
+// every T keeps a token's bits independent of the other tokens of its call.
 
-// Devices (bits) on which each up kernel has been allowed its dynamic shared memory:
-// [0][T] the tcgen05 kernel, [1][T] the CUDA-core one. hc_read_init clears a device's
-// bits (decode_forget_smem), so the attributes are set again after a device reset.
-std::atomic<unsigned long long> g_smem_set[2][kDecodeMaxT + 1];
+// Devices (bits) on which up_mix_tc_kernel<T> has been allowed its dynamic shared
+// memory. hc_read_init clears a device's bits (decode_forget_smem), so the attribute
+// is set again after a device reset.
+std::atomic<unsigned long long> g_smem_set[kDecodeMaxT + 1];
 
 // Allows `kernel` `bytes` of dynamic shared memory on this device, once per device.
 template <typename K>
@@ -611,13 +464,8 @@ cudaError_t allow_smem(K kernel, int bytes, int device, std::atomic<unsigned lon
 }
 
 template <int T>
-cudaError_t allow_up_reserve(int device) {
-    return allow_smem(up_mix_kernel<T>, kUpReserveT<T>, device, g_smem_set[1][T]);
-}
-
-template <int T>
 cudaError_t allow_up_tc(int device) {
-    return allow_smem(up_mix_tc_kernel<T>, kTcSmem, device, g_smem_set[0][T]);
+    return allow_smem(up_mix_tc_kernel<T>, kTcSmem, device, g_smem_set[T]);
 }
 
 
@@ -628,35 +476,29 @@ cudaError_t launch_chunk(const Ctx& ctx, const ReadArgs& a, int t0, cudaStream_t
     const float* P = a.P ? a.P + off : nullptr;
     float* lo = ctx.s.lo + (size_t)t0 * kRank;
     CUtensorMap tm_wu;
-    if (kUpTcT<T> && !encode_w_up_bf16(&tm_wu, a.W_up, kTcCols)) return cudaErrorInvalidValue;
-    cudaError_t e = kUpTcT<T> ? allow_up_tc<T>(ctx.device) : allow_up_reserve<T>(ctx.device);
+    if (!encode_w_up_bf16(&tm_wu, a.W_up, kTcCols)) return cudaErrorInvalidValue;
+    cudaError_t e = allow_up_tc<T>(ctx.device);
     if (e != cudaSuccess) return e;
     e = launch_pdl(down_slice_kernel<T>, dim3(kDownSlices, kDownRowBlocks), dim3(kDownThreads), 0,
                    st, R, P, a.w_norm, a.W_down, lo, ctx.eps);
     if (e != cudaSuccess) return e;
-    if (kUpTcT<T>)
-        return launch_pdl(up_mix_tc_kernel<T>, dim3(kWidth / kTcCols), dim3(kTcThreads),
-                          (size_t)kTcSmem, st, tm_wu, R, P, (const float*)lo,
-                          a.Rmix + (size_t)t0 * 16, a.out_f32 + off, a.out_bf16 + off,
-                          a.out_fp16 + off, ctx.s.status);
-    return launch_pdl(up_mix_kernel<T>, dim3(kWidth / (4 * kUpWarpsT<T>)), dim3(kUpThreadsT<T>),
-                      (size_t)kUpReserveT<T>, st, R, P, a.W_up, (const float*)lo,
+    return launch_pdl(up_mix_tc_kernel<T>, dim3(kWidth / kTcCols), dim3(kTcThreads),
+                      (size_t)kTcSmem, st, tm_wu, R, P, (const float*)lo,
                       a.Rmix + (size_t)t0 * 16, a.out_f32 + off, a.out_bf16 + off,
-                      a.out_fp16 + off);
+                      a.out_fp16 + off, ctx.s.status);
 }
 
 }  // namespace
 
 void decode_forget_smem(int device) {
     if (device < 0 || device >= 64) return;
-    for (auto& row : g_smem_set)
-        for (auto& bits : row) bits.fetch_and(~(1ull << device), std::memory_order_acq_rel);
+    for (auto& bits : g_smem_set) bits.fetch_and(~(1ull << device), std::memory_order_acq_rel);
 }
 
 namespace {
 template <int T>
 cudaError_t allow_chunk(int device) {
-    return kUpTcT<T> ? allow_up_tc<T>(device) : allow_up_reserve<T>(device);
+    return allow_up_tc<T>(device);
 }
 }  // namespace
 
