@@ -13,7 +13,9 @@
 
 A final test plants mistakes in the oracle (transposed operands, a flipped sign,
 a dropped factor, eps outside the root, the mix read the wrong way round) and
-checks that the brute-force pin catches every one.
+checks that the brute-force pin catches every one; another plants four in the
+bf16 encoder (truncation, ties away from zero, the wrong parity bit, NaN carried
+into infinity) and checks that the converter pin catches them.
 """
 import json
 import math
@@ -323,15 +325,50 @@ def _stratified_f32_bits():
     return np.concatenate([hi | np.uint32(lo) for lo in lows])
 
 
-def test_bf16_encoder_against_torch():
+def _bf16_encoder_mismatches(encode) -> int:
+    """Stratified fp32 patterns on which ``encode`` differs from torch's cast
+    (NaN inputs must give a NaN)."""
     bits = _stratified_f32_bits()
     x = bits.view(F32)
-    mine = O.f32_to_bf16_bits(x)
+    mine = encode(x)
     ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     nan = np.isnan(x)
-    assert np.array_equal(mine[~nan], ref[~nan])
-    back = O.bf16_bits_to_f64(mine[nan])
-    assert np.all(np.isnan(back))
+    bad = int(np.count_nonzero(mine[~nan] != ref[~nan]))
+    with np.errstate(invalid="ignore"):
+        bad += int(np.count_nonzero(~np.isnan(O.bf16_bits_to_f64(mine[nan]))))
+    return bad
+
+
+def test_bf16_encoder_against_torch():
+    assert _bf16_encoder_mismatches(O.f32_to_bf16_bits) == 0
+
+
+def _bf16_encoder_mutants():
+    def u32(x):
+        return np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+
+    def truncate(x):             # no rounding at all
+        return (u32(x) >> np.uint64(16)).astype(np.uint16)
+
+    def ties_away(x):            # half-way cases rounded away from zero
+        return ((u32(x) + np.uint64(0x8000)) >> np.uint64(16)).astype(np.uint16)
+
+    def ties_odd_lsb(x):         # the kept bit's parity read from the wrong place
+        u = u32(x)
+        return ((u + np.uint64(0x7FFF) + ((u >> np.uint64(15)) & np.uint64(1))) >> np.uint64(16)).astype(np.uint16)
+
+    def nan_to_inf(x):           # rounding carries a NaN with a low payload into infinity
+        u = u32(x)
+        return ((u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)).astype(np.uint16)
+
+    return {"truncate": truncate, "ties_away": ties_away, "ties_odd_lsb": ties_odd_lsb,
+            "nan_to_inf": nan_to_inf}
+
+
+@pytest.mark.parametrize("name", list(_bf16_encoder_mutants().keys()))
+def test_bf16_encoder_mistakes_are_caught(name):
+    """The converter pin fails on plausible encoder mistakes."""
+    assert _bf16_encoder_mismatches(_bf16_encoder_mutants()[name]) > 0
 
 
 def test_bf16_encoder_exhaustive():
