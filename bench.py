@@ -44,13 +44,11 @@ EPS = float(np.float32(1e-6))
 # write, both decode kernels together, on the current kernels; None when the
 # kernels changed after the last capture. The sweep's traffic is taken as its
 # algorithmic bytes times the ratio of this figure to the same read's algorithmic
-# bytes. The last capture (13,829,222 B: down_slice_kernel<4> 6,918,707 B,
-# up_mix_tc_kernel<4> 6,910,515 B; 48 rotated weight sets, so the weights come from
-# DRAM) predates the down kernel's one-pass sum-of-squares reduction, a change of
-# shuffles only.
-NCU_TRAFFIC_T4_P = None
-NCU_TRAFFIC_LAST = "13,829,222 B per T=4 read with P (13,783,296 algorithmic), before the " \
-                   "down kernel's one-pass sum-of-squares reduction"
+# bytes. Capture (two reads, 48 rotated weight sets, so the weights come from DRAM):
+# down_slice_kernel<4> 6,918,912 B, up_mix_tc_kernel<4> 6,910,336 B, both reads,
+# nothing written back to DRAM (the outputs stay in L2).
+NCU_TRAFFIC_T4_P = 13_829_248
+NCU_TRAFFIC_LAST = "13,829,248 B per T=4 read with P (13,783,296 algorithmic)"
 
 
 def read_bytes(T: int, with_P: bool) -> int:

@@ -530,3 +530,33 @@ def test_readout_y_is_the_mix_with_a_row_of_ones():
     # and it is the plain sum of the gated streams of the staged read
     st = O.hc_read(R, P, w_norm, W_down, W_up, ones, 1e-6, stages=True)
     assert np.allclose(O.readout_y(st["gated"]), st["gated"].sum(axis=1), rtol=1e-15, atol=0)
+
+
+def test_read_tokens_is_the_read_of_those_rows():
+    """hc_read_tokens (the checker of long chunks on sampled tokens) returns rows
+    ``idx`` of the whole read, for unsorted and repeated indices, with and without
+    the pending write: within float64 rounding of the batched matrix products, and
+    bitwise for the images wherever the fp32 values agree bitwise."""
+    rng = np.random.default_rng(79)
+    T, n, C, r = 9, 4, 16, 5
+    R = rng.standard_normal((T, n, C)).astype(np.float32)
+    P = (0.1 * rng.standard_normal((T, n, C))).astype(np.float32)
+    w_norm = O.f32_to_bf16_bits((1 + 0.1 * rng.standard_normal((n, C))).astype(np.float32))
+    W_down = O.f32_to_bf16_bits((0.2 * rng.standard_normal((r, n * C))).astype(np.float32))
+    W_up = O.f32_to_bf16_bits((0.2 * rng.standard_normal((n * C, r))).astype(np.float32))
+    logits = rng.standard_normal((T, n, n))
+    Rmix = (np.exp(logits) / np.exp(logits).sum(-1, keepdims=True)).astype(np.float32)
+    idx = np.array([7, 0, 3, 3, 8])
+    for Pv in (P, None):
+        full = O.hc_read(R, Pv, w_norm, W_down, W_up, Rmix, 1e-6)
+        some = O.hc_read_tokens(idx, R, Pv, w_norm, W_down, W_up, Rmix, 1e-6)
+        assert some[0].shape == (len(idx), n, C)
+        np.testing.assert_allclose(some[0], full[0][idx], rtol=1e-6, atol=1e-7)
+        same = some[0] == full[0][idx]
+        assert same.mean() > 0.99
+        for k in (1, 2):
+            assert np.array_equal(some[k][same], full[k][idx][same])
+    # a token's row does not depend on which other tokens are read with it: a wrong
+    # index (off by one) shows up
+    shifted = O.hc_read_tokens(idx + 1 - (idx == 8) * 9, R, P, w_norm, W_down, W_up, Rmix, 1e-6)
+    assert not np.allclose(shifted[0], O.hc_read(R, P, w_norm, W_down, W_up, Rmix, 1e-6)[0][idx])
