@@ -515,10 +515,11 @@ def gpu_arm(args) -> None:
                        stream=stream)
 
         def upmix_fused(k):
-            hc.hc_read_upmix(hc.HC_PATH_PREFILL, T, R, None, None, M, *o, stream=stream)
+            hc.hc_read_upmix(hc.HC_PATH_PREFILL, T, R, None, W0["W_up"], M, *o, stream=stream)
 
         def upmix_pair(k):
-            hc.hc_read_upmix(hc.HC_PATH_PREFILL_UNFUSED, T, R, None, None, M, *o, stream=stream)
+            hc.hc_read_upmix(hc.HC_PATH_PREFILL_UNFUSED, T, R, None, W0["W_up"], M, *o,
+                             stream=stream)
 
         def chunk_bf16(k):
             hc.hc_read_path(hc.HC_PATH_PREFILL_BF16_LO, T, R, None, W0["w_norm"], W0["W_down"],

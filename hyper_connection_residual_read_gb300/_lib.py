@@ -22,7 +22,6 @@ HC_ERR_CUDA = -4
 HC_ERR_TIMEOUT = -5
 HC_ERR_CHECK = -6
 HC_ERR_NOMEM = -7
-HC_ERR_RANGE = -8
 
 HC_PATH_AUTO = 0
 HC_PATH_DECODE = 1
@@ -170,8 +169,8 @@ def hc_read_noalloc(tokens, R, P, w_norm, W_down, W_up, Rmix, out_f32, out_bf16,
 def hc_read_upmix(path, tokens, R, P, W_up, Rmix, out_f32, out_bf16, out_fp16,
                   stream=None) -> None:
     """Re-runs the up projection + gate + mix stage of the last tile-path call
-    (``path``: HC_PATH_PREFILL, HC_PATH_PREFILL_UNFUSED or HC_PATH_PREFILL_BF16_LO;
-    ``W_up`` is read by the last one only and may be None otherwise)."""
+    (``path``: HC_PATH_PREFILL, HC_PATH_PREFILL_UNFUSED or HC_PATH_PREFILL_BF16_LO) on
+    the lo that call left in the library's scratch."""
     _check("hc_read_upmix", load().hc_read_upmix(
         path, tokens, _ptr(R), _ptr(P), _ptr(W_up), _ptr(Rmix), _ptr(out_f32), _ptr(out_bf16),
         _ptr(out_fp16), _stream(stream)))
@@ -187,8 +186,9 @@ def hc_read_y(tokens, R, P, w_norm, W_down, W_up, out_f32, out_bf16, out_fp16,
 
 
 def hc_read_lo_bf16(tokens, lo_out, stream=None) -> None:
-    """Copies the bf16 lo of the last HC_PATH_PREFILL_BF16_LO call into ``lo_out``
-    ([tokens][320] 16-bit device tensor)."""
+    """Copies lo of the last tile-path call, rounded once to bf16 (the A operand of the
+    HC_PATH_PREFILL_BF16_LO up GEMM), into ``lo_out`` ([tokens][320] 16-bit device
+    tensor)."""
     _check("hc_read_lo_bf16", load().hc_read_lo_bf16(tokens, _ptr(lo_out), _stream(stream)))
 
 

@@ -39,11 +39,9 @@ void free_ctx(Ctx& c) {
     cudaFree(c.s.status);
     cudaFree(c.s.sync);
     cudaFree(c.s.sched);
-    cudaFree(c.wd16);
-    cudaFree(c.wu16);
     cudaFree(c.partials);
     cudaFree(c.ssq);
-    cudaFree(c.lo16);
+    cudaFree(c.lo3);
     cudaFree(c.gated);
     c = Ctx();
 }
@@ -121,12 +119,10 @@ int run(int path, const ReadArgs& a, cudaStream_t st) {
             break;
         case HC_PATH_PREFILL:
             ce = launch_prefill(*c, a, PrefillMode::kFused, st);
-            c->lo_mode = 1;
             c->lo_tokens = a.T;
             break;
         case HC_PATH_PREFILL_BF16_LO:
             ce = launch_prefill(*c, a, PrefillMode::kFusedBf16Lo, st);
-            c->lo_mode = 2;
             c->lo_tokens = a.T;
             break;
         default:
@@ -140,7 +136,6 @@ int run(int path, const ReadArgs& a, cudaStream_t st) {
                 }
             }
             ce = launch_prefill(*c, a, PrefillMode::kUnfused, st);
-            c->lo_mode = 1;
             c->lo_tokens = a.T;
             break;
     }
@@ -227,7 +222,7 @@ struct CheckBufs {
 
 using namespace hc;
 
-extern "C" int hc_read_version(void) { return 100; }
+extern "C" int hc_read_version(void) { return 101; }
 
 extern "C" const char* hc_read_strerror(int code) {
     switch (code) {
@@ -239,7 +234,6 @@ extern "C" const char* hc_read_strerror(int code) {
         case HC_ERR_TIMEOUT: return "a bounded device-side wait gave up";
         case HC_ERR_CHECK: return "self check found a mismatch";
         case HC_ERR_NOMEM: return "scratch allocation failed";
-        case HC_ERR_RANGE: return "a prefill activation did not fit fp16 (|R' * w_norm| or |lo| >= 65504)";
         default: return "unknown status";
     }
 }
@@ -262,12 +256,10 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     ok &= cudaMalloc(&c.s.status, sizeof(int)) == cudaSuccess;
     ok &= cudaMalloc(&c.s.sync, 2 * sizeof(unsigned)) == cudaSuccess;
     ok &= cudaMalloc(&c.s.sched, 2 * kSchedPairs * sizeof(int)) == cudaSuccess;
-    ok &= cudaMalloc(&c.wd16, sizeof(__half) * (size_t)kRank * kCols) == cudaSuccess;
-    ok &= cudaMalloc(&c.wu16, sizeof(__half) * (size_t)kCols * kRank) == cudaSuccess;
     const size_t ts = (size_t)partial_tiles(max_tokens) * 128;
     ok &= cudaMalloc(&c.partials, sizeof(float) * ts * kStreams * 4 * kRank) == cudaSuccess;
     ok &= cudaMalloc(&c.ssq, sizeof(float) * ts * kStreams * 4) == cudaSuccess;
-    ok &= cudaMalloc(&c.lo16, sizeof(__half) * 2 * (size_t)max_tokens * kRank) == cudaSuccess;
+    ok &= cudaMalloc(&c.lo3, sizeof(uint16_t) * 3 * (size_t)max_tokens * kRank) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
         free_ctx(c);
@@ -278,7 +270,7 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
         cudaMemset(c.s.sched, 0, 2 * kSchedPairs * sizeof(int)) != cudaSuccess ||
         decode_setup(device) != cudaSuccess ||
         decode_fused_setup(&c.fused_decode) != cudaSuccess ||
-        cudaMemset(c.lo16, 0, sizeof(__half) * 2 * (size_t)max_tokens * kRank) != cudaSuccess ||
+        cudaMemset(c.lo3, 0, sizeof(uint16_t) * 3 * (size_t)max_tokens * kRank) != cudaSuccess ||
         prefill_setup(c) != cudaSuccess ||
         cudaDeviceSynchronize() != cudaSuccess) {
         free_ctx(c);
@@ -314,15 +306,11 @@ extern "C" int hc_read_upmix(int path, int tokens, const float* R, const float* 
     else if (path == HC_PATH_PREFILL_UNFUSED) mode = PrefillMode::kUnfused;
     else if (path == HC_PATH_PREFILL_BF16_LO) mode = PrefillMode::kFusedBf16Lo;
     else return HC_ERR_ARG;
-    // lo must hold what this stage reads: the last tile-path call's lo, of this form,
-    // for at least these tokens
-    const int want = mode == PrefillMode::kFusedBf16Lo ? 2 : 1;
-    if (tokens > 0 && (c->lo_mode != want || tokens > c->lo_tokens)) return HC_ERR_ARG;
-    // W_down is not used by this stage: validate against a harmless stand-in
-    ReadArgs a{tokens, R, P, reinterpret_cast<const uint16_t*>(c->wd16),
-               reinterpret_cast<const uint16_t*>(c->wd16),
-               mode == PrefillMode::kFusedBf16Lo ? W_up : reinterpret_cast<const uint16_t*>(c->wu16),
-               Rmix, out_f32, out_bf16, out_fp16};
+    // lo must hold what this stage reads: the last tile-path call's lo, for at least
+    // these tokens (every tile-path call leaves all three of its bf16 terms)
+    if (tokens > c->lo_tokens) return HC_ERR_ARG;
+    // w_norm and W_down are not used by this stage: validated against W_up, which is
+    ReadArgs a{tokens, R, P, W_up, W_up, W_up, Rmix, out_f32, out_bf16, out_fp16};
     if (int e = validate(*c, a)) return e;
     if (tokens == 0) return HC_OK;
     if (mode == PrefillMode::kUnfused && c->gated == nullptr) {
@@ -348,7 +336,6 @@ extern "C" int hc_read_y(int tokens, const float* R, const float* P, const uint1
     if (tokens == 0) return HC_OK;
     const cudaError_t ce = launch_prefill(*c, a, PrefillMode::kReadoutY,
                                           static_cast<cudaStream_t>(stream));
-    c->lo_mode = 1;
     c->lo_tokens = tokens;
     return ce == cudaSuccess ? HC_OK : HC_ERR_CUDA;
 }
@@ -357,11 +344,11 @@ extern "C" int hc_read_lo_bf16(int tokens, uint16_t* lo_out, void* stream) {
     int err;
     Ctx* c = current_ctx(&err);
     if (!c) return err;
-    if (tokens < 0 || c->lo_mode != 2 || tokens > c->lo_tokens) return HC_ERR_ARG;
+    if (tokens < 0 || tokens > c->lo_tokens) return HC_ERR_ARG;
     if (tokens == 0) return HC_OK;
     if (lo_out == nullptr || (reinterpret_cast<uintptr_t>(lo_out) & 15) != 0) return HC_ERR_ARG;
     if (int e = check_ptr(lo_out, c->device)) return e;
-    return cudaMemcpyAsync(lo_out, c->lo16, sizeof(uint16_t) * (size_t)tokens * kRank,
+    return cudaMemcpyAsync(lo_out, c->lo3, sizeof(uint16_t) * (size_t)tokens * kRank,
                            cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? HC_OK
                : HC_ERR_CUDA;
@@ -377,11 +364,14 @@ extern "C" int hc_read_status(void* stream) {
         cudaMemset(c->s.status, 0, sizeof(int)) != cudaSuccess)
         return HC_ERR_CUDA;
     if (word & kStatusTimeout) {
-        // a kernel that gave up may have left its scheduler pair mid-count
-        if (cudaMemset(c->s.sched, 0, 2 * kSchedPairs * sizeof(int)) != cudaSuccess) return HC_ERR_CUDA;
+        // a kernel that gave up may have left its scheduler pair or the one-kernel
+        // decode read's exchange counters mid-count (the stream is idle here)
+        if (cudaMemset(c->s.sched, 0, 2 * kSchedPairs * sizeof(int)) != cudaSuccess ||
+            cudaMemset(c->s.sync, 0, 2 * sizeof(unsigned)) != cudaSuccess)
+            return HC_ERR_CUDA;
         return HC_ERR_TIMEOUT;
     }
-    return (word & kStatusRangeBit) ? HC_ERR_RANGE : HC_OK;
+    return HC_OK;
 }
 
 extern "C" int hc_read_check(int max_tokens, uint64_t seed, hc_check_report* rep) {

@@ -44,6 +44,22 @@ __device__ __forceinline__ uint16_t to_fp16_bits(float x) {
     return __half_as_ushort(__float2half_rn(x));
 }
 
+// x0 and x1 each as the sum of three bf16 terms, packed in pairs: hi = bf16(x),
+// mid = bf16(x - hi), low = bf16(x - hi - mid), all round to nearest even. Both
+// differences are exact in fp32, so the three terms carry x to about 2^-27 of its size
+// with fp32's exponent range; the tensor cores multiply each term by a bf16 weight
+// exactly and sum the products in fp32.
+__device__ __forceinline__ void split3_bf16(float x0, float x1, uint32_t& hi, uint32_t& mid,
+                                            uint32_t& low) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float r0 = x0 - __low2float(h), r1 = x1 - __high2float(h);
+    const __nv_bfloat162 m = __floats2bfloat162_rn(r0, r1);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(r0 - __low2float(m), r1 - __high2float(m));
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    mid = *reinterpret_cast<const uint32_t*>(&m);
+    low = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // The gate: logistic sigmoid of the up projection times the residual value. expf is
 // the accurate one; the reciprocal is the fast one (within 2 ulp, and 0 when
 // expf(-u) overflows).

@@ -274,18 +274,6 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int* sta
     return true;
 }
 
-// x as the sum of three bf16 terms, packed in pairs: (x0, x1) -> hi, mid, low words.
-__device__ __forceinline__ void split3_bf16(float x0, float x1, uint32_t& hi, uint32_t& mid,
-                                            uint32_t& low) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    const float r0 = x0 - __low2float(h), r1 = x1 - __high2float(h);
-    const __nv_bfloat162 m = __floats2bfloat162_rn(r0, r1);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(r0 - __low2float(m), r1 - __high2float(m));
-    hi = *reinterpret_cast<const uint32_t*>(&h);
-    mid = *reinterpret_cast<const uint32_t*>(&m);
-    low = *reinterpret_cast<const uint32_t*>(&l);
-}
-
 template <int T>
 __global__ void __launch_bounds__(kTcThreads, 1)
 up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, const float* P,

@@ -34,7 +34,6 @@ constexpr int kSchedPairs = 2;
 
 // Device status word bits.
 constexpr int kStatusTimeout = 1;
-constexpr int kStatusRangeBit = 2;   // a prefill activation did not fit fp16
 
 struct Scratch {
     float* lo = nullptr;             // [max_tokens][kRank], the down projection's output
@@ -56,22 +55,17 @@ struct Ctx {
     char name[64] = {0};
     Scratch s;
     // prefill scratch
-    __half* wd16 = nullptr;          // W_down as fp16 [kRank][kCols]
-    __half* wu16 = nullptr;          // W_up as fp16 [kCols][kRank]
     // down partials, tile-blocked, in column quads, token-minor: [tiles][kStreams]
     // [4 K quarters][kRank / 4][128 tokens][4], and the sums of squares of R'
     // [tiles][kStreams][4 K quarters][128 tokens], tiles = partial_tiles(max_tokens)
     float* partials = nullptr;
     float* ssq = nullptr;
-    __half* lo16 = nullptr;          // lo as two fp16 terms [2][max_tokens][kRank]
+    // lo as three bf16 terms [3][max_tokens][kRank] (hi, mid, low; hi alone is lo
+    // rounded once to bf16)
+    uint16_t* lo3 = nullptr;
     float* gated = nullptr;          // [max_tokens][kCols], unfused prefill only (lazy)
-    CUtensorMap tm_wd;               // TMA maps over wd16, wu16, lo16
-    CUtensorMap tm_wu;
-    CUtensorMap tm_lo;
-    CUtensorMap tm_lo_bf16;          // lo16's first term read as bf16 (bf16-lo mode)
-    // what the last tile-path call left in lo16: 0 nothing, 1 two fp16 terms, 2 one
-    // bf16 term; and for how many tokens
-    int lo_mode = 0;
+    CUtensorMap tm_lo;               // TMA map over lo3
+    // tokens whose lo the last tile-path call left in lo3 (0: none)
     int lo_tokens = 0;
 };
 
@@ -116,9 +110,9 @@ cudaError_t prefill_setup(Ctx& ctx);
 // kReadoutY: the 2560-wide read-out y = sum of the gated streams, [T][2560] outputs.
 enum class PrefillMode { kFused, kUnfused, kFusedBf16Lo, kReadoutY };
 cudaError_t launch_prefill(const Ctx& ctx, const ReadArgs& a, PrefillMode mode, cudaStream_t st);
-// The two halves of the tile path: weights to fp16, down GEMM and lo split; then the
-// up GEMM with its gate + mix epilogue (fused) or writing gated + the mix (unfused).
-cudaError_t launch_prefill_down(const Ctx& ctx, const ReadArgs& a, PrefillMode mode, cudaStream_t st);
+// The two halves of the tile path: down GEMM and lo split; then the up GEMM with its
+// gate + mix epilogue (fused) or writing gated + the mix (unfused).
+cudaError_t launch_prefill_down(const Ctx& ctx, const ReadArgs& a, cudaStream_t st);
 // pdl: launched with programmatic dependent launch right after lo_split (inside a
 // read); the stage run alone is an ordinary launch (its predecessor may write R).
 cudaError_t launch_prefill_upmix(const Ctx& ctx, const ReadArgs& a, PrefillMode mode,

@@ -1,29 +1,29 @@
 // Prefill path of the hyper-connection read: thousands of tokens per call, on the
 // tcgen05 tensor cores with accumulators in tensor memory and operands fed by TMA.
 //
-//   convert_weights  W_down and W_up, bf16 -> fp16 (exact for |w| >= 2^-17; below
-//                    that the fp16 grid of 2^-24 rounds them by at most 3e-8).
 //   down_tile        the down projection per (128-token tile, stream, quarter of the
-//                    stream's 2560 columns): A = R' * w_norm split on the fly into two
-//                    fp16 terms (hi + residual), B = those columns of W_down, D = 128 x
-//                    320 fp32 in TMEM. The epilogue stores the unscaled partial dots
-//                    and the quarter's sums of squares of R'.
+//                    stream's 2560 columns): A = R' * w_norm split on the fly into three
+//                    bf16 terms, B = those columns of the caller's bf16 W_down as stored,
+//                    D = 128 x 320 fp32 in TMEM. The epilogue stores the unscaled
+//                    partial dots and the quarter's sums of squares of R'.
 //   lo_split         the norm fold of "#2488 sycl/A770: faster hyper-connection read
 //                    on Arc A-series", Summary, change 4: each stream's rs applied to
 //                    that stream's partial dots, summed in a fixed order; lo is stored
-//                    as two fp16 terms for the up projection's A operand.
-//   upmix_tile       the up projection per (128-token tile, 64 columns x 4 streams),
-//                    D = 128 x 256 fp32, double-buffered in TMEM; the epilogue applies
-//                    the gate and the 4x4 mix and writes mixed with its bf16 and fp16
-//                    images, so `gated` never reaches memory ("#1370 prefill: opt-in
-//                    STRATA_HC_UPMIX=1 on CUDA - the hyper-connection up projection with
-//                    gr_mix_r as its epilogue (sm_80+)", "Why" and "What it does").
-//                    The unfused variant stores `gated` instead, and mix_gated applies
-//                    the same mix afterwards (bitwise the same result).
+//                    as three bf16 terms for the up projection's A operand.
+//   upmix_tile       the up projection per (128-token tile, 64 columns x 4 streams) on
+//                    the caller's bf16 W_up, D = 128 x 256 fp32, double-buffered in
+//                    TMEM; the epilogue applies the gate and the 4x4 mix and writes
+//                    mixed with its bf16 and fp16 images, so `gated` never reaches
+//                    memory ("#1370 prefill: opt-in STRATA_HC_UPMIX=1 on CUDA - the
+//                    hyper-connection up projection with gr_mix_r as its epilogue
+//                    (sm_80+)", "Why" and "What it does"). The unfused variant stores
+//                    `gated` instead, and mix_gated applies the same mix afterwards
+//                    (bitwise the same result).
 //
-// Two fp16 terms per activation reproduce fp32 accuracy: the residual term carries
-// the next 11 bits, and the weights are exact in fp16, so each product of the MMA
-// is exact and the sums are fp32 in TMEM.
+// Three bf16 terms per activation (hi, mid, low; see split3_bf16) reproduce fp32
+// accuracy with fp32's exponent range, so the path takes any finite fp32 input; the
+// weights are used as the caller stores them (bf16, exact), each product of the MMA
+// is exact, and the sums are fp32 in TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -39,17 +39,20 @@ using namespace tc;
 
 constexpr int kTileM = 128;            // tokens per tile (TMEM lanes)
 constexpr int kBK = 64;                // K per pipeline stage: one 128-byte swizzle row
-constexpr int kTileBytes16 = kTileM * kBK * 2;    // 16 KB: one 128 x 64 fp16 operand tile
+constexpr int kTileBytes16 = kTileM * kBK * 2;    // 16 KB: one 128 x 64 bf16 operand tile
+constexpr int kTerms = 3;              // bf16 terms of an activation (split3_bf16)
 
 // down_tile
 constexpr int kDownN = kRank;          // 320 accumulator columns (two MMAs of N = 160)
-constexpr int kDownStages = 3;
+// Two stages of 88 KB (three 16 KB A terms and 40 KB of W_down): a third does not fit
+// in shared memory. R blocks are asked into L2 ahead of their loads (kDownPrefetch).
+constexpr int kDownStages = 2;
 constexpr int kDownBBytes = kDownN * kBK * 2;     // 40 KB
-constexpr int kDownStageBytes = 2 * kTileBytes16 + kDownBBytes;
+constexpr int kDownStageBytes = kTerms * kTileBytes16 + kDownBBytes;
 constexpr int kDownKBlocks = kWidth / kBK;        // 40 per stream
 // Each stream's K is split into quarters with an accumulator (and a partial) each:
 // the tensor cores' fp32 accumulation rounds toward zero at every MMA, so the depth
-// of one accumulation (here 10 K blocks x 4 steps x 2 terms = 80 MMAs) bounds the
+// of one accumulation (here 10 K blocks x 4 steps x 3 terms = 120 MMAs) bounds the
 // relative shrink of the result.
 constexpr int kDownKSplit = 4;
 constexpr int kDownKBlocksPerTile = kDownKBlocks / kDownKSplit;   // 10
@@ -74,7 +77,7 @@ constexpr int kUpCols = 64;            // output columns per tile (x 4 streams =
 constexpr int kUpN = kStreams * kUpCols;
 constexpr int kUpStages = 2;
 constexpr int kUpBBytes = kUpN * kBK * 2;         // 32 KB
-constexpr int kUpStageBytes = 2 * kTileBytes16 + kUpBBytes;
+constexpr int kUpStageBytes = kTerms * kTileBytes16 + kUpBBytes;   // 80 KB
 constexpr int kUpKBlocks = kRank / kBK;           // 5
 constexpr int kUpColTiles = kWidth / kUpCols;     // 40
 // Eight epilogue warps: two per TMEM lane quarter (32 tokens), one for each half of
@@ -107,24 +110,18 @@ constexpr int kRSlot = kStreams * kTileM * kEpiCols * 4;        // 16 KB
 // warp that waits on a slot's barrier consumes every fill of that slot. (With one
 // ring shared by both groups a warp a tile ahead of the other group could wait on
 // a slot whose previous fill, for the other group, was still in flight, and its
-// parity wait would take the fill before that one as complete.)
-constexpr int kRSlotsPerGroup = 3;
+// parity wait would take the fill before that one as complete.) Two slots a group:
+// with the three-term operand stages, shared memory holds no more. Without a
+// pending write one step's R is loaded while the previous one is consumed; with
+// one, a step takes both slots (R, then P).
+constexpr int kRSlotsPerGroup = 2;
 constexpr int kRSlots = 2 * kRSlotsPerGroup;
 constexpr int kUpSmem = kUpStages * kUpStageBytes + kRSlots * kRSlot + 1024;
-
-constexpr int kStatusRange = kStatusRangeBit;
+static_assert(kUpSmem <= 227 * 1024 - 1024, "up tile shared memory");
+static_assert(kDownSmem <= 227 * 1024 - 2048, "down tile shared memory");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-// hi = fp16(x), lo = fp16(x - hi): two fp16 terms whose sum carries 22 bits of x.
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-    const __half2 h = __floats2half2_rn(x0, x1);
-    const float2 hf = __half22float2(h);
-    const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-    hi = *reinterpret_cast<const uint32_t*>(&h);
-    lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // 32-byte global accesses (one whole DRAM sector per lane).
@@ -144,40 +141,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 
 // ---------------------------------------------------------------------------
-// weights bf16 -> fp16
-// ---------------------------------------------------------------------------
-__global__ void convert_weights_kernel(const uint16_t* __restrict__ wd, const uint16_t* __restrict__ wu,
-                                       __half* __restrict__ wd16, __half* __restrict__ wu16,
-                                       int n8_each, bool down_only) {
-    // the down tile after it (launched with programmatic dependent launch) may start
-    // its prologue and R stream now; it waits for this grid before loading W_down
-    pdl_launch_dependents();
-    const int n = down_only ? n8_each : 2 * n8_each;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-        const bool up = i >= n8_each;
-        const int j = up ? i - n8_each : i;
-        const uint4 v = *reinterpret_cast<const uint4*>((up ? wu : wd) + 8 * (size_t)j);
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const __half2 h = __floats2half2_rn(bf16_lo(in[q]), bf16_hi(in[q]));
-            out[q] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        *reinterpret_cast<uint4*>((up ? wu16 : wd16) + 8 * (size_t)j) =
-            make_uint4(out[0], out[1], out[2], out[3]);
-    }
-}
-
-// ---------------------------------------------------------------------------
 // down projection, one (128-token tile, stream, K quarter) per tile, persistent CTAs
 //
 // R reaches shared memory by TMA into the stage's A region, 32 KB of fp32 per K
 // block, laid out so that the 16 rows each converter warp owns occupy exactly the
-// bytes where that warp then writes the rows' two fp16 terms (hi in the first
-// 16 KB, lo in the second, 128-byte swizzled): the warp reads its rows into
-// registers, scales and splits them, and overwrites them in place, with no
-// synchronisation beyond the warp. The view of R that gives this layout is
+// bytes where that warp then writes the rows' first two bf16 terms (hi in the first
+// 16 KB, mid in the second, 128-byte swizzled; low goes to the third 16 KB): the warp
+// reads its rows into registers, scales and splits them, and overwrites them in
+// place, with no synchronisation beyond the warp. The view of R that gives this layout is
 // (column, stream, row r, half h, group g) with token = 16 g + 8 h + r; a tile's
 // two loads (h = 0, 1) each take 8 rows of 8 groups. A last tile with fewer than
 // 128 tokens is read by the converter warps from global memory instead.
@@ -186,8 +157,7 @@ __global__ void __launch_bounds__(kDownThreads, 1)
 down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                  const uint16_t* __restrict__ w_norm, const __grid_constant__ CUtensorMap tm_wd,
                  const __grid_constant__ CUtensorMap tm_r, float* __restrict__ partials,
-                 float* __restrict__ ssq, int T, int* __restrict__ status, int* __restrict__ sched,
-                 int pdl) {
+                 float* __restrict__ ssq, int T, int* __restrict__ status, int* __restrict__ sched) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full_bar[kDownStages], empty_bar[kDownStages];
@@ -226,7 +196,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
     const uint32_t tmem = tmem_slot;
 
     auto sA = [&](int slot, int term) { return smem + slot * kDownStageBytes + term * kTileBytes16; };
-    auto sB = [&](int slot) { return smem + slot * kDownStageBytes + 2 * kTileBytes16; };
+    auto sB = [&](int slot) { return smem + slot * kDownStageBytes + kTerms * kTileBytes16; };
     // the CTA's i-th tile from the queue (n_tiles: no more tiles, or the CTA gave up),
     // taken by a whole warp (its lane 0 releases the entry once every lane has read
     // it) or by one thread
@@ -247,7 +217,6 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             // the tile after the current one is fetched one tile early, so that its
             // first R blocks can be asked into L2 while the current tile is loaded
             int next = blockIdx.x;
-            bool wd_ready = !pdl;
             for (int i = 0; !abort_flag; ++i) {
                 if (!mbar_wait(&tq_empty[i % kDownTileQ], ((i / kDownTileQ) & 1) ^ 1, &abort_flag, status))
                     break;
@@ -266,20 +235,12 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     const int slot = it % kDownStages;
                     const uint32_t ph = (it / kDownStages) & 1;
                     if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
-                    // R (final before the read began) first; W_down's fp16 copy is written
-                    // by the conversion kernel before this one, so with programmatic
-                    // dependent launch it waits for that grid
                     if (full) {
                         mbar_arrive_expect_tx(&r_full[slot], 2 * kTileBytes16);
                         tma_load_5d(sA(slot, 0), &tm_r, kb * kBK, s, 0, 0, tt * 8, &r_full[slot]);
                         tma_load_5d(sA(slot, 1), &tm_r, kb * kBK, s, 0, 1, tt * 8, &r_full[slot]);
                     } else {
                         mbar_arrive(&r_full[slot]);
-                    }
-                    if (!wd_ready) {
-                        pdl_wait();
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                        wd_ready = true;
                     }
                     mbar_arrive_expect_tx(&full_bar[slot], kDownBBytes);
                     const int x = s * kWidth + kb * kBK;
@@ -302,7 +263,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
     } else if (warp == 1) {
         // MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(kTileM, kDownN / 2);
+            const uint32_t idesc = idesc_bf16_f32(kTileM, kDownN / 2);
             int it = 0;
             // waits until half-buffer use u may be written: its previous use drained
             auto half_free = [&](int u) {
@@ -334,7 +295,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                             tc_fence_after();
                         }
 #pragma unroll
-                        for (int term = 0; term < 2; ++term) {
+                        for (int term = 0; term < kTerms; ++term) {
                             const uint32_t a0 = smem_u32(sA(slot, term));
 #pragma unroll
                             for (int kk = 0; kk < kBK / 16; ++kk)
@@ -362,7 +323,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             const int tt = tile / (kStreams * kDownKSplit);
             const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
             const bool full = (tt + 1) * kTileM <= T;
-            float ss[8], amax = 0.f;
+            float ss[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss[i] = 0.f;
             // w_norm of this lane's 4 columns, loaded one K block ahead
@@ -393,7 +354,8 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                 const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x), w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
                 if (!mbar_wait(&r_full[slot], ph, &abort_flag, status)) break;
                 uint8_t* ahi = sA(slot, 0);
-                uint8_t* alo = sA(slot, 1);
+                uint8_t* amid = sA(slot, 1);
+                uint8_t* alow = sA(slot, 2);
                 if (full) {
                     // R rows j = 2i + (lane >> 4) of this warp: half j >> 3, row j & 7
 #pragma unroll
@@ -420,24 +382,22 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     sq = fmaf(r.z, r.z, sq);
                     sq = fmaf(r.w, r.w, sq);
                     ss[i] += sq;
-                    const float a0 = r.x * w0, a1 = r.y * w1, a2 = r.z * w2, a3 = r.w * w3;
-                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a0), fabsf(a1)), fmaxf(fabsf(a2), fabsf(a3))));
-                    uint32_t h0, l0, h1, l1;
-                    split2(a0, a1, h0, l0);
-                    split2(a2, a3, h1, l1);
+                    uint32_t h0, m0, l0, h1, m1, l1;
+                    split3_bf16(r.x * w0, r.y * w1, h0, m0, l0);
+                    split3_bf16(r.z * w2, r.w * w3, h1, m1, l1);
                     const uint32_t off = sw128_offset(row, kc);
                     *reinterpret_cast<uint2*>(ahi + off) = make_uint2(h0, h1);
-                    *reinterpret_cast<uint2*>(alo + off) = make_uint2(l0, l1);
+                    *reinterpret_cast<uint2*>(amid + off) = make_uint2(m0, m1);
+                    *reinterpret_cast<uint2*>(alow + off) = make_uint2(l0, l1);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&full_bar[slot]);
             }
             if (abort_flag) break;
-            if (amax >= 65504.f) atomicOr(status, kStatusRange);
             // sums of squares per row: the 16 lanes that share a row, in a fixed order.
             // The buffer of this parity was last read by the epilogue two tiles ago,
             // before it released that tile's second half-buffer; this tile's MMAs,
-            // which the conversions run at most three stages ahead of, waited for
+            // which the conversions run at most two stages ahead of, waited for
             // that release.
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -512,8 +472,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
 
 // ---------------------------------------------------------------------------
 // lo = sum over the streams (in order) of rs times the sum of the stream's quarter
-// partials (in order); stored as two fp16 terms, or as one bf16 term in the bf16-lo
-// mode. The partials come tile-blocked, in column quads, token-minor ([tile][stream]
+// partials (in order); stored as three bf16 terms [3][max_tokens][320] (hi, mid,
+// low; the bf16-lo mode of the up tile reads hi alone, which is lo rounded once to
+// bf16, nearest even). The partials come tile-blocked, in column quads, token-minor ([tile][stream]
 // [quarter][column / 4][128 tokens][4 columns]). A CTA takes one tile's 128 tokens
 // and 32 of the columns (8 quads): for each (stream, quarter) these are 16 KB in one
 // piece, and a lane reads one token's quad, a warp 512 contiguous bytes; shared
@@ -523,11 +484,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
 constexpr int kLoCols = 32;
 constexpr int kLoThreads = 512;    // 16 warps, two of the 32 columns each
 
-template <bool kBf16>
 __global__ void __launch_bounds__(kLoThreads)
 lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ssq,
-                __half* __restrict__ lo16, int T, int max_tokens, float eps,
-                int* __restrict__ status) {
+                uint16_t* __restrict__ lo3, int T, int max_tokens, float eps) {
     // the up tile after it (launched with programmatic dependent launch inside a read)
     // may start its prologue, R stream and weight loads now; it waits for this grid
     // before it loads lo
@@ -590,18 +549,13 @@ lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ss
         const int c4 = 4 * (lane & 7);
         const float x0 = lo_s[r][c4], x1 = lo_s[r][c4 + 1], x2 = lo_s[r][c4 + 2], x3 = lo_s[r][c4 + 3];
         const size_t off = (size_t)trow * kRank + cg * kLoCols + c4;
-        if (kBf16) {
-            // the pages' numerics: lo rounded once to bf16 (nearest even), one term
-            *reinterpret_cast<uint2*>(lo16 + off) = make_uint2(pack_bf16x2(x0, x1), pack_bf16x2(x2, x3));
-            continue;
-        }
-        if (fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3))) >= 65504.f)
-            atomicOr(status, kStatusRange);
-        uint32_t h0, l0, h1, l1;
-        split2(x0, x1, h0, l0);
-        split2(x2, x3, h1, l1);
-        *reinterpret_cast<uint2*>(lo16 + off) = make_uint2(h0, h1);
-        *reinterpret_cast<uint2*>(lo16 + (size_t)max_tokens * kRank + off) = make_uint2(l0, l1);
+        const size_t term = (size_t)max_tokens * kRank;
+        uint32_t h0, m0, l0, h1, m1, l1;
+        split3_bf16(x0, x1, h0, m0, l0);
+        split3_bf16(x2, x3, h1, m1, l1);
+        *reinterpret_cast<uint2*>(lo3 + off) = make_uint2(h0, h1);
+        *reinterpret_cast<uint2*>(lo3 + term + off) = make_uint2(m0, m1);
+        *reinterpret_cast<uint2*>(lo3 + 2 * term + off) = make_uint2(l0, l1);
     }
 }
 
@@ -620,10 +574,11 @@ struct EpiMaps {
 // kOut: what the epilogue writes. kOutGated: gated (fp32, the unfused pair's first
 // half); kOutMix: the 4x4 mix with the bf16/fp16 images; kOutY: the 2560-wide
 // read-out y[c] = sum_s gated[s][c] (streams in order) with its images.
-// kTerms = 2: A is lo as two fp16 terms and B the fp16 copy of W_up (fp32-accurate);
-// kTerms = 1: A is lo rounded to bf16 and B the caller's bf16 W_up (one MMA per step).
+// kLoTerms = 3: A is lo as its three bf16 terms (fp32-accurate); kLoTerms = 1: A is
+// the first term alone, lo rounded once to bf16 (one MMA per step). B is the caller's
+// bf16 W_up as stored in both.
 constexpr int kOutGated = 0, kOutMix = 1, kOutY = 2;
-template <int kOut, int kTerms>
+template <int kOut, int kLoTerms>
 __global__ void __launch_bounds__(kUpThreads, 1)
 upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtensorMap tm_lo,
                   const __grid_constant__ CUtensorMap tm_wu, const __grid_constant__ EpiMaps em,
@@ -680,7 +635,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
     const uint32_t tmem = tmem_slot;
 
     auto sA = [&](int slot, int term) { return smem + slot * kUpStageBytes + term * kTileBytes16; };
-    auto sB = [&](int slot) { return smem + slot * kUpStageBytes + 2 * kTileBytes16; };
+    auto sB = [&](int slot) { return smem + slot * kUpStageBytes + kTerms * kTileBytes16; };
     uint8_t* rring = smem + kUpStages * kUpStageBytes;
     // the CTA's i-th tile from the queue (n_tiles: no more tiles, or the CTA gave up)
     auto take_tile = [&](int i) -> int {
@@ -714,7 +669,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     const int slot = it % kUpStages;
                     const uint32_t ph = (it / kUpStages) & 1;
                     if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
-                    mbar_arrive_expect_tx(&full_bar[slot], kTerms * kTileBytes16 + kUpBBytes);
+                    mbar_arrive_expect_tx(&full_bar[slot], kLoTerms * kTileBytes16 + kUpBBytes);
 #pragma unroll
                     for (int s = 0; s < kStreams; ++s)
                         tma_load_2d_hint(sB(slot) + s * (kUpBBytes / kStreams), &tm_wu, kb * kBK,
@@ -726,7 +681,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                         lo_ready = true;
                     }
 #pragma unroll
-                    for (int term = 0; term < kTerms; ++term)
+                    for (int term = 0; term < kLoTerms; ++term)
                         tma_load_3d_hint(sA(slot, term), &tm_lo, kb * kBK, tt * kTileM, term,
                                          &full_bar[slot], keep);
                 }
@@ -734,7 +689,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = kTerms == 2 ? idesc_f16_f32(kTileM, kUpN) : idesc_bf16_f32(kTileM, kUpN);
+            const uint32_t idesc = idesc_bf16_f32(kTileM, kUpN);
             int it = 0;
             for (int lt = 0; !abort_flag; ++lt) {
                 const int tile = take_tile(lt);
@@ -751,7 +706,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     tc_fence_after();
                     const uint32_t b0 = smem_u32(sB(slot));
 #pragma unroll
-                    for (int term = 0; term < kTerms; ++term) {
+                    for (int term = 0; term < kLoTerms; ++term) {
                         const uint32_t a0 = smem_u32(sA(slot, term));
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
@@ -858,6 +813,9 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
 #pragma unroll
                             for (int e = 0; e < kEpiCols; ++e) rp[s][e] = which ? rp[s][e] + x[e] : x[e];
                         }
+                        // the next fill of this slot is a TMA write (async proxy): order
+                        // this lane's generic reads of the slot before it, then release
+                        fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0 && !(kTmaOut && which == 0)) mbar_arrive(&r_empty[slot]);
                     }
@@ -1011,12 +969,6 @@ bool encode_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, int 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool encode_fp16(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                 const cuuint64_t* strides, const cuuint32_t* box) {
-    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, rank, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
 // A [T][4][2560] activation or output tensor seen as 3D (c, stream, token), in tiles
 // of `cols` columns x 1 stream x `rows` tokens (TMA clips and zero-fills past T).
 bool encode_act(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base, int T,
@@ -1041,104 +993,77 @@ bool encode_down_r(CUtensorMap* map, const float* R, int T) {
                       CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// The caller's W_down [kRank][kCols] bf16 in boxes of 64 K x 160 rows, 128-byte
+// swizzled: one N half of a down tile's B operand per box.
+bool encode_w_down_bf16(CUtensorMap* map, const uint16_t* W_down) {
+    const cuuint64_t dims[2] = {kCols, kRank};
+    const cuuint64_t strides[1] = {kCols * 2};
+    const cuuint32_t box[2] = {kBK, kDownN / 2};
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W_down, 2, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 }  // namespace
 
+bool encode_w_up_bf16(CUtensorMap* map, const uint16_t* W_up, int box_rows) {
+    const cuuint64_t dims[2] = {kRank, kCols};
+    const cuuint64_t strides[1] = {kRank * 2};
+    const cuuint32_t box[2] = {kBK, (cuuint32_t)box_rows};
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W_up, 2, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 cudaError_t prefill_setup(Ctx& c) {
-    // tensor maps over the library's own scratch: fixed for the context's lifetime
+    // lo's three bf16 terms [3][max_tokens][kRank] in the library's scratch: the up
+    // tile's A operand, in boxes of 64 K x 128 tokens x 1 term (fixed for the context)
     {
-        const cuuint64_t dims[2] = {kCols, kRank};
-        const cuuint64_t strides[1] = {kCols * 2};
-        const cuuint32_t box[2] = {kBK, kDownN / 2};
-        if (!encode_fp16(&c.tm_wd, c.wd16, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    }
-    {
-        const cuuint64_t dims[2] = {kRank, kCols};
-        const cuuint64_t strides[1] = {kRank * 2};
-        const cuuint32_t box[2] = {kBK, kUpCols};
-        if (!encode_fp16(&c.tm_wu, c.wu16, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    }
-    {
-        const cuuint64_t dims[3] = {kRank, (cuuint64_t)c.max_tokens, 2};
+        const cuuint64_t dims[3] = {kRank, (cuuint64_t)c.max_tokens, kTerms};
         const cuuint64_t strides[2] = {kRank * 2, (cuuint64_t)c.max_tokens * kRank * 2};
         const cuuint32_t box[3] = {kBK, kTileM, 1};
-        if (!encode_fp16(&c.tm_lo, c.lo16, 3, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!encode_map(&c.tm_lo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.lo3, 3, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaFuncSetAttribute(down_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kDownSmem);
     if (e != cudaSuccess) return e;
-    {
-        const cuuint64_t dims[3] = {kRank, (cuuint64_t)c.max_tokens, 1};
-        const cuuint64_t strides[2] = {kRank * 2, (cuuint64_t)c.max_tokens * kRank * 2};
-        const cuuint32_t box[3] = {kBK, kTileM, 1};
-        if (!encode_map(&c.tm_lo_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.lo16, 3, dims, strides,
-                        box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return cudaErrorInvalidValue;
-    }
     // the register split of the up tile assumes the launch register count it was
     // written for: refuse to run a build whose count differs (the epilogue's
     // setmaxnreg.inc would wait for registers that are never given up)
-    {
+    const void* ks[] = {reinterpret_cast<const void*>(upmix_tile_kernel<kOutMix, kTerms>),
+                        reinterpret_cast<const void*>(upmix_tile_kernel<kOutMix, 1>),
+                        reinterpret_cast<const void*>(upmix_tile_kernel<kOutY, kTerms>),
+                        reinterpret_cast<const void*>(upmix_tile_kernel<kOutGated, kTerms>)};
+    for (const void* k : ks) {
         cudaFuncAttributes fa;
-        const void* ks[] = {reinterpret_cast<const void*>(upmix_tile_kernel<kOutMix, 2>),
-                            reinterpret_cast<const void*>(upmix_tile_kernel<kOutMix, 1>),
-                            reinterpret_cast<const void*>(upmix_tile_kernel<kOutY, 2>),
-                            reinterpret_cast<const void*>(upmix_tile_kernel<kOutGated, 2>)};
-        for (const void* k : ks) {
-            if ((e = cudaFuncGetAttributes(&fa, k)) != cudaSuccess) return e;
-            if (fa.numRegs != kUpRegsLaunch) return cudaErrorInvalidConfiguration;
-        }
+        if ((e = cudaFuncGetAttributes(&fa, k)) != cudaSuccess) return e;
+        if (fa.numRegs != kUpRegsLaunch) return cudaErrorInvalidConfiguration;
+        if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kUpSmem)) !=
+            cudaSuccess)
+            return e;
     }
-    e = cudaFuncSetAttribute(upmix_tile_kernel<kOutMix, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kUpSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(upmix_tile_kernel<kOutMix, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kUpSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(upmix_tile_kernel<kOutY, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kUpSmem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(upmix_tile_kernel<kOutGated, 2>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kUpSmem);
+    return cudaSuccess;
 }
 
-cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, PrefillMode mode, cudaStream_t st) {
-    const int n8 = kRank * kCols / 8;
-    // the bf16-lo mode feeds the caller's bf16 W_up to the up GEMM: only W_down is converted
-    convert_weights_kernel<<<2 * c.sm_count, 512, 0, st>>>(a.W_down, a.W_up, c.wd16, c.wu16,
-                                                           n8, mode == PrefillMode::kFusedBf16Lo);
+cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, cudaStream_t st) {
     const int n_tt = (a.T + kTileM - 1) / kTileM;
     const int down_tiles = n_tt * kStreams * kDownKSplit;
     const int down_grid = down_tiles < c.sm_count ? down_tiles : c.sm_count;
-    CUtensorMap tm_r;
-    if (!encode_down_r(&tm_r, a.R, a.T)) return cudaErrorInvalidValue;
-    {
-        // programmatic dependent launch after the conversion kernel: the prologue and
-        // the first R blocks overlap its end
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(down_grid);
-        cfg.blockDim = dim3(kDownThreads);
-        cfg.dynamicSmemBytes = kDownSmem;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, down_tile_kernel, a.R, a.P, a.w_norm, c.tm_wd,
-                                           tm_r, c.partials, c.ssq, a.T, c.s.status,
-                                           c.s.sched + 2 * kSchedDown, 1);
-        if (e != cudaSuccess) return e;
-    }
-    const int rgrid = ((a.T + kTileM - 1) / kTileM) * (kRank / kLoCols);
-    if (mode == PrefillMode::kFusedBf16Lo)
-        lo_split_kernel<true><<<rgrid, kLoThreads, 0, st>>>(c.partials, c.ssq, c.lo16, a.T,
-                                                            c.max_tokens, c.eps, c.s.status);
-    else
-        lo_split_kernel<false><<<rgrid, kLoThreads, 0, st>>>(c.partials, c.ssq, c.lo16, a.T,
-                                                             c.max_tokens, c.eps, c.s.status);
+    CUtensorMap tm_r, tm_wd;
+    if (!encode_down_r(&tm_r, a.R, a.T) || !encode_w_down_bf16(&tm_wd, a.W_down))
+        return cudaErrorInvalidValue;
+    // an ordinary launch: the first kernel of the read reads R and P, which the kernel
+    // before it on the stream may have written
+    down_tile_kernel<<<down_grid, kDownThreads, kDownSmem, st>>>(
+        a.R, a.P, a.w_norm, tm_wd, tm_r, c.partials, c.ssq, a.T, c.s.status,
+        c.s.sched + 2 * kSchedDown);
+    const int rgrid = n_tt * (kRank / kLoCols);
+    lo_split_kernel<<<rgrid, kLoThreads, 0, st>>>(c.partials, c.ssq, c.lo3, a.T, c.max_tokens,
+                                                  c.eps);
     return cudaGetLastError();
 }
 
+namespace {
 // An up tile launch, with programmatic stream serialisation when `pdl`.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_up(void (*kernel)(KArgs...), int grid, bool pdl, cudaStream_t st, Args... args) {
@@ -1154,6 +1079,7 @@ cudaError_t launch_up(void (*kernel)(KArgs...), int grid, bool pdl, cudaStream_t
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+}  // namespace
 
 cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mode, cudaStream_t st,
                                  bool pdl) {
@@ -1161,7 +1087,9 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
     const int up_tiles = n_tt * kUpColTiles;
     const int up_grid = up_tiles < c.sm_count ? up_tiles : c.sm_count;
     EpiMaps em;
-    bool ok = encode_act(&em.R, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.R, a.T, kEpiCols, kTileM);
+    CUtensorMap tm_wu;
+    bool ok = encode_w_up_bf16(&tm_wu, a.W_up, kUpCols);
+    ok = ok && encode_act(&em.R, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.R, a.T, kEpiCols, kTileM);
     ok = ok && encode_act(&em.P, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.P ? a.P : a.R, a.T,
                           kEpiCols, kTileM);
     // the mix's fp32 output (any [T][4][2560] fp32 tensor for the other epilogues)
@@ -1170,41 +1098,29 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
                           kEpiCols, kEpiRows);
     if (!ok) return cudaErrorInvalidValue;
     const int has_P = a.P != nullptr;
+    int* sched = c.s.sched + 2 * kSchedUp;
+    cudaError_t e = cudaSuccess;
     switch (mode) {
         case PrefillMode::kFused:
-            if (cudaError_t e = launch_up(upmix_tile_kernel<kOutMix, 2>, up_grid, pdl, st, a.Rmix,
-                                          c.tm_lo, c.tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16,
-                                          has_P, a.T, c.s.status, c.s.sched + 2 * kSchedUp, (int)pdl))
-                return e;
+            e = launch_up(upmix_tile_kernel<kOutMix, kTerms>, up_grid, pdl, st, a.Rmix, c.tm_lo,
+                          tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16, has_P, a.T, c.s.status,
+                          sched, (int)pdl);
             break;
-        case PrefillMode::kFusedBf16Lo: {
-            CUtensorMap tm_wu_bf16;   // over the caller's W_up [kCols][kRank] bf16
-            const cuuint64_t dims[2] = {kRank, kCols};
-            const cuuint64_t strides[1] = {kRank * 2};
-            const cuuint32_t box[2] = {kBK, kUpCols};
-            if (!encode_map(&tm_wu_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.W_up, 2, dims, strides,
-                            box, CU_TENSOR_MAP_SWIZZLE_128B))
-                return cudaErrorInvalidValue;
-            if (cudaError_t e = launch_up(upmix_tile_kernel<kOutMix, 1>, up_grid, pdl, st, a.Rmix,
-                                          c.tm_lo_bf16, tm_wu_bf16, em, a.out_f32, a.out_bf16,
-                                          a.out_fp16, has_P, a.T, c.s.status,
-                                          c.s.sched + 2 * kSchedUp, (int)pdl))
-                return e;
+        case PrefillMode::kFusedBf16Lo:
+            e = launch_up(upmix_tile_kernel<kOutMix, 1>, up_grid, pdl, st, a.Rmix, c.tm_lo, tm_wu,
+                          em, a.out_f32, a.out_bf16, a.out_fp16, has_P, a.T, c.s.status, sched,
+                          (int)pdl);
             break;
-        }
         case PrefillMode::kReadoutY:
-            if (cudaError_t e = launch_up(upmix_tile_kernel<kOutY, 2>, up_grid, pdl, st,
-                                          (const float*)nullptr, c.tm_lo, c.tm_wu, em, a.out_f32,
-                                          a.out_bf16, a.out_fp16, has_P, a.T, c.s.status,
-                                          c.s.sched + 2 * kSchedUp, (int)pdl))
-                return e;
+            e = launch_up(upmix_tile_kernel<kOutY, kTerms>, up_grid, pdl, st, (const float*)nullptr,
+                          c.tm_lo, tm_wu, em, a.out_f32, a.out_bf16, a.out_fp16, has_P, a.T,
+                          c.s.status, sched, (int)pdl);
             break;
         case PrefillMode::kUnfused: {
-            if (cudaError_t e = launch_up(upmix_tile_kernel<kOutGated, 2>, up_grid, pdl, st, a.Rmix,
-                                          c.tm_lo, c.tm_wu, em, c.gated, (uint16_t*)nullptr,
-                                          (uint16_t*)nullptr, has_P, a.T, c.s.status,
-                                          c.s.sched + 2 * kSchedUp, (int)pdl))
-                return e;
+            e = launch_up(upmix_tile_kernel<kOutGated, kTerms>, up_grid, pdl, st, a.Rmix, c.tm_lo,
+                          tm_wu, em, c.gated, (uint16_t*)nullptr, (uint16_t*)nullptr, has_P, a.T,
+                          c.s.status, sched, (int)pdl);
+            if (e != cudaSuccess) return e;
             const int n = a.T * (kWidth / 4);
             const int mgrid = (n + 255) / 256 < 8 * c.sm_count ? (n + 255) / 256 : 8 * c.sm_count;
             mix_gated_kernel<<<mgrid, 256, 0, st>>>(c.gated, a.Rmix, a.out_f32, a.out_bf16,
@@ -1212,19 +1128,12 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
             break;
         }
     }
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-bool encode_w_up_bf16(CUtensorMap* map, const uint16_t* W_up, int box_rows) {
-    const cuuint64_t dims[2] = {kRank, kCols};
-    const cuuint64_t strides[1] = {kRank * 2};
-    const cuuint32_t box[2] = {kBK, (cuuint32_t)box_rows};
-    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W_up, 2, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
 cudaError_t launch_prefill(const Ctx& c, const ReadArgs& a, PrefillMode mode, cudaStream_t st) {
-    cudaError_t e = launch_prefill_down(c, a, mode, st);
+    cudaError_t e = launch_prefill_down(c, a, st);
     if (e != cudaSuccess) return e;
     return launch_prefill_upmix(c, a, mode, st, true);
 }

@@ -78,8 +78,7 @@ enum hc_status {
     HC_ERR_CUDA = -4,      /* a CUDA runtime call or a launch failed */
     HC_ERR_TIMEOUT = -5,   /* a bounded device-side wait gave up (status word) */
     HC_ERR_CHECK = -6,     /* hc_read_check found a mismatch */
-    HC_ERR_NOMEM = -7,     /* scratch allocation failed */
-    HC_ERR_RANGE = -8      /* a tile-path activation did not fit fp16 (status word) */
+    HC_ERR_NOMEM = -7      /* scratch allocation failed */
 };
 
 /* Which kernels run. HC_PATH_AUTO picks the decode kernels for T <= 32 (the measured
@@ -89,7 +88,9 @@ enum hc_path {
     HC_PATH_AUTO = 0,
     HC_PATH_DECODE = 1,            /* per 8 tokens: sliced down kernel (CUDA cores, clusters),
                                       then the up + gate + mix kernel (tcgen05) */
-    HC_PATH_PREFILL = 2,           /* tile down, fused up + gate + mix epilogue */
+    HC_PATH_PREFILL = 2,           /* tile down, fused up + gate + mix epilogue (tcgen05;
+                                      activations as three bf16 terms, fp32-accurate over
+                                      fp32's whole range, weights used as stored) */
     HC_PATH_PREFILL_UNFUSED = 3,   /* tile down, up GEMM writing gated, then the mix */
     HC_PATH_DECODE_ONE_KERNEL = 4, /* per 8 tokens: one kernel with an in-kernel lo exchange
                                       (HC_ERR_ARG where its 160 CTAs cannot all be resident) */
@@ -131,15 +132,15 @@ int hc_read_path(int path, int tokens,
 
 /* Runs again only the second half of the tile path for the tokens of the most
  * recent tile-path call on this context: the up projection on the lo that call left
- * in the context's scratch, with the gate and the 4x4 mix, as `path` says:
- * HC_PATH_PREFILL (fused epilogue), HC_PATH_PREFILL_UNFUSED (up GEMM writing gated,
- * then the mix) or HC_PATH_PREFILL_BF16_LO (one bf16 term, fused). The fp16 paths use
- * the fp16 copy of W_up made by that call and ignore W_up; the bf16 path reads W_up
- * (bf16, [10240][320]). R, P and Rmix must be that call's (or equal) tensors.
- * HC_ERR_ARG if the last tile-path call left lo in the other form or for fewer
- * tokens, or for any path but these three. Stage timing and the fused-versus-unfused
- * comparison use it; a read needs only hc_read. Otherwise the checks and errors of
- * hc_read. The pages have no counterpart of it. */
+ * in the context's scratch (as three bf16 terms, whatever the call's path), with the
+ * gate and the 4x4 mix, as `path` says: HC_PATH_PREFILL (fused epilogue),
+ * HC_PATH_PREFILL_UNFUSED (up GEMM writing gated, then the mix) or
+ * HC_PATH_PREFILL_BF16_LO (the first term alone, fused). W_up (bf16, [10240][320]) is
+ * read by all three. R, P, W_up and Rmix must be that call's (or equal) tensors.
+ * HC_ERR_ARG if the last tile-path call read fewer tokens (or none), or for any path
+ * but these three. Stage timing and the fused-versus-unfused comparison use it; a read
+ * needs only hc_read. Otherwise the checks and errors of hc_read. The pages have no
+ * counterpart of it. */
 int hc_read_upmix(int path, int tokens,
                   const float* R, const float* P, const uint16_t* W_up, const float* Rmix,
                   float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
@@ -160,12 +161,13 @@ int hc_read_y(int tokens,
               float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
               void* stream);
 
-/* Copies the bf16 lo ([tokens][320] bf16 bits, row-major) that the most recent
- * HC_PATH_PREFILL_BF16_LO call on this context fed to its up GEMM into lo_out
- * (device memory, 16-byte aligned, caller-owned), asynchronously on `stream`. It is
- * the stage input that checks of that path condition on. HC_ERR_ARG if the last
- * tile-path call was not HC_PATH_PREFILL_BF16_LO, tokens exceeds its token count, or
- * lo_out is null, misaligned or not device memory of the context's device. */
+/* Copies lo of the most recent tile-path call on this context, rounded once to bf16
+ * (round to nearest even; [tokens][320] bf16 bits, row-major), into lo_out (device
+ * memory, 16-byte aligned, caller-owned), asynchronously on `stream`. It is what the
+ * up GEMM of HC_PATH_PREFILL_BF16_LO takes as its A operand, the stage input that
+ * checks of that path condition on. HC_ERR_ARG if tokens exceeds the token count of
+ * that call (or there was none), or lo_out is null, misaligned or not device memory of
+ * the context's device. */
 int hc_read_lo_bf16(int tokens, uint16_t* lo_out, void* stream);
 
 /* Result of the once-per-device self check. */
@@ -191,10 +193,9 @@ typedef struct hc_check_report {
 int hc_read_check(int max_tokens, uint64_t seed, hc_check_report* rep);
 
 /* Waits for `stream`, then reads and clears the device status word of the current
- * device's context: HC_OK; HC_ERR_TIMEOUT if a bounded wait gave up since the last
- * call; HC_ERR_RANGE if the tile path met an activation it cannot represent (its
- * tensor-core operands carry R' * w_norm and lo as two fp16 terms, so they need
- * |R' * w_norm| < 65504 and |lo| < 65504). HC_ERR_CUDA if the stream itself
+ * device's context: HC_OK, or HC_ERR_TIMEOUT if a bounded wait gave up since the last
+ * call (the outputs of that call are then unspecified; the library resets its own
+ * schedulers, so the next call runs normally). HC_ERR_CUDA if the stream itself
  * reports an error. */
 int hc_read_status(void* stream);
 

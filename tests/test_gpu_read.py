@@ -288,31 +288,31 @@ def _host(o):
 
 def test_upmix_stage_rerun_matches_the_read(weights):
     """The up + gate + mix stage run again on the read's lo gives the read's bits,
-    fused and unfused, and on the bf16-lo path; a stage whose lo form does not
-    match the last tile-path call is refused."""
+    fused and unfused; on the same lo the bf16-lo stage gives the bits of a bf16-lo
+    read (every tile-path read leaves lo as its three bf16 terms, the first of which
+    is lo rounded once to bf16); a stage for more tokens than the last read is
+    refused."""
     w, W = weights
     T = 260
     a = synth.make_activations(14, T, True)
     R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+    ref16 = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL_BF16_LO)
     ref = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL)
     for path in (hc.HC_PATH_PREFILL, hc.HC_PATH_PREFILL_UNFUSED):
         o = alloc_out(T)
-        hc.hc_read_upmix(path, T, R, P, None, M, *o)
+        hc.hc_read_upmix(path, T, R, P, W["W_up"], M, *o)
         torch.cuda.synchronize()
         for x, y in zip(ref, _host(o)):
             assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
     o = alloc_out(T)
-    with pytest.raises(hc.HcReadError):
-        hc.hc_read_upmix(hc.HC_PATH_PREFILL_BF16_LO, T, R, P, W["W_up"], M, *o)
-    with pytest.raises(hc.HcReadError):
-        hc.hc_read_upmix(hc.HC_PATH_PREFILL, T + 1, R, P, None, M, *o)
-    ref16 = gpu_read(T, R, P, W, M, hc.HC_PATH_PREFILL_BF16_LO)
     hc.hc_read_upmix(hc.HC_PATH_PREFILL_BF16_LO, T, R, P, W["W_up"], M, *o)
     torch.cuda.synchronize()
     for x, y in zip(ref16, _host(o)):
         assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
     with pytest.raises(hc.HcReadError):
-        hc.hc_read_upmix(hc.HC_PATH_PREFILL, T, R, P, None, M, *o)
+        hc.hc_read_upmix(hc.HC_PATH_PREFILL, T + 1, R, P, W["W_up"], M, *o)
+    with pytest.raises(hc.HcReadError):
+        hc.hc_read_upmix(hc.HC_PATH_DECODE, T, R, P, W["W_up"], M, *o)
 
 
 def _bf16_lo(T):
@@ -490,7 +490,32 @@ def test_up_tile_repeats_bitwise_into_poisoned_outputs(weights):
     for rep in range(8):
         path = hc.HC_PATH_PREFILL_UNFUSED if rep % 2 == 0 else hc.HC_PATH_PREFILL
         o = _poisoned_out(T)
-        hc.hc_read_upmix(path, T, R, None, None, M, *o)
+        hc.hc_read_upmix(path, T, R, None, W["W_up"], M, *o)
+        for x, y in zip(ref, o):
+            assert bool(torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x,
+                                    y.view(torch.int32) if y.dtype == torch.float32 else y)), rep
+    assert hc.hc_read_status() == 0
+
+
+def test_readout_y_repeats_bitwise_into_poisoned_outputs(weights):
+    """The y read-out's epilogue releases each R slot as soon as it has read it, so the
+    slot's next TMA fill can land right after; four repeats of an 8,192-token read
+    into fresh poisoned outputs give the same bits (a read of the slot that the next
+    fill overtook would differ in that step's columns of one token)."""
+    w, W = weights
+    T = 8192
+    c = synth.make_prefill_chunk(103, T)
+    R = dev_f32(c["R"])
+    shape = (T, synth.WIDTH)
+    ref = None
+    for rep in range(4):
+        o = (torch.full(shape, float("nan"), dtype=torch.float32, device="cuda"),
+             torch.full(shape, -1, dtype=torch.int16, device="cuda"),
+             torch.full(shape, -1, dtype=torch.int16, device="cuda"))
+        hc.hc_read_y(T, R, None, W["w_norm"], W["W_down"], W["W_up"], *o)
+        if ref is None:
+            ref = o
+            continue
         for x, y in zip(ref, o):
             assert bool(torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else x,
                                     y.view(torch.int32) if y.dtype == torch.float32 else y)), rep
