@@ -75,10 +75,14 @@ constexpr int kDownSmem = kDownStages * kDownStageBytes + 1024;
 // upmix_tile
 constexpr int kUpCols = 64;            // output columns per tile (x 4 streams = N 256)
 constexpr int kUpN = kStreams * kUpCols;
-constexpr int kUpStages = 2;
-constexpr int kUpBBytes = kUpN * kBK * 2;         // 32 KB
-constexpr int kUpStageBytes = kTerms * kTileBytes16 + kUpBBytes;   // 80 KB
-constexpr int kUpKBlocks = kRank / kBK;           // 5
+// K blocks of 32 (one 64-byte swizzle row): three stages of 40 KB (three 8 KB lo
+// terms and 16 KB of W_up) leave room for three R slots per epilogue group below
+constexpr int kUpBK = 32;
+constexpr int kUpStages = 3;
+constexpr int kUpTileBytes = kTileM * kUpBK * 2;  // 8 KB: one 128 x 32 bf16 lo term
+constexpr int kUpBBytes = kUpN * kUpBK * 2;       // 16 KB
+constexpr int kUpStageBytes = kTerms * kUpTileBytes + kUpBBytes;   // 40 KB
+constexpr int kUpKBlocks = kRank / kUpBK;         // 10
 constexpr int kUpColTiles = kWidth / kUpCols;     // 40
 // Eight epilogue warps: two per TMEM lane quarter (32 tokens), one for each half of
 // the tile's steps. The epilogue takes its tile in steps of 8 columns; a dedicated
@@ -110,11 +114,8 @@ constexpr int kRSlot = kStreams * kTileM * kEpiCols * 4;        // 16 KB
 // warp that waits on a slot's barrier consumes every fill of that slot. (With one
 // ring shared by both groups a warp a tile ahead of the other group could wait on
 // a slot whose previous fill, for the other group, was still in flight, and its
-// parity wait would take the fill before that one as complete.) Two slots a group:
-// with the three-term operand stages, shared memory holds no more. Without a
-// pending write one step's R is loaded while the previous one is consumed; with
-// one, a step takes both slots (R, then P).
-constexpr int kRSlotsPerGroup = 2;
+// parity wait would take the fill before that one as complete.)
+constexpr int kRSlotsPerGroup = 3;
 constexpr int kRSlots = 2 * kRSlotsPerGroup;
 constexpr int kUpSmem = kUpStages * kUpStageBytes + kRSlots * kRSlot + 1024;
 static_assert(kUpSmem <= 227 * 1024 - 1024, "up tile shared memory");
@@ -634,8 +635,8 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
-    auto sA = [&](int slot, int term) { return smem + slot * kUpStageBytes + term * kTileBytes16; };
-    auto sB = [&](int slot) { return smem + slot * kUpStageBytes + kTerms * kTileBytes16; };
+    auto sA = [&](int slot, int term) { return smem + slot * kUpStageBytes + term * kUpTileBytes; };
+    auto sB = [&](int slot) { return smem + slot * kUpStageBytes + kTerms * kUpTileBytes; };
     uint8_t* rring = smem + kUpStages * kUpStageBytes;
     // the CTA's i-th tile from the queue (n_tiles: no more tiles, or the CTA gave up)
     auto take_tile = [&](int i) -> int {
@@ -669,10 +670,10 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     const int slot = it % kUpStages;
                     const uint32_t ph = (it / kUpStages) & 1;
                     if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
-                    mbar_arrive_expect_tx(&full_bar[slot], kLoTerms * kTileBytes16 + kUpBBytes);
+                    mbar_arrive_expect_tx(&full_bar[slot], kLoTerms * kUpTileBytes + kUpBBytes);
 #pragma unroll
                     for (int s = 0; s < kStreams; ++s)
-                        tma_load_2d_hint(sB(slot) + s * (kUpBBytes / kStreams), &tm_wu, kb * kBK,
+                        tma_load_2d_hint(sB(slot) + s * (kUpBBytes / kStreams), &tm_wu, kb * kUpBK,
                                          s * kWidth + ct * kUpCols, &full_bar[slot], keep);
                     if (!lo_ready) {
                         pdl_wait();
@@ -682,7 +683,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     }
 #pragma unroll
                     for (int term = 0; term < kLoTerms; ++term)
-                        tma_load_3d_hint(sA(slot, term), &tm_lo, kb * kBK, tt * kTileM, term,
+                        tma_load_3d_hint(sA(slot, term), &tm_lo, kb * kUpBK, tt * kTileM, term,
                                          &full_bar[slot], keep);
                 }
             }
@@ -709,9 +710,9 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     for (int term = 0; term < kLoTerms; ++term) {
                         const uint32_t a0 = smem_u32(sA(slot, term));
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk)
-                            mma_f16(tmem + b * kUpN, desc_sw128(a0 + kk * 32),
-                                    desc_sw128(b0 + kk * 32), idesc, (kb | term | kk) != 0);
+                        for (int kk = 0; kk < kUpBK / 16; ++kk)
+                            mma_f16(tmem + b * kUpN, desc_sw64(a0 + kk * 32),
+                                    desc_sw64(b0 + kk * 32), idesc, (kb | term | kk) != 0);
                     }
                     mma_commit(&empty_bar[slot]);
                 }
@@ -813,11 +814,15 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
 #pragma unroll
                             for (int e = 0; e < kEpiCols; ++e) rp[s][e] = which ? rp[s][e] + x[e] : x[e];
                         }
-                        // the next fill of this slot is a TMA write (async proxy): order
-                        // this lane's generic reads of the slot before it, then release
-                        fence_proxy_async_smem();
+                        // the next fill of this slot is a TMA write (async proxy): a slot
+                        // released right after these reads orders them before it with a
+                        // proxy fence. (The mix's R slot is released later, after the TMA
+                        // store of the outputs written into it, behind the fence that
+                        // precedes that store.)
+                        const bool release_now = !(kTmaOut && which == 0);
+                        if (release_now) fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0 && !(kTmaOut && which == 0)) mbar_arrive(&r_empty[slot]);
+                        if (lane == 0 && release_now) mbar_arrive(&r_empty[slot]);
                     }
                     if (!ok) break;
 #pragma unroll
@@ -1003,6 +1008,16 @@ bool encode_w_down_bf16(CUtensorMap* map, const uint16_t* W_down) {
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The caller's W_up [kCols][kRank] bf16 in boxes of 32 K x 64 rows, 64-byte swizzled:
+// one stream's part of an up tile's B operand per box.
+bool encode_w_up_sw64(CUtensorMap* map, const uint16_t* W_up) {
+    const cuuint64_t dims[2] = {kRank, kCols};
+    const cuuint64_t strides[1] = {kRank * 2};
+    const cuuint32_t box[2] = {kUpBK, kUpCols};
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W_up, 2, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 }  // namespace
 
 bool encode_w_up_bf16(CUtensorMap* map, const uint16_t* W_up, int box_rows) {
@@ -1015,13 +1030,14 @@ bool encode_w_up_bf16(CUtensorMap* map, const uint16_t* W_up, int box_rows) {
 
 cudaError_t prefill_setup(Ctx& c) {
     // lo's three bf16 terms [3][max_tokens][kRank] in the library's scratch: the up
-    // tile's A operand, in boxes of 64 K x 128 tokens x 1 term (fixed for the context)
+    // tile's A operand, in boxes of 32 K x 128 tokens x 1 term, 64-byte swizzled (fixed
+    // for the context)
     {
         const cuuint64_t dims[3] = {kRank, (cuuint64_t)c.max_tokens, kTerms};
         const cuuint64_t strides[2] = {kRank * 2, (cuuint64_t)c.max_tokens * kRank * 2};
-        const cuuint32_t box[3] = {kBK, kTileM, 1};
+        const cuuint32_t box[3] = {kUpBK, kTileM, 1};
         if (!encode_map(&c.tm_lo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c.lo3, 3, dims, strides, box,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+                        CU_TENSOR_MAP_SWIZZLE_64B))
             return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaFuncSetAttribute(down_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1088,7 +1104,7 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
     const int up_grid = up_tiles < c.sm_count ? up_tiles : c.sm_count;
     EpiMaps em;
     CUtensorMap tm_wu;
-    bool ok = encode_w_up_bf16(&tm_wu, a.W_up, kUpCols);
+    bool ok = encode_w_up_sw64(&tm_wu, a.W_up);
     ok = ok && encode_act(&em.R, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.R, a.T, kEpiCols, kTileM);
     ok = ok && encode_act(&em.P, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.P ? a.P : a.R, a.T,
                           kEpiCols, kTileM);

@@ -197,6 +197,19 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     return d;
 }
 
+// The same for a K-major tile stored with the 64-byte swizzle: rows of 64 bytes (32
+// 16-bit elements of K), 8-row atoms of 512 bytes. The tile must start on a 512-byte
+// boundary; a K step of 16 elements advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);   // start address
+    d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused)
+    d |= static_cast<uint64_t>(512 >> 4) << 32;            // stride byte offset: 8 rows
+    d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
+    d |= static_cast<uint64_t>(4) << 61;                   // 64-byte swizzle
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: fp16 A and B (K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
