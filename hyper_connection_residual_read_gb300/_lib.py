@@ -35,7 +35,7 @@ STREAMS, WIDTH, RANK = 4, 2560, 320
 # every symbol include/hc_read.h declares
 EXPORTS = ("hc_read_init", "hc_read", "hc_read_path", "hc_read_check", "hc_read_status",
            "hc_read_strerror", "hc_read_shutdown", "hc_read_version", "hc_read_noalloc",
-           "hc_read_upmix", "hc_read_lo_bf16", "hc_read_y")
+           "hc_read_upmix", "hc_read_lo_bf16", "hc_read_y", "hc_read_set_wait_limit")
 
 
 class HcReadError(RuntimeError):
@@ -101,6 +101,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_read_y.restype = i32
     lib.hc_read_lo_bf16.argtypes = [i32, vp, vp]
     lib.hc_read_lo_bf16.restype = i32
+    lib.hc_read_set_wait_limit.argtypes = [u64]
+    lib.hc_read_set_wait_limit.restype = i32
     _lib = lib
     return lib
 
@@ -196,6 +198,12 @@ def hc_read_check(max_tokens: int = 8, seed: int = 0) -> tuple[int, dict]:
     rep = hc_check_report()
     code = load().hc_read_check(max_tokens, seed, ctypes.byref(rep))
     return code, rep.as_dict()
+
+
+def hc_read_set_wait_limit(ns: int) -> None:
+    """Bound of the one-kernel decode read's wait for the other CTAs' lo, in ns (0:
+    the default, 2 s). Tests of failure detection shorten it."""
+    _check("hc_read_set_wait_limit", load().hc_read_set_wait_limit(ns))
 
 
 def hc_read_status(stream=None) -> int:

@@ -354,6 +354,14 @@ extern "C" int hc_read_lo_bf16(int tokens, uint16_t* lo_out, void* stream) {
                : HC_ERR_CUDA;
 }
 
+extern "C" int hc_read_set_wait_limit(uint64_t ns) {
+    int err;
+    Ctx* c = current_ctx(&err);
+    if (!c) return err;
+    c->lo_wait_ns = ns > 0 ? ns : kDefaultWaitNs;
+    return HC_OK;
+}
+
 extern "C" int hc_read_status(void* stream) {
     int err;
     Ctx* c = current_ctx(&err);

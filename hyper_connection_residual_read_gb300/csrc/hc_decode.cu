@@ -261,7 +261,8 @@ constexpr int kTcSmem = kTcKBlocks * kTcABytes + kTcKBlocks * kTcBBytesMax + 102
 constexpr int kTcTmemCols = 32;                      // the smallest TMEM allocation
 
 // A bounded wait on an mbarrier phase: false after 2 s, with the timeout recorded in
-// the status word when there is one (the allocation-free entry has none).
+// the status word when there is one (the allocation-free entry has none; the kernel
+// then writes NaN outputs).
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int* status) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = tc::globaltimer();
@@ -396,16 +397,17 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
     }
     tc::tc_fence_before();
     __syncthreads();
-    if (ok) {
 #pragma unroll
-        for (int t = 0; t < T; ++t) {
-            const float m = mix_row(&m_s[t][warp * 4], g_s[t][0][lane], g_s[t][1][lane],
-                                    g_s[t][2][lane], g_s[t][3][lane]);
-            const size_t off = (size_t)t * kCols + warp * kWidth + c;
-            out_f32[off] = m;
-            out_bf16[off] = to_bf16_bits(m);
-            out_fp16[off] = to_fp16_bits(m);
-        }
+    for (int t = 0; t < T; ++t) {
+        // a CTA whose wait gave up writes NaN, so that even a caller without a status
+        // word (the allocation-free entry) finds no stale values in its outputs
+        const float m = ok ? mix_row(&m_s[t][warp * 4], g_s[t][0][lane], g_s[t][1][lane],
+                                     g_s[t][2][lane], g_s[t][3][lane])
+                           : __int_as_float(0x7fc00000);
+        const size_t off = (size_t)t * kCols + warp * kWidth + c;
+        out_f32[off] = m;
+        out_bf16[off] = to_bf16_bits(m);
+        out_fp16[off] = to_fp16_bits(m);
     }
     if (warp == 0) {
         tc::tc_fence_after();

@@ -23,7 +23,9 @@
 // All CTAs are resident before any of them waits: a dependent launch cannot start
 // until every CTA of this grid has issued launch_dependents, and the previous
 // kernel on the stream finishes on its own. A wait that still runs out of time
-// records a timeout in the device status word and the CTA goes on without lo.
+// (after the context's bound, 2 s unless a test shortened it) records a timeout in
+// the device status word and the CTA goes on without lo; the exchange counters may
+// then be left mid-count, and hc_read_status, which reports the timeout, resets them.
 #include <cooperative_groups.h>
 
 #include "hc_common.cuh"
@@ -40,7 +42,7 @@ constexpr int kCtas = kDownSlices * kDownRowBlocks;   // 160
 constexpr int kUpColsPerCta = kWidth / kCtas;         // 16
 constexpr int kParts = 16;                 // up: 16 lanes per column, 20 inputs each
 constexpr int kPartLen = kRank / kParts;   // 20
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kWaitNs = 2000000000ull;   // bound of the bulk-copy wait
 constexpr int kWupBytes = kStreams * kUpColsPerCta * kRank * 2;   // 40 KB
 
 constexpr int dyn_smem(int T) { return kWupBytes + T * kDownSliceCols * 4 + T * kRank * 4; }
@@ -86,7 +88,7 @@ __global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kThreads, 
 decode_fused_kernel(const float* R, const float* P, const uint16_t* __restrict__ w_norm,
                     const uint16_t* __restrict__ W_down, const uint16_t* __restrict__ W_up,
                     const float* Rmix, float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
-                    float* lo, unsigned* sync, float eps, int* status) {
+                    float* lo, unsigned* sync, float eps, int* status, uint64_t lo_wait_ns) {
     namespace cg = cooperative_groups;
     const int sl = blockIdx.x, rb = blockIdx.y;
     const int cid = rb * kDownSlices + sl;                 // 0..159
@@ -261,7 +263,7 @@ decode_fused_kernel(const float* R, const float* P, const uint16_t* __restrict__
         if (ld_acquire(&sync[0]) < (unsigned)kCtas) {
             const uint64_t t0 = gtimer();
             while (ld_acquire(&sync[0]) < (unsigned)kCtas) {
-                if (gtimer() - t0 > kWaitNs) {
+                if (gtimer() - t0 > lo_wait_ns) {
                     atomicOr(status, kStatusTimeout);
                     ok = 0;
                     break;
@@ -384,7 +386,7 @@ cudaError_t launch_fused_chunk(const Ctx& ctx, const ReadArgs& a, int t0, cudaSt
                       dyn_smem(T), st, a.R + off, a.P ? a.P + off : nullptr, a.w_norm, a.W_down, a.W_up,
                       a.Rmix + (size_t)t0 * 16, a.out_f32 + off, a.out_bf16 + off,
                       a.out_fp16 + off, ctx.s.lo + (size_t)t0 * kRank, ctx.s.sync, ctx.eps,
-                      ctx.s.status);
+                      ctx.s.status, ctx.lo_wait_ns);
 }
 
 template <int T>

@@ -34,6 +34,8 @@ constexpr int kSchedPairs = 2;
 
 // Device status word bits.
 constexpr int kStatusTimeout = 1;
+// Bound of a device-side wait on other CTAs before it gives up and reports a timeout.
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
 
 struct Scratch {
     float* lo = nullptr;             // [max_tokens][kRank], the down projection's output
@@ -52,6 +54,9 @@ struct Ctx {
     float eps = 1e-6f;
     int sm_count = 0;
     bool fused_decode = false;       // the one-kernel decode read can run on this device
+    // bound of the one-kernel decode read's wait for every CTA's lo (a test may shorten
+    // it to make the wait run out; hc_read_set_wait_limit)
+    uint64_t lo_wait_ns = kDefaultWaitNs;
     char name[64] = {0};
     Scratch s;
     // prefill scratch

@@ -13,6 +13,7 @@
 // kept in a file-scope __device__ array of fixed size. The CUDA runtime reserves
 // that array on every device that loads this library, and it stays there until the
 // process exits; the library itself allocates nothing on this path.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -30,22 +31,69 @@ constexpr int kNoAllocMaxDevices = 64;
 // writes every value the up kernel then reads.
 static __device__ __align__(256) float g_noalloc_lo[kNoAllocMaxTokens * kRank];
 
+// Per device: the device address of g_noalloc_lo, valid for the CUDA context it was
+// looked up in (identified by the driver's context ID, never reused within a
+// process). A reset of the device creates a new context, in which the module, and so
+// the array, may sit elsewhere: the next call then looks the address up again. Only
+// a successful set-up is remembered.
 struct DeviceScratch {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
-    float* lo = nullptr;   // device address of g_noalloc_lo on this device
+    std::mutex m;
+    unsigned long long ctx_id = 0;
+    float* lo = nullptr;
 };
 DeviceScratch g_scratch[kNoAllocMaxDevices];
 
-// In host code g_noalloc_lo names a host-side stand-in, not device memory: the
-// device address must be looked up once per device, with that device current.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The driver's ID of the calling thread's current context (0 if it cannot be read).
+unsigned long long current_ctx_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+        ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// In host code g_noalloc_lo names a host-side stand-in, not device memory: the device
+// address is looked up with the device current, once per device and context. The
+// same first call sets the decode kernels' shared-memory attributes for every chunk
+// size (1-8 tokens), so that no later call, with any token count, changes a kernel
+// attribute: one call on a device before any stream capture is enough.
 float* scratch_for(int device, cudaError_t* err) {
     DeviceScratch& d = g_scratch[device];
-    std::call_once(d.once, [&d] {
-        d.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.lo), g_noalloc_lo);
-    });
-    *err = d.err;
-    return d.err == cudaSuccess ? d.lo : nullptr;
+    std::lock_guard<std::mutex> lock(d.m);
+    const unsigned long long id = current_ctx_id();
+    if (d.lo != nullptr && id != 0 && id == d.ctx_id) {
+        *err = cudaSuccess;
+        return d.lo;
+    }
+    float* lo = nullptr;
+    if ((*err = cudaGetSymbolAddress(reinterpret_cast<void**>(&lo), g_noalloc_lo)) != cudaSuccess ||
+        (*err = decode_setup(device)) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    d.lo = lo;
+    // the lookup has made the context current if it was not; an ID of 0 (unreadable)
+    // means the address is looked up again on every call
+    d.ctx_id = current_ctx_id();
+    return lo;
 }
 
 bool device_ptr_ok(const void* p, int device) {

@@ -199,6 +199,18 @@ int hc_read_check(int max_tokens, uint64_t seed, hc_check_report* rep);
  * reports an error. */
 int hc_read_status(void* stream);
 
+/* Sets the bound of the one-kernel decode read's device-side wait for the other
+ * CTAs' lo (HC_PATH_DECODE_ONE_KERNEL) on the current device's context, in
+ * nanoseconds; 0 restores the default of 2 s. Failure-detection tests shorten it so
+ * that the wait runs out: the read then returns, hc_read_status reports
+ * HC_ERR_TIMEOUT and resets the exchange counters, and the next read runs normally.
+ * Only this wait, which has no copy in flight, is affected. The pages' persistent
+ * read has the same kind of bound ("#2226 STRATA_HC_PERSIST=1 (opt-in, HIP): the
+ * verifier's hyper-connection read as one persistent kernel", "What changed": a
+ * barrier timeout after which the read falls back). HC_ERR_NOT_INIT without a
+ * context. */
+int hc_read_set_wait_limit(uint64_t ns);
+
 /* Static description of a status code. */
 const char* hc_read_strerror(int code);
 
@@ -219,11 +231,17 @@ void hc_read_shutdown(void);
  * cudaFree or other allocating routine. Returns HC_ERR_ARG for tokens > 64 or the
  * pointer errors hc_read refuses, HC_ERR_ARCH off sm_103, HC_ERR_CUDA otherwise.
  *
- * The first call on a device (with that device current) looks up the array's
- * device address and sets the decode kernels' shared-memory attributes for each
- * token count it meets; make those first calls before any stream capture. Every call
- * on a device shares the one array: calls that may overlap on the GPU (on
- * different streams without ordering between them) race and must not be made. */
+ * The first call with tokens >= 1 on a device (with that device current) looks up
+ * the array's device address and sets the decode kernels' shared-memory attributes
+ * for every chunk size, so that one such call before any stream capture is enough
+ * for calls of any token count after it. After a device reset (a new CUDA context)
+ * the next call does that set-up again. Every call on a device shares the one array:
+ * calls that may overlap on the GPU (on different streams without ordering between
+ * them) race and must not be made.
+ *
+ * This entry has no device status word. If one of its bounded device waits gives up
+ * (after 2 s, which only a stalled device causes), the kernels write NaN into the
+ * outputs of the tokens concerned instead of leaving stale values there. */
 int hc_read_noalloc(int tokens,
                     const float* R, const float* P,
                     const uint16_t* w_norm, const uint16_t* W_down, const uint16_t* W_up,
