@@ -78,11 +78,23 @@ __device__ __forceinline__ float warp_reduce_8rows(const float (&v)[8], int lane
     return c;
 }
 
-template <int T>
-__global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kDownThreads)
+// T: tokens per chunk. The kernel reads its slice of W_down from HBM once and runs
+// the call's ntok tokens (at most 64) through it in chunks of T (the last chunk may
+// hold fewer). Each chunk stages its activations, takes the dot products and keeps
+// the CTA's partial of each token in shared memory; one exchange in the cluster then
+// finishes every token. kMulti = false: exactly one chunk (ntok == T). kMulti = true:
+// several; after its dot products each chunk loads the CTA's 40 KB slice of W_down
+// again for the next one, from L2, where the first load left it (holding the weights
+// in registers across a chunk would spill at the two-CTAs-per-SM register budget).
+// The staged activations live in dynamic shared memory: T x 5 KB.
+constexpr int kMultiMaxT = 64;   // tokens of one multi-chunk pass at most
+
+template <int T, bool kMulti>
+__global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kDownThreads, 2)
 down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w_norm,
-                  const uint16_t* __restrict__ W_down, float* lo, float eps) {
+                  const uint16_t* __restrict__ W_down, float* lo, float eps, int ntok_run) {
     namespace cg = cooperative_groups;
+    constexpr int NT = kMulti ? kMultiMaxT : T;   // tokens the exchange holds at most
     const int sl = blockIdx.x;                 // K slice 0..7 == rank in the cluster
     const int rb = blockIdx.y;                 // row block 0..19 == the cluster
     const int s = sl >> 1;                     // stream of the slice
@@ -93,6 +105,7 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
     const int rg = warp / kDownColGroups, cgp = warp % kDownColGroups;
     const int j0 = rb * kDownRowsPerCta + rg * 8;
     const int col = cgp * 256 + lane * 8;      // this lane's 8 columns within the slice
+    const int ntok = kMulti ? ntok_run : T;
 
     // 1. weights first (layer parameters may be read before the previous kernel
     //    on the stream has finished): 8 rows x 8 columns, one 16-byte load per row
@@ -105,9 +118,8 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
     // finds every CTA of the cluster started (their shared memory exists)
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     // the activations into L2 while the previous kernel finishes (read after the wait)
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-        if ((tid & 7) == 0) {   // one prefetch per 128-byte line
+    if ((tid & 7) == 0) {   // one prefetch per 128-byte line
+        for (int t = 0; t < ntok; ++t) {
             prefetch_l2(R + (size_t)t * kCols + k0 + 4 * tid);
             if (P != nullptr) prefetch_l2(P + (size_t)t * kCols + k0 + 4 * tid);
         }
@@ -115,114 +127,144 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
     pdl_launch_dependents();
     pdl_wait();
 
-    // 2. activations a = R' * w_norm (fp32) and per-token sums of squares of R'.
-    //    Smem layout: a lane's 8 columns are stored as two float4 runs, 128 floats
-    //    apart, so that consecutive lanes read consecutive 16-byte words.
-    __shared__ float4 a_s[T][kDownSliceCols / 4];
+    // staged activations a = R' * w_norm of a chunk. Layout: a lane's 8 columns are
+    // stored as two float4 runs, 128 floats apart, so that consecutive lanes read
+    // consecutive 16-byte words.
+    extern __shared__ float4 a_dyn[];
+    auto a_s = reinterpret_cast<float4 (*)[kDownSliceCols / 4]>(a_dyn);
     __shared__ float red_ss[kDownThreads / 32][T];
     __shared__ float red[T][kDownColGroups][kDownRowsPerCta];
-    __shared__ float ss_s[T];                      // this slice's sums of squares
-    __shared__ float inbox[kDownSlices][T][3];     // pushed by each slice: 2 partials, ss
-
-    float4 xs[T];
-#pragma unroll
-    for (int t = 0; t < T; ++t)
-        xs[t] = *reinterpret_cast<const float4*>(R + (size_t)t * kCols + k0 + 4 * tid);
-    if (P != nullptr) {
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-            const float4 p = *reinterpret_cast<const float4*>(P + (size_t)t * kCols + k0 + 4 * tid);
-            xs[t].x += p.x; xs[t].y += p.y; xs[t].z += p.z; xs[t].w += p.w;
-        }
-    }
+    __shared__ float part[NT][kDownRowsPerCta];    // this slice's partial of each token
+    __shared__ float ss_p[NT];                     // this slice's sums of squares
+    __shared__ float inbox[kDownSlices][NT][3];    // pushed by each slice: 2 partials, ss
     const float w0 = bf16_lo(wn.x), w1 = bf16_hi(wn.x), w2 = bf16_lo(wn.y), w3 = bf16_hi(wn.y);
-    {
-        const int c = 4 * tid;                       // first of this thread's 4 columns
-        const int scg = c >> 8, slane = (c & 255) >> 3, half = (c & 7) >> 2;
-        const int slot = scg * 64 + half * 32 + slane;   // float4 index
-        // all tokens' sums over the warp in one 8-row reduce-scatter: 9 shuffles for
-        // any T instead of 5 per token (measured: T = 8 10.23 -> 9.81 us per read).
-        // It pairs lanes at the same distances as a per-token xor butterfly, so each
-        // token's sum has the same bits, and no token's tree depends on the others.
-        float ssv[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) ssv[t] = 0.f;
-#pragma unroll
-        for (int t = 0; t < T; ++t) {
-            const float4 x = xs[t];
-            float ss = x.x * x.x;
-            ss = fmaf(x.y, x.y, ss);
-            ss = fmaf(x.z, x.z, ss);
-            ss = fmaf(x.w, x.w, ss);
-            a_s[t][slot] = make_float4(x.x * w0, x.y * w1, x.z * w2, x.w * w3);
-            ssv[t] = ss;
-        }
-        const float ssum = warp_reduce_8rows(ssv, lane);
-        const int tr = (lane >> 2) & 7;
-        if ((lane & 3) == 0 && tr < T) red_ss[warp][tr] = ssum;
-    }
-    __syncthreads();
-    if (tid < T) {
-        float ss = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDownThreads / 32; ++w) ss += red_ss[w][tid];
-        ss_s[tid] = ss;
-    }
 
-    // 3. partial dots of 8 rows over this lane's 8 columns, reduced over the warp
-    float wf[8][8];
+#pragma unroll 1
+    for (int tc0 = 0; tc0 < ntok; tc0 += T) {
+        const int nt = ntok - tc0 < T ? ntok - tc0 : T;   // tokens of this chunk
+        const float* Rc = R + (size_t)tc0 * kCols;
+        const float* Pc = P != nullptr ? P + (size_t)tc0 * kCols : nullptr;
+
+        // 2. activations and per-token sums of squares of R' (zero past the chunk's
+        //    tokens)
+        float4 xs[T];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        wf[r][0] = bf16_lo(wv[r].x); wf[r][1] = bf16_hi(wv[r].x);
-        wf[r][2] = bf16_lo(wv[r].y); wf[r][3] = bf16_hi(wv[r].y);
-        wf[r][4] = bf16_lo(wv[r].z); wf[r][5] = bf16_hi(wv[r].z);
-        wf[r][6] = bf16_lo(wv[r].w); wf[r][7] = bf16_hi(wv[r].w);
-    }
+        for (int t = 0; t < T; ++t)
+            xs[t] = t < nt ? *reinterpret_cast<const float4*>(Rc + (size_t)t * kCols + k0 + 4 * tid)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Pc != nullptr) {
 #pragma unroll
-    for (int t = 0; t < T; ++t) {
-        const float4 x0 = a_s[t][cgp * 64 + lane];
-        const float4 x1 = a_s[t][cgp * 64 + 32 + lane];
-        float acc[8];
+            for (int t = 0; t < T; ++t) {
+                if (t >= nt) continue;
+                const float4 p = *reinterpret_cast<const float4*>(Pc + (size_t)t * kCols + k0 + 4 * tid);
+                xs[t].x += p.x; xs[t].y += p.y; xs[t].z += p.z; xs[t].w += p.w;
+            }
+        }
+        {
+            const int c = 4 * tid;                       // first of this thread's 4 columns
+            const int scg = c >> 8, slane = (c & 255) >> 3, half = (c & 7) >> 2;
+            const int slot = scg * 64 + half * 32 + slane;   // float4 index
+            // all tokens' sums over the warp in one 8-row reduce-scatter: 9 shuffles for
+            // any T instead of 5 per token (measured: T = 8 10.23 -> 9.81 us per read).
+            // It pairs lanes at the same distances as a per-token xor butterfly, so each
+            // token's sum has the same bits, and no token's tree depends on the others.
+            float ssv[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) ssv[t] = 0.f;
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                const float4 x = xs[t];
+                float ss = x.x * x.x;
+                ss = fmaf(x.y, x.y, ss);
+                ss = fmaf(x.z, x.z, ss);
+                ss = fmaf(x.w, x.w, ss);
+                a_s[t][slot] = make_float4(x.x * w0, x.y * w1, x.z * w2, x.w * w3);
+                ssv[t] = ss;
+            }
+            const float ssum = warp_reduce_8rows(ssv, lane);
+            const int tr = (lane >> 2) & 7;
+            if ((lane & 3) == 0 && tr < T) red_ss[warp][tr] = ssum;
+        }
+        __syncthreads();
+        if (tid < T && tid < nt) {
+            float ss = 0.f;
+#pragma unroll
+            for (int w = 0; w < kDownThreads / 32; ++w) ss += red_ss[w][tid];
+            ss_p[tc0 + tid] = ss;
+        }
+
+        // 3. partial dots of 8 rows over this lane's 8 columns, reduced over the warp
+        float wf[8][8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-            float v = wf[r][0] * x0.x;
-            v = fmaf(wf[r][1], x0.y, v);
-            v = fmaf(wf[r][2], x0.z, v);
-            v = fmaf(wf[r][3], x0.w, v);
-            v = fmaf(wf[r][4], x1.x, v);
-            v = fmaf(wf[r][5], x1.y, v);
-            v = fmaf(wf[r][6], x1.z, v);
-            v = fmaf(wf[r][7], x1.w, v);
-            acc[r] = v;
+            wf[r][0] = bf16_lo(wv[r].x); wf[r][1] = bf16_hi(wv[r].x);
+            wf[r][2] = bf16_lo(wv[r].y); wf[r][3] = bf16_hi(wv[r].y);
+            wf[r][4] = bf16_lo(wv[r].z); wf[r][5] = bf16_hi(wv[r].z);
+            wf[r][6] = bf16_lo(wv[r].w); wf[r][7] = bf16_hi(wv[r].w);
         }
-        const float sum = warp_reduce_8rows(acc, lane);
-        if ((lane & 3) == 0) red[t][cgp][rg * 8 + ((lane >> 2) & 7)] = sum;
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+            const float4 x0 = a_s[t][cgp * 64 + lane];
+            const float4 x1 = a_s[t][cgp * 64 + 32 + lane];
+            float acc[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                float v = wf[r][0] * x0.x;
+                v = fmaf(wf[r][1], x0.y, v);
+                v = fmaf(wf[r][2], x0.z, v);
+                v = fmaf(wf[r][3], x0.w, v);
+                v = fmaf(wf[r][4], x1.x, v);
+                v = fmaf(wf[r][5], x1.y, v);
+                v = fmaf(wf[r][6], x1.z, v);
+                v = fmaf(wf[r][7], x1.w, v);
+                acc[r] = v;
+            }
+            const float sum = warp_reduce_8rows(acc, lane);
+            if ((lane & 3) == 0) red[t][cgp][rg * 8 + ((lane >> 2) & 7)] = sum;
+        }
+        if constexpr (kMulti) {
+            // the next chunk's weights, from L2: issued here, where few registers are
+            // live, so that they arrive while this chunk is summed and the next staged
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                wv[r] = *reinterpret_cast<const uint4*>(W_down + (size_t)(j0 + r) * kCols + k0 + col);
+        }
+        __syncthreads();
+        // this slice's partial for each of its 16 rows: column groups summed in order
+        if (tid < T * kDownRowsPerCta && tid / kDownRowsPerCta < nt) {
+            const int t = tid / kDownRowsPerCta, j = tid % kDownRowsPerCta;
+            float v = red[t][0][j];
+#pragma unroll
+            for (int g = 1; g < kDownColGroups; ++g) v += red[t][g][j];
+            part[tc0 + t][j] = v;
+        }
+        // (the next chunk writes red and a_s only after the barrier that follows its
+        // staging, which every thread reaches after these reads)
     }
     __syncthreads();
 
-    // 4. this slice's partial for its 16 rows, column groups summed in order, pushed
-    //    into the shared memory of the CTA that finishes the row: CTA d finishes rows
-    //    2d and 2d+1 of the block and receives, from every slice r, those two
-    //    partials and r's sums of squares. Remote stores need no round trip, and after
-    //    the one cluster barrier that publishes them no CTA touches another's memory.
+    // 4. the partials pushed into the shared memory of the CTA that finishes the row:
+    //    CTA d finishes rows 2d and 2d+1 of the block and receives, from every slice
+    //    r, those two partials and r's sums of squares, for every token. Remote stores
+    //    need no round trip, and after the one cluster barrier that publishes them no
+    //    CTA touches another's memory. The wait first: every CTA of the cluster has
+    //    started.
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     cg::cluster_group cluster = cg::this_cluster();
-    if (tid < T * kDownRowsPerCta) {
-        const int t = tid / kDownRowsPerCta, j = tid % kDownRowsPerCta;
-        float v = red[t][0][j];
-#pragma unroll
-        for (int g = 1; g < kDownColGroups; ++g) v += red[t][g][j];
-        *cluster.map_shared_rank(&inbox[sl][t][j & 1], j >> 1) = v;
-    } else if (tid >= 128 && tid < 128 + T * kDownSlices) {
-        const int t = (tid - 128) / kDownSlices, d = (tid - 128) % kDownSlices;
-        *cluster.map_shared_rank(&inbox[sl][t][2], d) = ss_s[t];
+    for (int i = tid; i < ntok * kDownRowsPerCta; i += kDownThreads) {
+        const int t = i / kDownRowsPerCta, j = i % kDownRowsPerCta;
+        *cluster.map_shared_rank(&inbox[sl][t][j & 1], j >> 1) = part[t][j];
+    }
+    for (int i = tid; i < ntok * kDownSlices; i += kDownThreads) {
+        const int t = i / kDownSlices, d = i % kDownSlices;
+        *cluster.map_shared_rank(&inbox[sl][t][2], d) = ss_p[t];
     }
     cluster.sync();
 
     // 5. CTA `sl` finishes rows 2*sl and 2*sl+1 of the block, summing the slices of
     //    each stream in order and applying that stream's rs
-    if (tid < T * 2) {
-        const int t = tid >> 1, jj = tid & 1;
+    for (int i = tid; i < ntok * 2; i += kDownThreads) {
+        const int t = i >> 1, jj = i & 1;
         float v = 0.f;
 #pragma unroll
         for (int st = 0; st < kStreams; ++st) {
@@ -231,34 +273,46 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
             const float d = inbox[2 * st][t][jj] + inbox[2 * st + 1][t][jj];
             v = fmaf(rs, d, v);
         }
-        lo[t * kRank + rb * kDownRowsPerCta + 2 * sl + jj] = v;
+        lo[(size_t)t * kRank + rb * kDownRowsPerCta + 2 * sl + jj] = v;
     }
 }
 
+// Dynamic shared memory of down_slice_kernel<T, ...>: the staged activations.
+template <int T> constexpr int kDownDynSmem = T * kDownSliceCols * 4;
+
 // ---------------------------------------------------------------------------
-// up_mix_tc_kernel - the up projection of a decode chunk on the tcgen05 tensor
-// cores: all of the chunk's tokens in one pass of MMAs instead of a loop over them.
+// up_mix_tc_kernel - the up projection of a decode read on the tcgen05 tensor cores:
+// all of the call's tokens (up to 64) in one pass of MMAs instead of a loop over them.
 // A CTA owns 32 output columns: A = their 128 W_up rows (4 streams x 32 columns,
-// bf16 as stored, loaded by TMA before the dependency wait). B = lo of the chunk's
-// tokens as three bf16 terms hi + mid + low (x - hi and x - hi - mid are exact in
-// fp32, so the three carry x to about 2^-27 of its size), the terms side by side as
-// B rows term * T + t, so that one MMA takes all three: N = 16 up to 5 tokens, 32
-// above. D = 128 x N fp32 in TMEM; each bf16 product is exact in fp32 and each term
-// accumulates 20 MMAs deep; the epilogue adds a token's three columns, smallest
-// first. TMEM lane = row, so warp w holds stream w and lane l column l; the gate is
-// applied there, the four streams of a column meet in shared memory, and the mix
-// writes each output row with stores that are contiguous across the warp.
+// bf16 as stored, loaded by TMA before the dependency wait). B = lo of the tokens as
+// three bf16 terms hi + mid + low (split3_bf16), the terms side by side as B rows
+// term * T + t, so that one MMA takes all three: N = 3T rounded up to 16. D = 128 x N
+// fp32 in TMEM; each bf16 product is exact in fp32 and each term accumulates 20 MMAs
+// deep; the epilogue adds a token's three columns, smallest first. TMEM lane = row,
+// so warp w holds stream w and lane l column l; the gate is applied there, the four
+// streams of a column meet in shared memory, and the mix writes each output row with
+// stores that are contiguous across the warp.
+//
+// TM is the largest token count of the instantiation: for TM <= 8 the kernel reads
+// exactly TM tokens; TM = 16, 32 and 64 take any T in (TM / 2, TM] (and 16 any T in
+// 9..16), given at run time.
 // ---------------------------------------------------------------------------
 constexpr int kTcCols = 32;                          // output columns per CTA
 constexpr int kTcRows = kStreams * kTcCols;          // 128 W_up rows: MMA M
 constexpr int kTcKB = 64;                            // K per 128-byte swizzle row
 constexpr int kTcKBlocks = kRank / kTcKB;            // 5
-template <int T> constexpr int kTcN = 3 * T <= 16 ? 16 : 32;   // MMA N: 3 terms x T tokens
 constexpr int kTcABytes = kTcRows * kTcKB * 2;       // 16 KB per K block
-constexpr int kTcBBytesMax = 32 * kTcKB * 2;         // 4 KB per K block at N = 32
 constexpr int kTcThreads = 128;
-constexpr int kTcSmem = kTcKBlocks * kTcABytes + kTcKBlocks * kTcBBytesMax + 1024;
-constexpr int kTcTmemCols = 32;                      // the smallest TMEM allocation
+constexpr int kWideMaxT = 64;                        // tokens of one decode pass at most
+// MMA N: 3 terms x TM tokens, rounded up to 16 (32 for 6-8 tokens)
+template <int TM> constexpr int kTcN = (3 * TM + 15) / 16 * 16;
+// B rows reserved: 32 for every TM <= 8, so that those kernels keep one shared-memory
+// footprint (and one CTA per SM) whatever their token count
+template <int TM> constexpr int kTcBRows = TM <= 8 ? 32 : kTcN<TM>;
+template <int TM> constexpr int kTcSmem = kTcKBlocks * kTcABytes + kTcKBlocks * kTcBRows<TM> * kTcKB * 2 + 1024;
+// TMEM columns: a power of two, at least 32
+template <int TM> constexpr int kTcTmemCols = kTcN<TM> <= 32 ? 32 : kTcN<TM> <= 64 ? 64 : kTcN<TM> <= 128 ? 128 : 256;
+static_assert(kTcSmem<kWideMaxT> <= 227 * 1024 - 8 * 1024, "up kernel shared memory");
 
 // A bounded wait on an mbarrier phase: false after 2 s, with the timeout recorded in
 // the status word when there is one (the allocation-free entry has none; the kernel
@@ -275,30 +329,62 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int* sta
     return true;
 }
 
-template <int T>
+// 8 consecutive fp32 columns of this thread's TMEM lane at three column offsets, one
+// wait for all three.
+__device__ __forceinline__ void tmem_ld8x3(uint32_t a0, uint32_t a1, uint32_t a2, float (&h)[8],
+                                           float (&m)[8], float (&l)[8]) {
+    uint32_t r[24];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%24];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%25];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%26];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23])
+        : "r"(a0), "r"(a1), "r"(a2)
+        : "memory");
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        h[e] = __uint_as_float(r[e]);
+        m[e] = __uint_as_float(r[8 + e]);
+        l[e] = __uint_as_float(r[16 + e]);
+    }
+}
+
+template <int TM>
 __global__ void __launch_bounds__(kTcThreads, 1)
 up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, const float* P,
                  const float* lo, const float* Rmix, float* out_f32, uint16_t* out_bf16,
-                 uint16_t* out_fp16, int* status) {
+                 uint16_t* out_fp16, int* status, int t_run) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned: the 128-byte swizzle pattern repeats every 8 rows of 128 B
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int kN = kTcN<T>, kBBytes = kN * kTcKB * 2;
+    constexpr bool kSmall = TM <= 8;
+    constexpr int kN = kTcN<TM>, kBBytes = kN * kTcKB * 2;
+    constexpr int kBStride = kTcBRows<TM> * kTcKB * 2;  // bytes per K block of B
+    const int T = kSmall ? TM : t_run;                  // tokens of this read
     uint8_t* sA = smem;                                  // [K block][128 rows][128 B]
     uint8_t* sB = smem + kTcKBlocks * kTcABytes;         // [K block][N rows][128 B]
     __shared__ __align__(8) uint64_t w_full, mma_done;
     __shared__ uint32_t tmem_slot;
-    __shared__ float g_s[T][kStreams][kTcCols];
-    __shared__ __align__(16) float m_s[T][16];
+    __shared__ __align__(16) float m_s[TM][16];
+    // gated values of the tokens: static for a few tokens, else over the A tiles once
+    // the MMAs have read them
+    __shared__ float g_small[kSmall ? TM : 1][kStreams][kTcCols];
+    float (*g_s)[kStreams][kTcCols] =
+        kSmall ? g_small : reinterpret_cast<float (*)[kStreams][kTcCols]>(sA);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x * kTcCols + lane;           // this thread's output column
+    (void)kBBytes;
 
     if (tid == 0) {
         tc::mbar_init(&w_full, 1);
         tc::mbar_init(&mma_done, 1);
         tc::fence_barrier_init();
     }
-    if (warp == 0) tc::tmem_alloc(&tmem_slot, kTcTmemCols);
+    if (warp == 0) tc::tmem_alloc(&tmem_slot, kTcTmemCols<TM>);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -318,7 +404,6 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
     // this thread's residual (and pending write) into L2 while the down kernel runs:
     // a warp's 32 columns of a stream are one 128-byte line
     if (lane == 0) {
-#pragma unroll
         for (int t = 0; t < T; ++t) {
             prefetch_l2(R + (size_t)t * kCols + warp * kWidth + c);
             if (P != nullptr) prefetch_l2(P + (size_t)t * kCols + warp * kWidth + c);
@@ -327,39 +412,44 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
     pdl_launch_dependents();
     pdl_wait();
 
-    // 2. lo of the chunk as three bf16 terms in the B tiles (K-major, 128-byte
-    //    swizzled, tokens as rows), R' of this thread's (stream, column), the mix
-    float rp[T];
+    // 2. lo of the tokens as three bf16 terms in the B tiles (K-major, 128-byte
+    //    swizzled, rows term * T + t), R' of this thread's (stream, column), the mix
+    float rp[TM];
 #pragma unroll
-    for (int t = 0; t < T; ++t) rp[t] = R[(size_t)t * kCols + warp * kWidth + c];
+    for (int t = 0; t < TM; ++t)
+        rp[t] = t < T ? R[(size_t)t * kCols + warp * kWidth + c] : 0.f;
     if (P != nullptr) {
 #pragma unroll
-        for (int t = 0; t < T; ++t) rp[t] += P[(size_t)t * kCols + warp * kWidth + c];
+        for (int t = 0; t < TM; ++t)
+            if (t < T) rp[t] += P[(size_t)t * kCols + warp * kWidth + c];
     }
     // (rows past 3 T stay unwritten: they only feed D columns nobody reads)
-    constexpr int kQuads = T * kRank / 4;                // float4 granules of lo
-    constexpr int kIters = (kQuads + kTcThreads - 1) / kTcThreads;
-    float4 xq[kIters];
+    const int quads = T * kRank / 4;                     // float4 granules of lo
+    constexpr int kBatch = kSmall ? (TM * kRank / 4 + kTcThreads - 1) / kTcThreads : 10;
+    for (int base = 0; base < quads; base += kBatch * kTcThreads) {
+        float4 xq[kBatch];
 #pragma unroll
-    for (int i = 0; i < kIters; ++i) {                   // every load in flight at once
-        const int e = tid + i * kTcThreads;
-        if (e < kQuads) xq[i] = reinterpret_cast<const float4*>(lo)[e];
-    }
+        for (int i = 0; i < kBatch; ++i) {               // every load of a batch in flight
+            const int e = base + tid + i * kTcThreads;
+            if (e < quads) xq[i] = reinterpret_cast<const float4*>(lo)[e];
+        }
 #pragma unroll
-    for (int i = 0; i < kIters; ++i) {
-        const int e = tid + i * kTcThreads;
-        if (e >= kQuads) continue;
-        const int t = e / (kRank / 4), k = 4 * (e % (kRank / 4));
-        uint32_t h0, m0, l0, h1, m1, l1;
-        split3_bf16(xq[i].x, xq[i].y, h0, m0, l0);
-        split3_bf16(xq[i].z, xq[i].w, h1, m1, l1);
-        uint8_t* b = sB + (k / kTcKB) * kBBytes;
-        const int kin = k % kTcKB;
-        *reinterpret_cast<uint2*>(b + tc::sw128_offset(t, kin)) = make_uint2(h0, h1);
-        *reinterpret_cast<uint2*>(b + tc::sw128_offset(T + t, kin)) = make_uint2(m0, m1);
-        *reinterpret_cast<uint2*>(b + tc::sw128_offset(2 * T + t, kin)) = make_uint2(l0, l1);
+        for (int i = 0; i < kBatch; ++i) {
+            const int e = base + tid + i * kTcThreads;
+            if (e >= quads) continue;
+            const int t = e / (kRank / 4), k = 4 * (e % (kRank / 4));
+            uint32_t h0, m0, l0, h1, m1, l1;
+            split3_bf16(xq[i].x, xq[i].y, h0, m0, l0);
+            split3_bf16(xq[i].z, xq[i].w, h1, m1, l1);
+            uint8_t* b = sB + (k / kTcKB) * kBStride;
+            const int kin = k % kTcKB;
+            *reinterpret_cast<uint2*>(b + tc::sw128_offset(t, kin)) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2*>(b + tc::sw128_offset(T + t, kin)) = make_uint2(m0, m1);
+            *reinterpret_cast<uint2*>(b + tc::sw128_offset(2 * T + t, kin)) = make_uint2(l0, l1);
+        }
     }
-    if (tid < T * 4) reinterpret_cast<float4*>(&m_s[0][0])[tid] = reinterpret_cast<const float4*>(Rmix)[tid];
+    for (int e = tid; e < T * 4; e += kTcThreads)
+        reinterpret_cast<float4*>(&m_s[0][0])[e] = reinterpret_cast<const float4*>(Rmix)[e];
     tc::fence_proxy_async_smem();
     __syncthreads();
 
@@ -376,7 +466,7 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
 #pragma unroll
                 for (int kk = 0; kk < kTcKB / 16; ++kk)
                     tc::mma_f16(tmem, tc::desc_sw128(tc::smem_u32(sA + kb * kTcABytes) + kk * 32),
-                                tc::desc_sw128(tc::smem_u32(sB + kb * kBBytes) + kk * 32), idesc,
+                                tc::desc_sw128(tc::smem_u32(sB + kb * kBStride) + kk * 32), idesc,
                                 (kb | kk) != 0);
             tc::mma_commit(&mma_done);
         }
@@ -386,18 +476,32 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
     const bool ok = ok_s && tc_wait(&mma_done, 0, status);
 
     // 4. gate in place (warp = stream, lane = column), the streams meet in shared
-    //    memory, then the mix and the three images
+    //    memory (over the A tiles for many tokens: the MMAs have read them), then the
+    //    mix and the three images
     if (ok) {
         tc::tc_fence_after();
-        float u[32];
-        tc::tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16), u);
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        if constexpr (kSmall) {
+            float u[32];
+            tc::tmem_ld32(lane_base, u);
 #pragma unroll
-        for (int t = 0; t < T; ++t)
-            g_s[t][warp][lane] = gate_value((u[2 * T + t] + u[T + t]) + u[t], rp[t]);
+            for (int t = 0; t < TM; ++t)
+                g_s[t][warp][lane] = gate_value((u[2 * TM + t] + u[TM + t]) + u[t], rp[t]);
+        } else {
+#pragma unroll
+            for (int g0 = 0; g0 < TM; g0 += 8) {
+                if (g0 >= T) break;
+                float h[8], m[8], l[8];
+                tmem_ld8x3(lane_base + g0, lane_base + T + g0, lane_base + 2 * T + g0, h, m, l);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (g0 + e < T) g_s[g0 + e][warp][lane] = gate_value((l[e] + m[e]) + h[e], rp[g0 + e]);
+            }
+        }
     }
     tc::tc_fence_before();
     __syncthreads();
-#pragma unroll
+#pragma unroll(kSmall ? TM : 1)
     for (int t = 0; t < T; ++t) {
         // a CTA whose wait gave up writes NaN, so that even a caller without a status
         // word (the allocation-free entry) finds no stale values in its outputs
@@ -411,7 +515,7 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
     }
     if (warp == 0) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, kTcTmemCols);
+        tc::tmem_dealloc(tmem, kTcTmemCols<TM>);
     }
 }
 
@@ -432,15 +536,19 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// The up kernel of every chunk is the tcgen05 one. Measured, µs per read with P, for
+// The up kernel of every read is the tcgen05 one. Measured, µs per read with P, for
 // T = 1..8: 6.13, 6.14, 6.67, 7.21, 7.94, 8.68, 9.63, 10.20, against 5.0, 6.1, 7.1,
 // 7.9, 8.8, 9.7, 10.8, 12.2 with the CUDA-core up kernel it replaced. One kernel for
 // every T keeps a token's bits independent of the other tokens of its call.
 
-// Devices (bits) on which up_mix_tc_kernel<T> has been allowed its dynamic shared
-// memory. hc_read_init clears a device's bits (decode_forget_smem), so the attribute
-// is set again after a device reset.
-std::atomic<unsigned long long> g_smem_set[kDecodeMaxT + 1];
+// Devices (bits) on which up_mix_tc_kernel<TM> has been allowed its dynamic shared
+// memory, for TM = 1..8 and then 16, 32, 64. hc_read_init clears a device's bits
+// (decode_forget_smem), so the attributes are set again after a device reset.
+// Then the multi-chunk down kernels of 5..8 tokens a chunk (flags 12..15), whose
+// staged activations and exchange arrays exceed the default 48 KB.
+constexpr int kSmemFlags = kDecodeMaxT + 8;
+std::atomic<unsigned long long> g_smem_set[kSmemFlags];
+template <int TM> constexpr int smem_flag() { return TM <= 8 ? TM : TM == 16 ? 9 : TM == 32 ? 10 : 11; }
 
 // Allows `kernel` `bytes` of dynamic shared memory on this device, once per device.
 template <typename K>
@@ -453,29 +561,57 @@ cudaError_t allow_smem(K kernel, int bytes, int device, std::atomic<unsigned lon
     return e;
 }
 
-template <int T>
+template <int TM>
 cudaError_t allow_up_tc(int device) {
-    return allow_smem(up_mix_tc_kernel<T>, kTcSmem, device, g_smem_set[T]);
+    return allow_smem(up_mix_tc_kernel<TM>, kTcSmem<TM>, device, g_smem_set[smem_flag<TM>()]);
 }
 
+template <int TC>
+cudaError_t allow_down_multi(int device) {
+    return allow_smem(down_slice_kernel<TC, true>, kDownDynSmem<TC>, device, g_smem_set[7 + TC]);
+}
 
-template <int T>
-cudaError_t launch_chunk(const Ctx& ctx, const ReadArgs& a, int t0, cudaStream_t st) {
+// One decode pass over n <= 64 tokens starting at token t0: the down kernel in chunks
+// of TC tokens (one pass over its weights), then the up kernel for all n tokens.
+template <int TC, int TM>
+cudaError_t launch_pass(const Ctx& ctx, const ReadArgs& a, int t0, int n, cudaStream_t st) {
+    constexpr bool kMulti = TM > 8;
     const size_t off = (size_t)t0 * kCols;
     const float* R = a.R + off;
     const float* P = a.P ? a.P + off : nullptr;
     float* lo = ctx.s.lo + (size_t)t0 * kRank;
     CUtensorMap tm_wu;
     if (!encode_w_up_bf16(&tm_wu, a.W_up, kTcCols)) return cudaErrorInvalidValue;
-    cudaError_t e = allow_up_tc<T>(ctx.device);
+    cudaError_t e = allow_up_tc<TM>(ctx.device);
+    if (e == cudaSuccess && kMulti) e = allow_down_multi<TC>(ctx.device);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(down_slice_kernel<T>, dim3(kDownSlices, kDownRowBlocks), dim3(kDownThreads), 0,
-                   st, R, P, a.w_norm, a.W_down, lo, ctx.eps);
+    e = launch_pdl(down_slice_kernel<TC, kMulti>, dim3(kDownSlices, kDownRowBlocks), dim3(kDownThreads),
+                   (size_t)kDownDynSmem<TC>, st, R, P, a.w_norm, a.W_down, lo, ctx.eps, n);
     if (e != cudaSuccess) return e;
-    return launch_pdl(up_mix_tc_kernel<T>, dim3(kWidth / kTcCols), dim3(kTcThreads),
-                      (size_t)kTcSmem, st, tm_wu, R, P, (const float*)lo,
+    return launch_pdl(up_mix_tc_kernel<TM>, dim3(kWidth / kTcCols), dim3(kTcThreads),
+                      (size_t)kTcSmem<TM>, st, tm_wu, R, P, (const float*)lo,
                       a.Rmix + (size_t)t0 * 16, a.out_f32 + off, a.out_bf16 + off,
-                      a.out_fp16 + off, ctx.s.status);
+                      a.out_fp16 + off, ctx.s.status, n);
+}
+
+// n tokens (9..64) read with the weights streamed once: chunks of TC = ceil(n / chunks)
+// tokens in the down kernel, the smallest wide up kernel that holds n.
+template <int TM>
+cudaError_t launch_wide_tc(const Ctx& ctx, const ReadArgs& a, int t0, int n, int tc, cudaStream_t st) {
+    switch (tc) {
+        case 5: return launch_pass<5, TM>(ctx, a, t0, n, st);
+        case 6: return launch_pass<6, TM>(ctx, a, t0, n, st);
+        case 7: return launch_pass<7, TM>(ctx, a, t0, n, st);
+        default: return launch_pass<8, TM>(ctx, a, t0, n, st);
+    }
+}
+
+cudaError_t launch_wide(const Ctx& ctx, const ReadArgs& a, int t0, int n, cudaStream_t st) {
+    const int chunks = (n + kDecodeMaxT - 1) / kDecodeMaxT;
+    const int tc = (n + chunks - 1) / chunks;       // 5..8 for n in 9..64
+    if (n <= 16) return launch_wide_tc<16>(ctx, a, t0, n, tc, st);
+    if (n <= 32) return launch_wide_tc<32>(ctx, a, t0, n, tc, st);
+    return launch_wide_tc<64>(ctx, a, t0, n, tc, st);
 }
 
 }  // namespace
@@ -485,39 +621,54 @@ void decode_forget_smem(int device) {
     for (auto& bits : g_smem_set) bits.fetch_and(~(1ull << device), std::memory_order_acq_rel);
 }
 
-namespace {
-template <int T>
-cudaError_t allow_chunk(int device) {
-    return allow_up_tc<T>(device);
-}
-}  // namespace
-
 cudaError_t decode_setup(int device) {
     decode_forget_smem(device);
-    cudaError_t e = allow_chunk<1>(device);
-    if (e == cudaSuccess) e = allow_chunk<2>(device);
-    if (e == cudaSuccess) e = allow_chunk<3>(device);
-    if (e == cudaSuccess) e = allow_chunk<4>(device);
-    if (e == cudaSuccess) e = allow_chunk<5>(device);
-    if (e == cudaSuccess) e = allow_chunk<6>(device);
-    if (e == cudaSuccess) e = allow_chunk<7>(device);
-    if (e == cudaSuccess) e = allow_chunk<8>(device);
+    cudaError_t e = allow_up_tc<1>(device);
+    if (e == cudaSuccess) e = allow_up_tc<2>(device);
+    if (e == cudaSuccess) e = allow_up_tc<3>(device);
+    if (e == cudaSuccess) e = allow_up_tc<4>(device);
+    if (e == cudaSuccess) e = allow_up_tc<5>(device);
+    if (e == cudaSuccess) e = allow_up_tc<6>(device);
+    if (e == cudaSuccess) e = allow_up_tc<7>(device);
+    if (e == cudaSuccess) e = allow_up_tc<8>(device);
+    if (e == cudaSuccess) e = allow_up_tc<16>(device);
+    if (e == cudaSuccess) e = allow_up_tc<32>(device);
+    if (e == cudaSuccess) e = allow_up_tc<64>(device);
+    if (e == cudaSuccess) e = allow_down_multi<5>(device);
+    if (e == cudaSuccess) e = allow_down_multi<6>(device);
+    if (e == cudaSuccess) e = allow_down_multi<7>(device);
+    if (e == cudaSuccess) e = allow_down_multi<8>(device);
     return e;
 }
 
+// Any T: passes of up to 64 tokens. A pass of 1-8 tokens is one chunk (down and up
+// kernels of exactly that many tokens); 17-64 tokens stream the weights once (one
+// down kernel in chunks, one up kernel); 9-16 tokens run as two chunks of up to 8,
+// whose kernels overlap by programmatic dependent launch. Measured on GB300 (µs per
+// read with P, one weight set): one pass 20.4 / 36.8 / 71.8 at 16 / 32 / 64 tokens
+// against 19.4 / 38.7 / 77.2 in chunks of 8. The time grows with the tokens in the
+// down kernel's staging and dot products (about 5-7 µs per chunk of 8), not with the
+// weight stream.
+constexpr int kWideMinT = 17;
+
 cudaError_t launch_decode(const Ctx& ctx, const ReadArgs& a, cudaStream_t st) {
-    for (int t0 = 0; t0 < a.T; t0 += kDecodeMaxT) {
-        const int n = a.T - t0 < kDecodeMaxT ? a.T - t0 : kDecodeMaxT;
+    for (int t0 = 0; t0 < a.T;) {
+        const int left = a.T - t0;
+        const int n = left >= kWideMinT ? (left < kWideMaxT ? left : kWideMaxT)
+                                        : (left < kDecodeMaxT ? left : kDecodeMaxT);
+        const int p0 = t0;                       // first token of this pass
+        t0 += n;
         cudaError_t e;
         switch (n) {
-            case 1: e = launch_chunk<1>(ctx, a, t0, st); break;
-            case 2: e = launch_chunk<2>(ctx, a, t0, st); break;
-            case 3: e = launch_chunk<3>(ctx, a, t0, st); break;
-            case 4: e = launch_chunk<4>(ctx, a, t0, st); break;
-            case 5: e = launch_chunk<5>(ctx, a, t0, st); break;
-            case 6: e = launch_chunk<6>(ctx, a, t0, st); break;
-            case 7: e = launch_chunk<7>(ctx, a, t0, st); break;
-            default: e = launch_chunk<8>(ctx, a, t0, st); break;
+            case 1: e = launch_pass<1, 1>(ctx, a, p0, 1, st); break;
+            case 2: e = launch_pass<2, 2>(ctx, a, p0, 2, st); break;
+            case 3: e = launch_pass<3, 3>(ctx, a, p0, 3, st); break;
+            case 4: e = launch_pass<4, 4>(ctx, a, p0, 4, st); break;
+            case 5: e = launch_pass<5, 5>(ctx, a, p0, 5, st); break;
+            case 6: e = launch_pass<6, 6>(ctx, a, p0, 6, st); break;
+            case 7: e = launch_pass<7, 7>(ctx, a, p0, 7, st); break;
+            case 8: e = launch_pass<8, 8>(ctx, a, p0, 8, st); break;
+            default: e = launch_wide(ctx, a, p0, n, st); break;
         }
         if (e != cudaSuccess) return e;
     }

@@ -96,6 +96,16 @@ def test_ragged_token_counts(weights, T, path):
     assert_matches_oracle(got, want)
 
 
+@pytest.mark.parametrize("T,with_P", [(33, True), (40, False), (57, True), (64, True), (65, False),
+                                      (130, True)])
+def test_decode_passes_of_up_to_64_tokens(weights, T, with_P):
+    """The decode kernels read up to 64 tokens in one pass over the weights (the down
+    kernel in chunks of 5-8 tokens, the up kernel on all of them); 65 and 130 tokens
+    take a second and third pass."""
+    got, want = run_case(weights, T, with_P, 150 + T, hc.HC_PATH_DECODE)
+    assert_matches_oracle(got, want)
+
+
 @pytest.mark.parametrize("T", [1, 4, 8])
 def test_one_kernel_decode_path(weights, T):
     got, want = run_case(weights, T, True, 300 + T, hc.HC_PATH_DECODE_ONE_KERNEL)
@@ -125,12 +135,14 @@ def test_pending_write_equals_preadded(weights):
 
 @pytest.mark.parametrize("path", [hc.HC_PATH_DECODE, hc.HC_PATH_DECODE_ONE_KERNEL])
 def test_token_batch_invariance_decode(weights, path):
-    """Token t's bits do not depend on the other tokens of the call."""
+    """Token t's bits do not depend on the other tokens of the call (40 tokens in one
+    pass of the decode kernels, 8 in the one-kernel read)."""
     w, W = weights
-    a = synth.make_activations(9, 8, True)
+    n = 40 if path == hc.HC_PATH_DECODE else 8
+    a = synth.make_activations(9, n, True)
     R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
-    full = gpu_read(8, R, P, W, M, path)
-    for t in (0, 5, 7):
+    full = gpu_read(n, R, P, W, M, path)
+    for t in (0, 5, 7) + ((13, 39) if n > 8 else ()):
         one = gpu_read(1, R[t:t + 1].contiguous(), P[t:t + 1].contiguous(), W,
                        M[t:t + 1].contiguous(), path)
         assert np.array_equal(one[0][0].view(np.uint32), full[0][t].view(np.uint32))
