@@ -45,10 +45,10 @@ EPS = float(np.float32(1e-6))
 # kernels changed after the last capture. The sweep's traffic is taken as its
 # algorithmic bytes times the ratio of this figure to the same read's algorithmic
 # bytes. Capture (two reads, 48 rotated weight sets, so the weights come from DRAM):
-# down_slice_kernel<4> 6,918,912 B, up_mix_tc_kernel<4> 6,910,336 B, both reads,
+# down_slice_kernel<4, 0> 6,918,912 B, up_mix_tc_kernel<4> 6,910,848 B, both reads,
 # nothing written back to DRAM (the outputs stay in L2).
-NCU_TRAFFIC_T4_P = 13_829_248
-NCU_TRAFFIC_LAST = "13,829,248 B per T=4 read with P (13,783,296 algorithmic)"
+NCU_TRAFFIC_T4_P = 13_829_760
+NCU_TRAFFIC_LAST = "13,829,760 B per T=4 read with P (13,783,296 algorithmic)"
 
 
 def read_bytes(T: int, with_P: bool) -> int:
@@ -448,7 +448,7 @@ def gpu_arm(args) -> None:
         for kind in ("done", "out"):
             ev[(kind, b)].record(stream)
 
-    def e2e_step(k):
+    def e2e_step(k, graphed=True):
         b = k % 2
         # inputs of this step into buffer b once the step that last read it is done
         h2d_stream.wait_event(ev[("done", b)])
@@ -459,7 +459,10 @@ def gpu_arm(args) -> None:
         stream.wait_event(ev[("in", b)])
         stream.wait_event(ev[("out", b)])
         with torch.cuda.stream(stream):   # a graph replays on the current stream
-            e2e_graphs[(k % n_groups, b)].replay()
+            if graphed:
+                e2e_graphs[(k % n_groups, b)].replay()
+            else:                          # the 16 public calls, launched one by one
+                enqueue_reads(k % n_groups, b)
         ev[("done", b)].record(stream)
         # the outputs back while the next step computes
         d2h_stream.wait_event(ev[("done", b)])
@@ -467,11 +470,11 @@ def gpu_arm(args) -> None:
             pin_out.copy_(dev_out[b], non_blocking=True)
         ev[("out", b)].record(d2h_stream)
 
-    def e2e_run(steps, warmup):
+    def e2e_run(steps, warmup, graphed=True):
         """Device time of `steps` pipelined steps, from the first copy to the last
         output back on the host, after `warmup` steps."""
         for k in range(warmup):
-            e2e_step(k)
+            e2e_step(k, graphed)
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -479,7 +482,7 @@ def gpu_arm(args) -> None:
         h2d_stream.wait_event(e0)
         d2h_stream.wait_event(e0)
         for k in range(warmup, warmup + steps):
-            e2e_step(k)
+            e2e_step(k, graphed)
         stream.wait_stream(d2h_stream)
         e1.record(stream)
         barrier()
@@ -487,6 +490,9 @@ def gpu_arm(args) -> None:
 
     e2e_steps = max(10, min(args.steps, 500))
     ms_e = e2e_run(e2e_steps, min(args.warmup, 5) + 3)
+    # the same pipelined steps with every read a direct call (no CUDA graph): the
+    # host's launch work per call is then on the path
+    ms_e_direct = e2e_run(e2e_steps, min(args.warmup, 5) + 3, graphed=False)
 
     def e2e_serial_step(k):
         # the same step with copies and reads in order on one stream: no overlap
@@ -609,7 +615,10 @@ def gpu_arm(args) -> None:
                 "d2h_bytes_per_step": d2h,
                 "pipelining": "step k+1's inputs and step k-1's outputs cross on two copy "
                               "streams while step k computes",
-                "serial_us": us_per_unit(ms_e_serial, e2e_steps * reads_per_step, world)},
+                "serial_us": us_per_unit(ms_e_serial, e2e_steps * reads_per_step, world),
+                "ungraphed_us": us_per_unit(ms_e_direct, e2e_steps * reads_per_step, world),
+                "ungraphed": "the same pipelined steps, each read a direct hc_read call "
+                             "(no CUDA graph)"},
         "gpu_launches": kernel_launches_per_step * args.steps,
         "decode_by_T": per_t,
         "decode_paths_us_by_T_with_P": per_t_paths,
