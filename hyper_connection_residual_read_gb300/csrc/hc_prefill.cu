@@ -38,24 +38,25 @@ namespace {
 using namespace tc;
 
 constexpr int kTileM = 128;            // tokens per tile (TMEM lanes)
-constexpr int kBK = 64;                // K per pipeline stage: one 128-byte swizzle row
-constexpr int kTileBytes16 = kTileM * kBK * 2;    // 16 KB: one 128 x 64 bf16 operand tile
+constexpr int kBK = 64;                // K of a W_up box for the decode up kernel (128-byte swizzle)
 constexpr int kTerms = 3;              // bf16 terms of an activation (split3_bf16)
 
 // down_tile
 constexpr int kDownN = kRank;          // 320 accumulator columns (two MMAs of N = 160)
-// Two stages of 88 KB (three 16 KB A terms and 40 KB of W_down): a third does not fit
-// in shared memory. R blocks are asked into L2 ahead of their loads (kDownPrefetch).
-constexpr int kDownStages = 2;
-constexpr int kDownBBytes = kDownN * kBK * 2;     // 40 KB
-constexpr int kDownStageBytes = kTerms * kTileBytes16 + kDownBBytes;
-constexpr int kDownKBlocks = kWidth / kBK;        // 40 per stream
+// K blocks of 32 (one 64-byte swizzle row): four stages of 44 KB (three 8 KB A terms
+// and 20 KB of W_down). With K blocks of 64, two stages of 88 KB were all that fit.
+constexpr int kDownBK = 32;
+constexpr int kDownStages = 4;
+constexpr int kDownTileBytes = kTileM * kDownBK * 2;   // 8 KB: one 128 x 32 bf16 term
+constexpr int kDownBBytes = kDownN * kDownBK * 2;      // 20 KB
+constexpr int kDownStageBytes = kTerms * kDownTileBytes + kDownBBytes;
+constexpr int kDownKBlocks = kWidth / kDownBK;         // 80 per stream
 // Each stream's K is split into quarters with an accumulator (and a partial) each:
 // the tensor cores' fp32 accumulation rounds toward zero at every MMA, so the depth
-// of one accumulation (here 10 K blocks x 4 steps x 3 terms = 120 MMAs) bounds the
+// of one accumulation (here 20 K blocks x 2 steps x 3 terms = 120 MMAs) bounds the
 // relative shrink of the result.
 constexpr int kDownKSplit = 4;
-constexpr int kDownKBlocksPerTile = kDownKBlocks / kDownKSplit;   // 10
+constexpr int kDownKBlocksPerTile = kDownKBlocks / kDownKSplit;   // 20
 // TMA, MMA, 8 converter warps, 4 epilogue warps (one per TMEM lane quarter): the
 // epilogue of one tile runs while the converters already produce the next tile's A
 constexpr int kDownThreads = 448;
@@ -68,7 +69,7 @@ constexpr int kDownTileQ = 4;
 constexpr int kDownHalf = kDownN / 2;
 constexpr int kDownHalfBufs = 3;
 // R blocks are asked into L2 this many K blocks before their TMA load
-constexpr int kDownPrefetch = 3;
+constexpr int kDownPrefetch = 6;
 constexpr int kDownTileQConsumers = 1 + 8 + 4;
 constexpr int kDownSmem = kDownStages * kDownStageBytes + 1024;
 
@@ -121,6 +122,13 @@ constexpr int kUpSmem = kUpStages * kUpStageBytes + kRSlots * kRSlot + 1024;
 static_assert(kUpSmem <= 227 * 1024 - 1024, "up tile shared memory");
 static_assert(kDownSmem <= 227 * 1024 - 2048, "down tile shared memory");
 
+// Byte offset of 16-bit element (row r, k) in a K-major 64-byte-swizzled tile: rows of
+// 64 bytes, 8-row atoms of 512 bytes, the 16-byte chunk index XORed with bits 1-2 of r.
+__device__ __forceinline__ uint32_t sw64_offset(int r, int k) {
+    return static_cast<uint32_t>((r >> 3) * 512 + (r & 7) * 64 +
+                                 (((k >> 3) ^ ((r >> 1) & 3)) << 4) + (k & 7) * 2);
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
@@ -144,12 +152,12 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // ---------------------------------------------------------------------------
 // down projection, one (128-token tile, stream, K quarter) per tile, persistent CTAs
 //
-// R reaches shared memory by TMA into the stage's A region, 32 KB of fp32 per K
-// block, laid out so that the 16 rows each converter warp owns occupy exactly the
-// bytes where that warp then writes the rows' first two bf16 terms (hi in the first
-// 16 KB, mid in the second, 128-byte swizzled; low goes to the third 16 KB): the warp
-// reads its rows into registers, scales and splits them, and overwrites them in
-// place, with no synchronisation beyond the warp. The view of R that gives this layout is
+// R reaches shared memory by TMA into the stage's A region, 16 KB of fp32 per K
+// block of 32 columns, laid out so that the 16 rows each converter warp owns occupy
+// exactly the bytes where that warp then writes the rows' first two bf16 terms (hi in
+// the first 8 KB, mid in the second, 64-byte swizzled; low goes to the third 8 KB):
+// the warp reads its rows into registers, scales and splits them, and overwrites them
+// in place, with no synchronisation beyond the warp. The view of R that gives this layout is
 // (column, stream, row r, half h, group g) with token = 16 g + 8 h + r; a tile's
 // two loads (h = 0, 1) each take 8 rows of 8 groups. A last tile with fewer than
 // 128 tokens is read by the converter warps from global memory instead.
@@ -196,8 +204,8 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
-    auto sA = [&](int slot, int term) { return smem + slot * kDownStageBytes + term * kTileBytes16; };
-    auto sB = [&](int slot) { return smem + slot * kDownStageBytes + kTerms * kTileBytes16; };
+    auto sA = [&](int slot, int term) { return smem + slot * kDownStageBytes + term * kDownTileBytes; };
+    auto sB = [&](int slot) { return smem + slot * kDownStageBytes + kTerms * kDownTileBytes; };
     // the CTA's i-th tile from the queue (n_tiles: no more tiles, or the CTA gave up),
     // taken by a whole warp (its lane 0 releases the entry once every lane has read
     // it) or by one thread
@@ -237,14 +245,14 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     const uint32_t ph = (it / kDownStages) & 1;
                     if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
                     if (full) {
-                        mbar_arrive_expect_tx(&r_full[slot], 2 * kTileBytes16);
-                        tma_load_5d(sA(slot, 0), &tm_r, kb * kBK, s, 0, 0, tt * 8, &r_full[slot]);
-                        tma_load_5d(sA(slot, 1), &tm_r, kb * kBK, s, 0, 1, tt * 8, &r_full[slot]);
+                        mbar_arrive_expect_tx(&r_full[slot], 2 * kDownTileBytes);
+                        tma_load_5d(sA(slot, 0), &tm_r, kb * kDownBK, s, 0, 0, tt * 8, &r_full[slot]);
+                        tma_load_5d(sA(slot, 1), &tm_r, kb * kDownBK, s, 0, 1, tt * 8, &r_full[slot]);
                     } else {
                         mbar_arrive(&r_full[slot]);
                     }
                     mbar_arrive_expect_tx(&full_bar[slot], kDownBBytes);
-                    const int x = s * kWidth + kb * kBK;
+                    const int x = s * kWidth + kb * kDownBK;
                     tma_load_2d(sB(slot), &tm_wd, x, 0, &full_bar[slot]);
                     tma_load_2d(sB(slot) + kDownBBytes / 2, &tm_wd, x, kDownN / 2, &full_bar[slot]);
                     // R of the block kDownPrefetch stages ahead into L2: later in this
@@ -253,10 +261,10 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     if (pk < kDownKBlocksPerTile) {
                         if (full)
                             for (int h = 0; h < 2; ++h)
-                                tma_prefetch_5d(&tm_r, (kb + kDownPrefetch) * kBK, s, 0, h, tt * 8);
+                                tma_prefetch_5d(&tm_r, (kb + kDownPrefetch) * kDownBK, s, 0, h, tt * 8);
                     } else if (next_full) {
                         const int nkb = nkq * kDownKBlocksPerTile + pk - kDownKBlocksPerTile;
-                        for (int h = 0; h < 2; ++h) tma_prefetch_5d(&tm_r, nkb * kBK, ns, 0, h, ntt * 8);
+                        for (int h = 0; h < 2; ++h) tma_prefetch_5d(&tm_r, nkb * kDownBK, ns, 0, h, ntt * 8);
                     }
                 }
             }
@@ -299,9 +307,9 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                         for (int term = 0; term < kTerms; ++term) {
                             const uint32_t a0 = smem_u32(sA(slot, term));
 #pragma unroll
-                            for (int kk = 0; kk < kBK / 16; ++kk)
-                                mma_f16(h ? d1 : d0, desc_sw128(a0 + kk * 32),
-                                        desc_sw128(b0 + h * (kDownBBytes / 2) + kk * 32), idesc,
+                            for (int kk = 0; kk < kDownBK / 16; ++kk)
+                                mma_f16(h ? d1 : d0, desc_sw64(a0 + kk * 32),
+                                        desc_sw64(b0 + h * (kDownBBytes / 2) + kk * 32), idesc,
                                         (kl | term | kk) != 0);
                         }
                     }
@@ -314,9 +322,10 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         }
     } else if (warp < 10) {
         // 8 converter warps produce A: warp cw owns rows 16*cw..16*cw+15 of the tile;
-        // lanes 0-15 and 16-31 take two rows at a time, 4 columns each
+        // eight lanes take a row, 4 columns each, four rows at a time
         const int cw = warp - 2;
-        const int kc = 4 * (lane & 15);                 // this lane's 4 columns in a K block
+        const int kc = 4 * (lane & 7);                  // this lane's 4 columns in a K block
+        const int jr = lane >> 3;                       // its row within a group of four
         int it = 0;
         for (int lt = 0; !abort_flag; ++lt) {
             const int tile = take_tile(lt, true);
@@ -324,22 +333,22 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             const int tt = tile / (kStreams * kDownKSplit);
             const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
             const bool full = (tt + 1) * kTileM <= T;
-            float ss[8];
+            float ss[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ss[i] = 0.f;
+            for (int i = 0; i < 4; ++i) ss[i] = 0.f;
             // w_norm of this lane's 4 columns, loaded one K block ahead
             uint2 wv_next = *reinterpret_cast<const uint2*>(
-                w_norm + s * kWidth + kq * kDownKBlocksPerTile * kBK + kc);
+                w_norm + s * kWidth + kq * kDownKBlocksPerTile * kDownBK + kc);
             for (int kb = kq * kDownKBlocksPerTile; kb < (kq + 1) * kDownKBlocksPerTile; ++kb, ++it) {
                 const int slot = it % kDownStages;
                 const uint32_t ph = (it / kDownStages) & 1;
-                const int k = s * kWidth + kb * kBK + kc;
-                float4 x[8];
+                const int k = s * kWidth + kb * kDownBK + kc;
+                float4 x[4];
                 // P (and, in a last partial tile, R) straight from global memory,
                 // issued before the wait
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int tr = tt * kTileM + 16 * cw + 2 * i + (lane >> 4);
+                for (int i = 0; i < 4; ++i) {
+                    const int tr = tt * kTileM + 16 * cw + 4 * i + jr;
                     x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (tr < T) {
                         if (P != nullptr) x[i] = *reinterpret_cast<const float4*>(P + (size_t)tr * kCols + k);
@@ -351,19 +360,20 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                 }
                 const uint2 wv = wv_next;
                 if (kb + 1 < (kq + 1) * kDownKBlocksPerTile)
-                    wv_next = *reinterpret_cast<const uint2*>(w_norm + k + kBK);
+                    wv_next = *reinterpret_cast<const uint2*>(w_norm + k + kDownBK);
                 const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x), w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
                 if (!mbar_wait(&r_full[slot], ph, &abort_flag, status)) break;
                 uint8_t* ahi = sA(slot, 0);
                 uint8_t* amid = sA(slot, 1);
                 uint8_t* alow = sA(slot, 2);
                 if (full) {
-                    // R rows j = 2i + (lane >> 4) of this warp: half j >> 3, row j & 7
+                    // R rows j = 4i + jr of this warp: half j >> 3, row j & 7, 128 bytes
+                    // a row; all of them are read before any term is written over them
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int j = 2 * i + (lane >> 4);
+                    for (int i = 0; i < 4; ++i) {
+                        const int j = 4 * i + jr;
                         const float4 r = *reinterpret_cast<const float4*>(
-                            sA(slot, j >> 3) + (cw * 8 + (j & 7)) * 256 + kc * 4);
+                            sA(slot, j >> 3) + (cw * 8 + (j & 7)) * 128 + kc * 4);
                         // R + P in that order: the pending write's single rounding
                         if (P != nullptr) {
                             x[i].x = r.x + x[i].x; x[i].y = r.y + x[i].y;
@@ -375,8 +385,8 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     __syncwarp();
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int row = 16 * cw + 2 * i + (lane >> 4);
+                for (int i = 0; i < 4; ++i) {
+                    const int row = 16 * cw + 4 * i + jr;
                     const float4 r = x[i];
                     float sq = r.x * r.x;
                     sq = fmaf(r.y, r.y, sq);
@@ -386,7 +396,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     uint32_t h0, m0, l0, h1, m1, l1;
                     split3_bf16(r.x * w0, r.y * w1, h0, m0, l0);
                     split3_bf16(r.z * w2, r.w * w3, h1, m1, l1);
-                    const uint32_t off = sw128_offset(row, kc);
+                    const uint32_t off = sw64_offset(row, kc);
                     *reinterpret_cast<uint2*>(ahi + off) = make_uint2(h0, h1);
                     *reinterpret_cast<uint2*>(amid + off) = make_uint2(m0, m1);
                     *reinterpret_cast<uint2*>(alow + off) = make_uint2(l0, l1);
@@ -395,19 +405,18 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                 mbar_arrive(&full_bar[slot]);
             }
             if (abort_flag) break;
-            // sums of squares per row: the 16 lanes that share a row, in a fixed order.
+            // sums of squares per row: the 8 lanes that share a row, in a fixed order.
             // The buffer of this parity was last read by the epilogue two tiles ago,
             // before it released that tile's second half-buffer; this tile's MMAs,
-            // which the conversions run at most two stages ahead of, waited for
-            // that release.
+            // which the conversions run at most four stages (of a tile's twenty K
+            // blocks) ahead of, waited for that release.
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 4; ++i) {
                 float v = ss[i];
                 v += __shfl_xor_sync(0xffffffffu, v, 1);
                 v += __shfl_xor_sync(0xffffffffu, v, 2);
                 v += __shfl_xor_sync(0xffffffffu, v, 4);
-                v += __shfl_xor_sync(0xffffffffu, v, 8);
-                if ((lane & 15) == 0) ss_s[lt & 1][16 * cw + 2 * i + (lane >> 4)] = v;
+                if ((lane & 7) == 0) ss_s[lt & 1][16 * cw + 4 * i + jr] = v;
             }
             mbar_arrive(&ss_full[lt & 1]);
         }
@@ -993,19 +1002,19 @@ bool encode_down_r(CUtensorMap* map, const float* R, int T) {
     const cuuint64_t dims[5] = {kWidth, kStreams, 8, 2, groups};
     const cuuint64_t row = (cuuint64_t)kCols * 4;
     const cuuint64_t strides[4] = {(cuuint64_t)kWidth * 4, row, 8 * row, 16 * row};
-    const cuuint32_t box[5] = {kBK, 1, 8, 1, 8};
+    const cuuint32_t box[5] = {kDownBK, 1, 8, 1, 8};
     return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, R, 5, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// The caller's W_down [kRank][kCols] bf16 in boxes of 64 K x 160 rows, 128-byte
+// The caller's W_down [kRank][kCols] bf16 in boxes of 32 K x 160 rows, 64-byte
 // swizzled: one N half of a down tile's B operand per box.
 bool encode_w_down_bf16(CUtensorMap* map, const uint16_t* W_down) {
     const cuuint64_t dims[2] = {kCols, kRank};
     const cuuint64_t strides[1] = {kCols * 2};
-    const cuuint32_t box[2] = {kBK, kDownN / 2};
+    const cuuint32_t box[2] = {kDownBK, kDownN / 2};
     return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W_down, 2, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+                      CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // The caller's W_up [kCols][kRank] bf16 in boxes of 32 K x 64 rows, 64-byte swizzled:
