@@ -8,12 +8,12 @@ from . import synth  # noqa: F401
 
 _BINDING = ("hc_read_init", "hc_read", "hc_read_path", "hc_read_check", "hc_read_status",
             "hc_read_noalloc", "hc_read_upmix", "hc_read_lo_bf16", "hc_read_y",
-            "hc_read_set_wait_limit",
+            "hc_read_set_wait_limit", "hc_read_bounds_checked",
             "hc_read_shutdown", "hc_read_version", "strerror", "HcReadError", "load",
             "HC_PATH_AUTO", "HC_PATH_DECODE", "HC_PATH_PREFILL", "HC_PATH_PREFILL_UNFUSED",
             "HC_PATH_DECODE_ONE_KERNEL", "HC_PATH_PREFILL_BF16_LO",
             "HC_OK", "HC_ERR_ARG", "HC_ERR_NOT_INIT", "HC_ERR_ARCH", "HC_ERR_CUDA",
-            "HC_ERR_TIMEOUT", "HC_ERR_CHECK", "HC_ERR_NOMEM",
+            "HC_ERR_TIMEOUT", "HC_ERR_CHECK", "HC_ERR_NOMEM", "HC_ERR_BOUNDS",
             "EXPORTS", "LIB_PATH")
 
 

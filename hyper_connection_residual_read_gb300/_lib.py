@@ -22,6 +22,7 @@ HC_ERR_CUDA = -4
 HC_ERR_TIMEOUT = -5
 HC_ERR_CHECK = -6
 HC_ERR_NOMEM = -7
+HC_ERR_BOUNDS = -8
 
 HC_PATH_AUTO = 0
 HC_PATH_DECODE = 1
@@ -35,7 +36,8 @@ STREAMS, WIDTH, RANK = 4, 2560, 320
 # every symbol include/hc_read.h declares
 EXPORTS = ("hc_read_init", "hc_read", "hc_read_path", "hc_read_check", "hc_read_status",
            "hc_read_strerror", "hc_read_shutdown", "hc_read_version", "hc_read_noalloc",
-           "hc_read_upmix", "hc_read_lo_bf16", "hc_read_y", "hc_read_set_wait_limit")
+           "hc_read_upmix", "hc_read_lo_bf16", "hc_read_y", "hc_read_set_wait_limit",
+           "hc_read_bounds_checked")
 
 
 class HcReadError(RuntimeError):
@@ -103,6 +105,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_read_lo_bf16.restype = i32
     lib.hc_read_set_wait_limit.argtypes = [u64]
     lib.hc_read_set_wait_limit.restype = i32
+    lib.hc_read_bounds_checked.argtypes = []
+    lib.hc_read_bounds_checked.restype = i32
     _lib = lib
     return lib
 
@@ -137,6 +141,11 @@ def strerror(code: int) -> str:
 
 def hc_read_version() -> int:
     return load().hc_read_version()
+
+
+def hc_read_bounds_checked() -> bool:
+    """True if the loaded library is the bounds-checked build."""
+    return bool(load().hc_read_bounds_checked())
 
 
 def hc_read_init(device: int = 0, max_tokens: int = 8, eps: float = 1e-6) -> None:

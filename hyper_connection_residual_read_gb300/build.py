@@ -31,8 +31,8 @@ def nvcc() -> str:
     return path
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra: list[str], build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -40,23 +40,37 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compiles and links the library; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+# The bounds-checked variant (every hand-indexed global access range-checked; see
+# hc_read_bounds_checked in include/hc_read.h), built on demand beside the objects.
+BOUNDS_LIB = os.path.join(BUILD, "bounds", "libhcread_bounds.so")
+
+
+def build(verbose: bool = False, extra: list[str] | None = None, out: str = LIB) -> str:
+    """Compiles and links the library into `out`; returns its path."""
+    build_dir = BUILD if out == LIB else os.path.join(os.path.dirname(out), "obj")
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     extra = list(extra or [])
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, build_dir), srcs))
+    tmp = out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, out)
     if verbose:
-        print(f"built {LIB} from {len(srcs)} sources")
-    return LIB
+        print(f"built {out} from {len(srcs)} sources")
+    return out
+
+
+def build_bounds_checked(verbose: bool = False) -> str:
+    """The bounds-checked variant of the library (-DHC_BOUNDS_CHECK)."""
+    return build(verbose, ["-DHC_BOUNDS_CHECK"], BOUNDS_LIB)
 
 
 if __name__ == "__main__":
-    build(verbose=True, extra=sys.argv[1:])
+    if sys.argv[1:] == ["--bounds"]:
+        build_bounds_checked(verbose=True)
+    else:
+        build(verbose=True, extra=sys.argv[1:])

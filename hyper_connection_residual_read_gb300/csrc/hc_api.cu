@@ -222,7 +222,15 @@ struct CheckBufs {
 
 using namespace hc;
 
-extern "C" int hc_read_version(void) { return 101; }
+extern "C" int hc_read_version(void) { return 102; }
+
+extern "C" int hc_read_bounds_checked(void) {
+#ifdef HC_BOUNDS_CHECK
+    return 1;
+#else
+    return 0;
+#endif
+}
 
 extern "C" const char* hc_read_strerror(int code) {
     switch (code) {
@@ -234,6 +242,7 @@ extern "C" const char* hc_read_strerror(int code) {
         case HC_ERR_TIMEOUT: return "a bounded device-side wait gave up";
         case HC_ERR_CHECK: return "self check found a mismatch";
         case HC_ERR_NOMEM: return "scratch allocation failed";
+        case HC_ERR_BOUNDS: return "the bounds-checked build skipped an out-of-range access";
         default: return "unknown status";
     }
 }
@@ -379,7 +388,7 @@ extern "C" int hc_read_status(void* stream) {
             return HC_ERR_CUDA;
         return HC_ERR_TIMEOUT;
     }
-    return HC_OK;
+    return (word & kStatusBounds) ? HC_ERR_BOUNDS : HC_OK;
 }
 
 extern "C" int hc_read_check(int max_tokens, uint64_t seed, hc_check_report* rep) {

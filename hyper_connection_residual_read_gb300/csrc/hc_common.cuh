@@ -7,6 +7,25 @@
 
 namespace hc {
 
+// Range checks of the bounds-checked build (compiled with -DHC_BOUNDS_CHECK): before a
+// hand-indexed global access the kernel asks whether elements [i, i + n) lie within
+// the buffer's extent as the kernel's own arguments give it; if not, the access is
+// skipped and bit 2 of the device status word is set (hc_read_status reports
+// HC_ERR_BOUNDS). There is no trap: the context stays usable. The normal build
+// compiles every check to `true`. (TMA accesses need no check: the hardware clips
+// them to the tensor map.)
+#ifdef HC_BOUNDS_CHECK
+__device__ __forceinline__ bool hc_in_range(size_t i, size_t n, size_t extent, int* status) {
+    if (i + n <= extent) return true;
+    if (status != nullptr) atomicOr(status, 2);
+    return false;
+}
+#define HC_IN_RANGE(i, n, extent, status) \
+    ::hc::hc_in_range(static_cast<size_t>(i), static_cast<size_t>(n), static_cast<size_t>(extent), (status))
+#else
+#define HC_IN_RANGE(i, n, extent, status) true
+#endif
+
 // 16-byte streaming load that skips L1 (each weight byte is read once per call).
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
     uint4 v;

@@ -92,7 +92,8 @@ constexpr int kMultiMaxT = 64;   // tokens of one multi-chunk pass at most
 template <int T, bool kMulti>
 __global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kDownThreads, 2)
 down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w_norm,
-                  const uint16_t* __restrict__ W_down, float* lo, float eps, int ntok_run) {
+                  const uint16_t* __restrict__ W_down, float* lo, float eps, int ntok_run,
+                  int* status) {
     namespace cg = cooperative_groups;
     constexpr int NT = kMulti ? kMultiMaxT : T;   // tokens the exchange holds at most
     const int sl = blockIdx.x;                 // K slice 0..7 == rank in the cluster
@@ -111,9 +112,14 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
     //    on the stream has finished): 8 rows x 8 columns, one 16-byte load per row
     uint4 wv[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-        wv[r] = ldg_stream_v4(W_down + (size_t)(j0 + r) * kCols + k0 + col);
-    const uint2 wn = *reinterpret_cast<const uint2*>(w_norm + k0 + 4 * tid);
+    for (int r = 0; r < 8; ++r) {
+        const size_t wi = (size_t)(j0 + r) * kCols + k0 + col;
+        wv[r] = HC_IN_RANGE(wi, 8, (size_t)kRank * kCols, status) ? ldg_stream_v4(W_down + wi)
+                                                                  : make_uint4(0, 0, 0, 0);
+    }
+    const uint2 wn = HC_IN_RANGE(k0 + 4 * tid, 4, kCols, status)
+                         ? *reinterpret_cast<const uint2*>(w_norm + k0 + 4 * tid)
+                         : make_uint2(0, 0);
     // first half of a cluster barrier: the wait before the pushes of step 4 then
     // finds every CTA of the cluster started (their shared memory exists)
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -148,14 +154,18 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
         // 2. activations and per-token sums of squares of R' (zero past the chunk's
         //    tokens)
         float4 xs[T];
+        const size_t act_extent = (size_t)ntok * kCols;   // R and P from the pass's start
+        (void)act_extent;
 #pragma unroll
         for (int t = 0; t < T; ++t)
-            xs[t] = t < nt ? *reinterpret_cast<const float4*>(Rc + (size_t)t * kCols + k0 + 4 * tid)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            xs[t] = t < nt && HC_IN_RANGE((size_t)(tc0 + t) * kCols + k0 + 4 * tid, 4, act_extent, status)
+                        ? *reinterpret_cast<const float4*>(Rc + (size_t)t * kCols + k0 + 4 * tid)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
         if (Pc != nullptr) {
 #pragma unroll
             for (int t = 0; t < T; ++t) {
                 if (t >= nt) continue;
+                if (!HC_IN_RANGE((size_t)(tc0 + t) * kCols + k0 + 4 * tid, 4, act_extent, status)) continue;
                 const float4 p = *reinterpret_cast<const float4*>(Pc + (size_t)t * kCols + k0 + 4 * tid);
                 xs[t].x += p.x; xs[t].y += p.y; xs[t].z += p.z; xs[t].w += p.w;
             }
@@ -226,8 +236,12 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
             // the next chunk's weights, from L2: issued here, where few registers are
             // live, so that they arrive while this chunk is summed and the next staged
 #pragma unroll
-            for (int r = 0; r < 8; ++r)
-                wv[r] = *reinterpret_cast<const uint4*>(W_down + (size_t)(j0 + r) * kCols + k0 + col);
+            for (int r = 0; r < 8; ++r) {
+                const size_t wi = (size_t)(j0 + r) * kCols + k0 + col;
+                wv[r] = HC_IN_RANGE(wi, 8, (size_t)kRank * kCols, status)
+                            ? *reinterpret_cast<const uint4*>(W_down + wi)
+                            : make_uint4(0, 0, 0, 0);
+            }
         }
         __syncthreads();
         // this slice's partial for each of its 16 rows: column groups summed in order
@@ -273,7 +287,8 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
             const float d = inbox[2 * st][t][jj] + inbox[2 * st + 1][t][jj];
             v = fmaf(rs, d, v);
         }
-        lo[(size_t)t * kRank + rb * kDownRowsPerCta + 2 * sl + jj] = v;
+        const size_t li = (size_t)t * kRank + rb * kDownRowsPerCta + 2 * sl + jj;
+        if (HC_IN_RANGE(li, 1, (size_t)ntok * kRank, status)) lo[li] = v;
     }
 }
 
@@ -415,13 +430,19 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
     // 2. lo of the tokens as three bf16 terms in the B tiles (K-major, 128-byte
     //    swizzled, rows term * T + t), R' of this thread's (stream, column), the mix
     float rp[TM];
+    const size_t act_extent = (size_t)T * kCols;
+    (void)act_extent;
 #pragma unroll
-    for (int t = 0; t < TM; ++t)
-        rp[t] = t < T ? R[(size_t)t * kCols + warp * kWidth + c] : 0.f;
+    for (int t = 0; t < TM; ++t) {
+        const size_t ri = (size_t)t * kCols + warp * kWidth + c;
+        rp[t] = t < T && HC_IN_RANGE(ri, 1, act_extent, status) ? R[ri] : 0.f;
+    }
     if (P != nullptr) {
 #pragma unroll
-        for (int t = 0; t < TM; ++t)
-            if (t < T) rp[t] += P[(size_t)t * kCols + warp * kWidth + c];
+        for (int t = 0; t < TM; ++t) {
+            const size_t ri = (size_t)t * kCols + warp * kWidth + c;
+            if (t < T && HC_IN_RANGE(ri, 1, act_extent, status)) rp[t] += P[ri];
+        }
     }
     // (rows past 3 T stay unwritten: they only feed D columns nobody reads)
     const int quads = T * kRank / 4;                     // float4 granules of lo
@@ -431,7 +452,8 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {               // every load of a batch in flight
             const int e = base + tid + i * kTcThreads;
-            if (e < quads) xq[i] = reinterpret_cast<const float4*>(lo)[e];
+            if (e < quads && HC_IN_RANGE(4 * (size_t)e, 4, (size_t)T * kRank, status))
+                xq[i] = reinterpret_cast<const float4*>(lo)[e];
         }
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
@@ -449,7 +471,8 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
         }
     }
     for (int e = tid; e < T * 4; e += kTcThreads)
-        reinterpret_cast<float4*>(&m_s[0][0])[e] = reinterpret_cast<const float4*>(Rmix)[e];
+        if (HC_IN_RANGE(4 * (size_t)e, 4, (size_t)T * 16, status))
+            reinterpret_cast<float4*>(&m_s[0][0])[e] = reinterpret_cast<const float4*>(Rmix)[e];
     tc::fence_proxy_async_smem();
     __syncthreads();
 
@@ -509,6 +532,7 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
                                      g_s[t][2][lane], g_s[t][3][lane])
                            : __int_as_float(0x7fc00000);
         const size_t off = (size_t)t * kCols + warp * kWidth + c;
+        if (!HC_IN_RANGE(off, 1, act_extent, status)) continue;
         out_f32[off] = m;
         out_bf16[off] = to_bf16_bits(m);
         out_fp16[off] = to_fp16_bits(m);
@@ -580,16 +604,17 @@ cudaError_t launch_pass(const Ctx& ctx, const ReadArgs& a, int t0, int n, cudaSt
     const float* R = a.R + off;
     const float* P = a.P ? a.P + off : nullptr;
     float* lo = ctx.s.lo + (size_t)t0 * kRank;
-    CUtensorMap tm_wu;
-    if (!encode_w_up_bf16(&tm_wu, a.W_up, kTcCols)) return cudaErrorInvalidValue;
+    const CUtensorMap* tm_wu = decode_w_up_map(ctx, a.W_up);
+    if (tm_wu == nullptr) return cudaErrorInvalidValue;
     cudaError_t e = allow_up_tc<TM>(ctx.device);
     if (e == cudaSuccess && kMulti) e = allow_down_multi<TC>(ctx.device);
     if (e != cudaSuccess) return e;
     e = launch_pdl(down_slice_kernel<TC, kMulti>, dim3(kDownSlices, kDownRowBlocks), dim3(kDownThreads),
-                   (size_t)kDownDynSmem<TC>, st, R, P, a.w_norm, a.W_down, lo, ctx.eps, n);
+                   (size_t)kDownDynSmem<TC>, st, R, P, a.w_norm, a.W_down, lo, ctx.eps, n,
+                   ctx.s.status);
     if (e != cudaSuccess) return e;
     return launch_pdl(up_mix_tc_kernel<TM>, dim3(kWidth / kTcCols), dim3(kTcThreads),
-                      (size_t)kTcSmem<TM>, st, tm_wu, R, P, (const float*)lo,
+                      (size_t)kTcSmem<TM>, st, *tm_wu, R, P, (const float*)lo,
                       a.Rmix + (size_t)t0 * 16, a.out_f32 + off, a.out_bf16 + off,
                       a.out_fp16 + off, ctx.s.status, n);
 }
@@ -615,6 +640,20 @@ cudaError_t launch_wide(const Ctx& ctx, const ReadArgs& a, int t0, int n, cudaSt
 }
 
 }  // namespace
+
+const CUtensorMap* decode_w_up_map(const Ctx& ctx, const uint16_t* W_up) {
+    WupMapCache& c = ctx.wu_maps;
+    // Fibonacci hashing of the address: weight sets allocated back to back sit a fixed
+    // stride apart, which a plain modulus would send to one slot
+    const uint64_t h = (static_cast<uint64_t>(reinterpret_cast<uintptr_t>(W_up)) >> 8) *
+                       0x9E3779B97F4A7C15ull;
+    const int slot = static_cast<int>(h >> 58);   // 64 slots
+    if (c.key[slot] == W_up) return &c.map[slot];
+    c.key[slot] = nullptr;
+    if (!encode_w_up_bf16(&c.map[slot], W_up, kTcCols)) return nullptr;
+    c.key[slot] = W_up;
+    return &c.map[slot];
+}
 
 void decode_forget_smem(int device) {
     if (device < 0 || device >= 64) return;

@@ -125,19 +125,32 @@ decode_fused_kernel(const float* R, const float* P, const uint16_t* __restrict__
                      : "memory");
 #pragma unroll
         for (int st = 0; st < kStreams; ++st) {
-            const uint16_t* src = W_up + (size_t)(st * kWidth + cbase) * kRank;
+            const size_t wi = (size_t)(st * kWidth + cbase) * kRank;
+            const uint16_t* src = W_up + wi;
             const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&wup_s[st][0][0]));
-            asm volatile(
-                "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-                    "r"(dst), "l"(src), "r"((uint32_t)(kUpColsPerCta * kRank * 2)), "r"(wbar_a)
-                : "memory");
+            if (HC_IN_RANGE(wi, kUpColsPerCta * kRank, (size_t)kCols * kRank, status)) {
+                asm volatile(
+                    "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+                        "r"(dst), "l"(src), "r"((uint32_t)(kUpColsPerCta * kRank * 2)), "r"(wbar_a)
+                    : "memory");
+            } else {
+                // the copy is skipped: its bytes still count, so the wait below ends
+                asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(wbar_a),
+                             "r"((uint32_t)(kUpColsPerCta * kRank * 2))
+                             : "memory");
+            }
         }
     }
     uint4 wv[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-        wv[r] = ldg_stream_v4(W_down + (size_t)(j0 + r) * kCols + k0 + col);
-    const uint2 wn = *reinterpret_cast<const uint2*>(w_norm + k0 + 4 * tid);
+    for (int r = 0; r < 8; ++r) {
+        const size_t wi = (size_t)(j0 + r) * kCols + k0 + col;
+        wv[r] = HC_IN_RANGE(wi, 8, (size_t)kRank * kCols, status) ? ldg_stream_v4(W_down + wi)
+                                                                  : make_uint4(0, 0, 0, 0);
+    }
+    const uint2 wn = HC_IN_RANGE(k0 + 4 * tid, 4, kCols, status)
+                         ? *reinterpret_cast<const uint2*>(w_norm + k0 + 4 * tid)
+                         : make_uint2(0, 0);
     pdl_launch_dependents();
     pdl_wait();
 
@@ -145,10 +158,13 @@ decode_fused_kernel(const float* R, const float* P, const uint16_t* __restrict__
     float4 xs[T];
 #pragma unroll
     for (int t = 0; t < T; ++t)
-        xs[t] = *reinterpret_cast<const float4*>(R + (size_t)t * kCols + k0 + 4 * tid);
+        xs[t] = HC_IN_RANGE((size_t)t * kCols + k0 + 4 * tid, 4, (size_t)T * kCols, status)
+                    ? *reinterpret_cast<const float4*>(R + (size_t)t * kCols + k0 + 4 * tid)
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
     if (P != nullptr) {
 #pragma unroll
         for (int t = 0; t < T; ++t) {
+            if (!HC_IN_RANGE((size_t)t * kCols + k0 + 4 * tid, 4, (size_t)T * kCols, status)) continue;
             const float4 p = *reinterpret_cast<const float4*>(P + (size_t)t * kCols + k0 + 4 * tid);
             xs[t].x += p.x; xs[t].y += p.y; xs[t].z += p.z; xs[t].w += p.w;
         }
@@ -239,7 +255,8 @@ decode_fused_kernel(const float* R, const float* P, const uint16_t* __restrict__
             const float d = pv[2 * st] + pv[2 * st + 1];
             v = fmaf(rs, d, v);
         }
-        lo[t * kRank + rb * kDownRowsPerCta + j] = v;
+        if (HC_IN_RANGE(t * kRank + rb * kDownRowsPerCta + j, 1, T * kRank, status))
+            lo[t * kRank + rb * kDownRowsPerCta + j] = v;
     }
     // publish this CTA's rows: the CTA barrier orders the stores before thread 0's
     // release-add at GPU scope. (No CTA leaves before every CTA has published, so the
@@ -253,8 +270,9 @@ decode_fused_kernel(const float* R, const float* P, const uint16_t* __restrict__
 #pragma unroll
     for (int t = 0; t < T; ++t) {
         const size_t off = (size_t)t * kCols + up_sp * kWidth + cbase + up_cl;
-        rp[t] = R[off];
-        if (P != nullptr) rp[t] += P[off];
+        const bool in = HC_IN_RANGE(off, 1, (size_t)T * kCols, status);
+        rp[t] = in ? R[off] : 0.f;
+        if (P != nullptr && in) rp[t] += P[off];
     }
 
     // 5. wait for every cluster's lo, then read it with R' and the mix
@@ -274,10 +292,13 @@ decode_fused_kernel(const float* R, const float* P, const uint16_t* __restrict__
     }
     __syncthreads();
     for (int e = tid; e < T * kRank / 4; e += kThreads) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(lo) + e);
+        const float4 v = HC_IN_RANGE(4 * (size_t)e, 4, (size_t)T * kRank, status)
+                             ? __ldcg(reinterpret_cast<const float4*>(lo) + e)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
         reinterpret_cast<float4*>(&lo_s[0][0])[e] = v;
     }
-    if (tid < T * 4) reinterpret_cast<float4*>(&m_s[0][0])[tid] = reinterpret_cast<const float4*>(Rmix)[tid];
+    if (tid < T * 4 && HC_IN_RANGE(4 * (size_t)tid, 4, (size_t)T * 16, status))
+        reinterpret_cast<float4*>(&m_s[0][0])[tid] = reinterpret_cast<const float4*>(Rmix)[tid];
     __syncthreads();
     // the last CTA to have read lo resets the counters for the next call
     if (tid == 0) {
@@ -352,9 +373,11 @@ decode_fused_kernel(const float* R, const float* P, const uint16_t* __restrict__
             if (part < 4) {
                 const float m = mix_row(&m_s[t][part * 4], g0, g1, g2, g3);
                 const size_t off = (size_t)t * kCols + part * kWidth + c;
-                out_f32[off] = m;
-                out_bf16[off] = to_bf16_bits(m);
-                out_fp16[off] = to_fp16_bits(m);
+                if (HC_IN_RANGE(off, 1, (size_t)T * kCols, status)) {
+                    out_f32[off] = m;
+                    out_bf16[off] = to_bf16_bits(m);
+                    out_fp16[off] = to_fp16_bits(m);
+                }
             }
         }
     }

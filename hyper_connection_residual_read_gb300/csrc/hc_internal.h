@@ -34,6 +34,7 @@ constexpr int kSchedPairs = 2;
 
 // Device status word bits.
 constexpr int kStatusTimeout = 1;
+constexpr int kStatusBounds = 2;     // the range-checked build skipped an access
 // Bound of a device-side wait on other CTAs before it gives up and reports a timeout.
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
 
@@ -45,6 +46,15 @@ struct Scratch {
     int* sched = nullptr;
     unsigned* sync = nullptr;        // fused decode: [0] clusters that published lo,
                                      // [1] CTAs that have read it (both reset per call)
+};
+
+// Tensor maps over the caller's W_up for the decode up kernel, by W_up's address (a
+// map depends on nothing else): encoding one costs host time on every call otherwise.
+// Direct-mapped by a hash of the address; a collision only re-encodes.
+struct WupMapCache {
+    static constexpr int kSize = 64;
+    const void* key[kSize] = {};
+    CUtensorMap map[kSize];
 };
 
 struct Ctx {
@@ -72,6 +82,7 @@ struct Ctx {
     CUtensorMap tm_lo;               // TMA map over lo3
     // tokens whose lo the last tile-path call left in lo3 (0: none)
     int lo_tokens = 0;
+    mutable WupMapCache wu_maps;     // decode: W_up tensor maps by address
 };
 
 // 128-token tiles of the partials.
@@ -94,6 +105,9 @@ struct ReadArgs {
 // A TMA map over the caller's W_up [kCols][kRank] bf16, in boxes of 64 K x box_rows
 // rows with the 128-byte swizzle (the K-major layout of a tcgen05 operand).
 bool encode_w_up_bf16(CUtensorMap* map, const uint16_t* W_up, int box_rows);
+// The decode up kernel's map over W_up (boxes of 64 K x 32 rows), from the context's
+// cache or encoded into it; nullptr if it cannot be encoded.
+const CUtensorMap* decode_w_up_map(const Ctx& ctx, const uint16_t* W_up);
 
 // Forgets which decode kernels were allowed their shared memory on `device`, then
 // sets those attributes for every chunk size, so that no launch inside a stream

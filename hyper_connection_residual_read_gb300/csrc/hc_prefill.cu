@@ -337,8 +337,10 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
 #pragma unroll
             for (int i = 0; i < 4; ++i) ss[i] = 0.f;
             // w_norm of this lane's 4 columns, loaded one K block ahead
-            uint2 wv_next = *reinterpret_cast<const uint2*>(
-                w_norm + s * kWidth + kq * kDownKBlocksPerTile * kDownBK + kc);
+            const int wk0 = s * kWidth + kq * kDownKBlocksPerTile * kDownBK + kc;
+            uint2 wv_next = HC_IN_RANGE(wk0, 4, kCols, status)
+                                ? *reinterpret_cast<const uint2*>(w_norm + wk0)
+                                : make_uint2(0, 0);
             for (int kb = kq * kDownKBlocksPerTile; kb < (kq + 1) * kDownKBlocksPerTile; ++kb, ++it) {
                 const int slot = it % kDownStages;
                 const uint32_t ph = (it / kDownStages) & 1;
@@ -350,7 +352,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                 for (int i = 0; i < 4; ++i) {
                     const int tr = tt * kTileM + 16 * cw + 4 * i + jr;
                     x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (tr < T) {
+                    if (tr < T && HC_IN_RANGE((size_t)tr * kCols + k, 4, (size_t)T * kCols, status)) {
                         if (P != nullptr) x[i] = *reinterpret_cast<const float4*>(P + (size_t)tr * kCols + k);
                         if (!full) {
                             const float4 r = *reinterpret_cast<const float4*>(R + (size_t)tr * kCols + k);
@@ -359,7 +361,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     }
                 }
                 const uint2 wv = wv_next;
-                if (kb + 1 < (kq + 1) * kDownKBlocksPerTile)
+                if (kb + 1 < (kq + 1) * kDownKBlocksPerTile && HC_IN_RANGE(k + kDownBK, 4, kCols, status))
                     wv_next = *reinterpret_cast<const uint2*>(w_norm + k + kDownBK);
                 const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x), w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
                 if (!mbar_wait(&r_full[slot], ph, &abort_flag, status)) break;
@@ -439,7 +441,8 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             // MMA of the tile, and their buffer is rewritten two tiles later, which
             // cannot start before this tile's second half is drained below
             if (!mbar_wait(&ss_full[lt & 1], (lt >> 1) & 1, &abort_flag, status)) break;
-            if (valid) ssq[prow * kTileM + m] = ss_s[lt & 1][m];
+            if (valid && HC_IN_RANGE(prow * kTileM + m, 1, (size_t)n_tiles * kTileM, status))
+                ssq[prow * kTileM + m] = ss_s[lt & 1][m];
             // column quads, token-minor: [tile][stream][quarter][column / 4][128 tokens]
             // [4 columns], so a lane stores 16 bytes and a warp 512 contiguous bytes;
             // each half-buffer is released as soon as it has been read
@@ -455,7 +458,10 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                         const int cq = (h * kDownHalf + c0) / 4;
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            dst[(cq + i) * kTileM] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                            if (HC_IN_RANGE(prow * kRank * kTileM + 4 * ((size_t)(cq + i) * kTileM + m), 4,
+                                            (size_t)n_tiles * kRank * kTileM, status))
+                                dst[(cq + i) * kTileM] =
+                                    make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                     }
                 }
                 tc_fence_before();
@@ -496,7 +502,10 @@ constexpr int kLoThreads = 512;    // 16 warps, two of the 32 columns each
 
 __global__ void __launch_bounds__(kLoThreads)
 lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ssq,
-                uint16_t* __restrict__ lo3, int T, int max_tokens, float eps) {
+                uint16_t* __restrict__ lo3, int T, int max_tokens, float eps, int* status) {
+    // extents (floats) of the partials and sums of squares of this call's tiles
+    const size_t n_rows = (size_t)((T + kTileM - 1) / kTileM) * kStreams * kDownKSplit;
+    (void)n_rows;
     // the up tile after it (launched with programmatic dependent launch inside a read)
     // may start its prologue, R stream and weight loads now; it waits for this grid
     // before it loads lo
@@ -513,8 +522,9 @@ lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ss
 #pragma unroll
         for (int s = 0; s < kStreams; ++s) {
             float ss = 0.f;
-            if (valid) {
-                const float* q4 = ssq + (base + (size_t)s * kDownKSplit) * kTileM + tr;
+            const size_t qi = (base + (size_t)s * kDownKSplit) * kTileM + tr;
+            if (valid && HC_IN_RANGE(qi + (size_t)(kDownKSplit - 1) * kTileM, 1, n_rows * kTileM, status)) {
+                const float* q4 = ssq + qi;
                 ss = q4[0];
 #pragma unroll
                 for (int q = 1; q < kDownKSplit; ++q) ss += q4[q * kTileM];
@@ -535,11 +545,17 @@ lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ss
 #pragma unroll
         for (int s = 0; s < kStreams; ++s) {
             const float4* ps = p + (size_t)s * kDownKSplit * (kRank / 4) * kTileM;
-            float4 d = ps[0];
+            const size_t last = 4 * (size_t)(ps + (size_t)(kDownKSplit - 1) * (kRank / 4) * kTileM -
+                                             reinterpret_cast<const float4*>(partials));
+            (void)last;
+            float4 d = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (HC_IN_RANGE(last, 4, n_rows * kRank * kTileM, status)) {
+                d = ps[0];
 #pragma unroll
-            for (int q = 1; q < kDownKSplit; ++q) {
-                const float4 w = ps[(size_t)q * (kRank / 4) * kTileM];
-                d.x += w.x; d.y += w.y; d.z += w.z; d.w += w.w;
+                for (int q = 1; q < kDownKSplit; ++q) {
+                    const float4 w = ps[(size_t)q * (kRank / 4) * kTileM];
+                    d.x += w.x; d.y += w.y; d.z += w.z; d.w += w.w;
+                }
             }
             const float r = rs_s[s][tr];
             v[0] = fmaf(r, d.x, v[0]);
@@ -560,6 +576,7 @@ lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ss
         const float x0 = lo_s[r][c4], x1 = lo_s[r][c4 + 1], x2 = lo_s[r][c4 + 2], x3 = lo_s[r][c4 + 3];
         const size_t off = (size_t)trow * kRank + cg * kLoCols + c4;
         const size_t term = (size_t)max_tokens * kRank;
+        if (!HC_IN_RANGE(2 * term + off, 4, 3 * term, status)) continue;
         uint32_t h0, m0, l0, h1, m1, l1;
         split3_bf16(x0, x1, h0, m0, l0);
         split3_bf16(x2, x3, h1, m1, l1);
@@ -776,7 +793,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
             const bool valid = t < T;
             float mx[16];
             if (kOut == kOutMix) {
-                if (valid) {
+                if (valid && HC_IN_RANGE((size_t)t * 16, 16, (size_t)T * 16, status)) {
                     const float4* m4 = reinterpret_cast<const float4*>(Rmix + (size_t)t * 16);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -859,7 +876,9 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                             uint32_t w[8];
 #pragma unroll
                             for (int e = 0; e < kEpiCols; ++e) w[e] = __float_as_uint(o[e]);
-                            if (valid) st_global_v8(out_f32 + (size_t)t * kRowStride + so * kWidth + c, w);
+                            if (valid && HC_IN_RANGE((size_t)t * kRowStride + so * kWidth + c, 8,
+                                                     (size_t)T * kRowStride, status))
+                                st_global_v8(out_f32 + (size_t)t * kRowStride + so * kWidth + c, w);
                         }
                         if (kOut != kOutGated) {
 #pragma unroll
@@ -891,6 +910,7 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
                     const size_t off = (size_t)t * kRowStride + ct * kUpCols + k0 * kEpiCols;
 #pragma unroll
                     for (int so = 0; so < kOutStreams; ++so) {
+                        if (!HC_IN_RANGE(off + so * kWidth, 16, (size_t)T * kRowStride, status)) continue;
                         st_global_v8(out_bf16 + off + so * kWidth, bb[so]);
                         st_global_v8(out_fp16 + off + so * kWidth, hh[so]);
                     }
@@ -923,11 +943,15 @@ upmix_tile_kernel(const float* __restrict__ Rmix, const __grid_constant__ CUtens
 // The mix of the unfused pair: reads gated back and applies the same 4x4 mix.
 __global__ void mix_gated_kernel(const float* __restrict__ gated, const float* __restrict__ Rmix,
                                  float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16,
-                                 uint16_t* __restrict__ out_fp16, int T) {
+                                 uint16_t* __restrict__ out_fp16, int T, int* status) {
     const int per_tok = kWidth / 4;
     const int n = T * per_tok;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const int t = i / per_tok, c = 4 * (i % per_tok);
+        // every access of this element group lies in token t's rows
+        if (!HC_IN_RANGE((size_t)t * kCols + 3 * kWidth + c, 4, (size_t)T * kCols, status) ||
+            !HC_IN_RANGE((size_t)t * 16, 16, (size_t)T * 16, status))
+            continue;
         float mx[16];
         const float4* m4 = reinterpret_cast<const float4*>(Rmix + (size_t)t * 16);
 #pragma unroll
@@ -1084,7 +1108,7 @@ cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, cudaStream_t st
         c.s.sched + 2 * kSchedDown);
     const int rgrid = n_tt * (kRank / kLoCols);
     lo_split_kernel<<<rgrid, kLoThreads, 0, st>>>(c.partials, c.ssq, c.lo3, a.T, c.max_tokens,
-                                                  c.eps);
+                                                  c.eps, c.s.status);
     return cudaGetLastError();
 }
 
@@ -1149,7 +1173,7 @@ cudaError_t launch_prefill_upmix(const Ctx& c, const ReadArgs& a, PrefillMode mo
             const int n = a.T * (kWidth / 4);
             const int mgrid = (n + 255) / 256 < 8 * c.sm_count ? (n + 255) / 256 : 8 * c.sm_count;
             mix_gated_kernel<<<mgrid, 256, 0, st>>>(c.gated, a.Rmix, a.out_f32, a.out_bf16,
-                                                    a.out_fp16, a.T);
+                                                    a.out_fp16, a.T, c.s.status);
             break;
         }
     }

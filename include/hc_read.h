@@ -78,7 +78,9 @@ enum hc_status {
     HC_ERR_CUDA = -4,      /* a CUDA runtime call or a launch failed */
     HC_ERR_TIMEOUT = -5,   /* a bounded device-side wait gave up (status word) */
     HC_ERR_CHECK = -6,     /* hc_read_check found a mismatch */
-    HC_ERR_NOMEM = -7      /* scratch allocation failed */
+    HC_ERR_NOMEM = -7,     /* scratch allocation failed */
+    HC_ERR_BOUNDS = -8     /* the bounds-checked build skipped an out-of-range access
+                              (status word; see hc_read_bounds_checked) */
 };
 
 /* Which kernels run. HC_PATH_AUTO picks the decode kernels for T <= 32 (the measured
@@ -195,8 +197,8 @@ int hc_read_check(int max_tokens, uint64_t seed, hc_check_report* rep);
 /* Waits for `stream`, then reads and clears the device status word of the current
  * device's context: HC_OK, or HC_ERR_TIMEOUT if a bounded wait gave up since the last
  * call (the outputs of that call are then unspecified; the library resets its own
- * schedulers, so the next call runs normally). HC_ERR_CUDA if the stream itself
- * reports an error. */
+ * schedulers, so the next call runs normally), or HC_ERR_BOUNDS if the bounds-checked
+ * build skipped an access. HC_ERR_CUDA if the stream itself reports an error. */
 int hc_read_status(void* stream);
 
 /* Sets the bound of the one-kernel decode read's device-side wait for the other
@@ -251,6 +253,14 @@ int hc_read_noalloc(int tokens,
 
 /* ABI version (major * 100 + minor). */
 int hc_read_version(void);
+
+/* 1 if this library was compiled with -DHC_BOUNDS_CHECK, else 0. In that build every
+ * hand-indexed global access of every kernel is first checked against its buffer's
+ * extent as the kernel's arguments give it; an access out of range is skipped, and
+ * hc_read_status reports HC_ERR_BOUNDS. There is no trap, so the context stays
+ * usable. The normal build has no checks. It stands in for a memory checker, and
+ * the pages have no counterpart of it. */
+int hc_read_bounds_checked(void);
 
 #ifdef __cplusplus
 }

@@ -36,8 +36,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_strerror(lib):
-    assert hc.hc_read_version() == 101
-    for code in range(0, -8, -1):
+    assert hc.hc_read_version() == 102
+    assert hc.hc_read_bounds_checked() is False     # the default build has no checks
+    for code in range(0, -9, -1):
         assert hc.strerror(code) != "unknown status"
     assert hc.strerror(-99) == "unknown status"
 
@@ -49,7 +50,7 @@ def test_binding_constants_match_the_header():
     text = open(os.path.join(ROOT, "include", "hc_read.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     enums = dict((k, int(v)) for k, v in re.findall(r"\b(HC_(?:OK|ERR_\w+|PATH_\w+))\s*=\s*(-?\d+)", text))
-    assert len(enums) == 14, sorted(enums)
+    assert len(enums) == 15, sorted(enums)
     for name, value in enums.items():
         assert getattr(_lib, name) == value, name
     macros = dict((k, int(v)) for k, v in re.findall(r"#define\s+HC_READ_(\w+)\s+(\d+)", text))
