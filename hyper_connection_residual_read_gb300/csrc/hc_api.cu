@@ -263,7 +263,7 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     bool ok = true;
     ok &= cudaMalloc(&c.s.lo, sizeof(float) * (size_t)max_tokens * kRank) == cudaSuccess;
     ok &= cudaMalloc(&c.s.status, sizeof(int)) == cudaSuccess;
-    ok &= cudaMalloc(&c.s.sync, 2 * sizeof(unsigned)) == cudaSuccess;
+    ok &= cudaMalloc(&c.s.sync, kSyncWords * sizeof(unsigned)) == cudaSuccess;
     ok &= cudaMalloc(&c.s.sched, 2 * kSchedPairs * sizeof(int)) == cudaSuccess;
     const size_t ts = (size_t)partial_tiles(max_tokens) * 128;
     ok &= cudaMalloc(&c.partials, sizeof(float) * ts * kStreams * 4 * kRank) == cudaSuccess;
@@ -275,7 +275,7 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
         return HC_ERR_NOMEM;
     }
     if (cudaMemset(c.s.status, 0, sizeof(int)) != cudaSuccess ||
-        cudaMemset(c.s.sync, 0, 2 * sizeof(unsigned)) != cudaSuccess ||
+        cudaMemset(c.s.sync, 0, kSyncWords * sizeof(unsigned)) != cudaSuccess ||
         cudaMemset(c.s.sched, 0, 2 * kSchedPairs * sizeof(int)) != cudaSuccess ||
         decode_setup(device) != cudaSuccess ||
         decode_fused_setup(&c.fused_decode) != cudaSuccess ||
@@ -384,7 +384,7 @@ extern "C" int hc_read_status(void* stream) {
         // a kernel that gave up may have left its scheduler pair or the one-kernel
         // decode read's exchange counters mid-count (the stream is idle here)
         if (cudaMemset(c->s.sched, 0, 2 * kSchedPairs * sizeof(int)) != cudaSuccess ||
-            cudaMemset(c->s.sync, 0, 2 * sizeof(unsigned)) != cudaSuccess)
+            cudaMemset(c->s.sync, 0, kSyncWords * sizeof(unsigned)) != cudaSuccess)
             return HC_ERR_CUDA;
         return HC_ERR_TIMEOUT;
     }

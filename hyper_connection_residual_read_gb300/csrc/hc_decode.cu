@@ -32,6 +32,10 @@
 // tree for the dots) came before the tcgen05 one; its measured times are given at
 // the launcher below.
 //
+// decode_read_kernel is the same read as one kernel (the down kernel's body as its
+// first phase, a global exchange of lo, an up phase on the CUDA cores); it is the
+// HC_PATH_DECODE_ONE_KERNEL path and is described above it.
+//
 // Only the weight pointers carry __restrict__. A load through a const __restrict__
 // pointer may be treated as invariant and moved above griddepcontrol.wait; the
 // activations (R, P, lo, Rmix) are written by the kernels before these on the
@@ -89,11 +93,19 @@ __device__ __forceinline__ float warp_reduce_8rows(const float (&v)[8], int lane
 // The staged activations live in dynamic shared memory: T x 5 KB.
 constexpr int kMultiMaxT = 64;   // tokens of one multi-chunk pass at most
 
-template <int T, bool kMulti>
-__global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kDownThreads, 2)
-down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w_norm,
-                  const uint16_t* __restrict__ W_down, float* lo, float eps, int ntok_run,
-                  int* status) {
+//
+// The body is a device function shared with the one-kernel read (decode_read_kernel),
+// which runs it as its first phase. Hooks: hk.before_wait() is called by every thread
+// once the weight loads are issued, right before the dependency wait, hk.after_wait()
+// right after it, and hk.store_lo(i, v) stores lo element i (token * 320 + row); the
+// row-finishing stores are made by warp 0 alone when ntok <= 16. The staging area (T x
+// 5 KB) starts `a_off` bytes into the dynamic shared memory (addressed from the extern
+// array itself, so that the compiler keeps shared-memory loads and stores).
+template <int T, bool kMulti, typename Hooks>
+__device__ __forceinline__ void down_phase(const float* R, const float* P,
+                                           const uint16_t* __restrict__ w_norm,
+                                           const uint16_t* __restrict__ W_down, float eps,
+                                           int ntok_run, int* status, int a_off, Hooks& hk) {
     namespace cg = cooperative_groups;
     constexpr int NT = kMulti ? kMultiMaxT : T;   // tokens the exchange holds at most
     const int sl = blockIdx.x;                 // K slice 0..7 == rank in the cluster
@@ -130,14 +142,16 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
             if (P != nullptr) prefetch_l2(P + (size_t)t * kCols + k0 + 4 * tid);
         }
     }
+    hk.before_wait();
     pdl_launch_dependents();
     pdl_wait();
+    hk.after_wait();
 
     // staged activations a = R' * w_norm of a chunk. Layout: a lane's 8 columns are
     // stored as two float4 runs, 128 floats apart, so that consecutive lanes read
     // consecutive 16-byte words.
-    extern __shared__ float4 a_dyn[];
-    auto a_s = reinterpret_cast<float4 (*)[kDownSliceCols / 4]>(a_dyn);
+    extern __shared__ __align__(16) uint8_t down_dyn[];
+    auto a_s = reinterpret_cast<float4 (*)[kDownSliceCols / 4]>(down_dyn + a_off);
     __shared__ float red_ss[kDownThreads / 32][T];
     __shared__ float red[T][kDownColGroups][kDownRowsPerCta];
     __shared__ float part[NT][kDownRowsPerCta];    // this slice's partial of each token
@@ -288,8 +302,25 @@ down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w
             v = fmaf(rs, d, v);
         }
         const size_t li = (size_t)t * kRank + rb * kDownRowsPerCta + 2 * sl + jj;
-        if (HC_IN_RANGE(li, 1, (size_t)ntok * kRank, status)) lo[li] = v;
+        if (HC_IN_RANGE(li, 1, (size_t)ntok * kRank, status)) hk.store_lo(li, v);
     }
+}
+
+// lo to global memory, nothing around the wait: the two-kernel read.
+struct PlainLo {
+    float* lo;
+    __device__ __forceinline__ void before_wait() {}
+    __device__ __forceinline__ void after_wait() {}
+    __device__ __forceinline__ void store_lo(size_t i, float v) { lo[i] = v; }
+};
+
+template <int T, bool kMulti>
+__global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kDownThreads, 2)
+down_slice_kernel(const float* R, const float* P, const uint16_t* __restrict__ w_norm,
+                  const uint16_t* __restrict__ W_down, float* lo, float eps, int ntok_run,
+                  int* status) {
+    PlainLo hk{lo};
+    down_phase<T, kMulti>(R, P, w_norm, W_down, eps, ntok_run, status, 0, hk);
 }
 
 // Dynamic shared memory of down_slice_kernel<T, ...>: the staged activations.
@@ -365,6 +396,39 @@ __device__ __forceinline__ void tmem_ld8x3(uint32_t a0, uint32_t a1, uint32_t a2
         h[e] = __uint_as_float(r[e]);
         m[e] = __uint_as_float(r[8 + e]);
         l[e] = __uint_as_float(r[16 + e]);
+    }
+}
+
+// lo of T tokens ([T][kRank] fp32, read through L2) as three bf16 terms in the B tiles
+// of an up MMA: K-major, 128-byte swizzled, one tile of `b_stride` bytes per 64-wide
+// K block, rows term * T + t. Rows past 3 T stay unwritten: they only feed D columns
+// nobody reads. kBatch loads of each thread are in flight at once.
+template <int kThreadsN, int kBatch>
+__device__ __forceinline__ void stage_lo_terms(const float* lo, int T, uint8_t* sB, int b_stride,
+                                               int tid, int* status) {
+    const int quads = T * kRank / 4;                     // float4 granules of lo
+    for (int base = 0; base < quads; base += kBatch * kThreadsN) {
+        float4 xq[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int e = base + tid + i * kThreadsN;
+            if (e < quads && HC_IN_RANGE(4 * (size_t)e, 4, (size_t)T * kRank, status))
+                xq[i] = __ldcg(reinterpret_cast<const float4*>(lo) + e);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int e = base + tid + i * kThreadsN;
+            if (e >= quads) continue;
+            const int t = e / (kRank / 4), k = 4 * (e % (kRank / 4));
+            uint32_t h0, m0, l0, h1, m1, l1;
+            split3_bf16(xq[i].x, xq[i].y, h0, m0, l0);
+            split3_bf16(xq[i].z, xq[i].w, h1, m1, l1);
+            uint8_t* b = sB + (k / kTcKB) * b_stride;
+            const int kin = k % kTcKB;
+            *reinterpret_cast<uint2*>(b + tc::sw128_offset(t, kin)) = make_uint2(h0, h1);
+            *reinterpret_cast<uint2*>(b + tc::sw128_offset(T + t, kin)) = make_uint2(m0, m1);
+            *reinterpret_cast<uint2*>(b + tc::sw128_offset(2 * T + t, kin)) = make_uint2(l0, l1);
+        }
     }
 }
 
@@ -444,39 +508,17 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
             if (t < T && HC_IN_RANGE(ri, 1, act_extent, status)) rp[t] += P[ri];
         }
     }
-    // (rows past 3 T stay unwritten: they only feed D columns nobody reads)
-    const int quads = T * kRank / 4;                     // float4 granules of lo
     constexpr int kBatch = kSmall ? (TM * kRank / 4 + kTcThreads - 1) / kTcThreads : 10;
-    for (int base = 0; base < quads; base += kBatch * kTcThreads) {
-        float4 xq[kBatch];
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {               // every load of a batch in flight
-            const int e = base + tid + i * kTcThreads;
-            if (e < quads && HC_IN_RANGE(4 * (size_t)e, 4, (size_t)T * kRank, status))
-                xq[i] = reinterpret_cast<const float4*>(lo)[e];
-        }
-#pragma unroll
-        for (int i = 0; i < kBatch; ++i) {
-            const int e = base + tid + i * kTcThreads;
-            if (e >= quads) continue;
-            const int t = e / (kRank / 4), k = 4 * (e % (kRank / 4));
-            uint32_t h0, m0, l0, h1, m1, l1;
-            split3_bf16(xq[i].x, xq[i].y, h0, m0, l0);
-            split3_bf16(xq[i].z, xq[i].w, h1, m1, l1);
-            uint8_t* b = sB + (k / kTcKB) * kBStride;
-            const int kin = k % kTcKB;
-            *reinterpret_cast<uint2*>(b + tc::sw128_offset(t, kin)) = make_uint2(h0, h1);
-            *reinterpret_cast<uint2*>(b + tc::sw128_offset(T + t, kin)) = make_uint2(m0, m1);
-            *reinterpret_cast<uint2*>(b + tc::sw128_offset(2 * T + t, kin)) = make_uint2(l0, l1);
-        }
-    }
+    stage_lo_terms<kTcThreads, kBatch>(lo, T, sB, kBStride, tid, status);
     for (int e = tid; e < T * 4; e += kTcThreads)
         if (HC_IN_RANGE(4 * (size_t)e, 4, (size_t)T * 16, status))
             reinterpret_cast<float4*>(&m_s[0][0])[e] = reinterpret_cast<const float4*>(Rmix)[e];
     tc::fence_proxy_async_smem();
     __syncthreads();
 
-    // 3. the MMAs, issued by one thread once the weights have landed
+    // 3. the MMAs, issued by one thread once the weights have landed (20 MMAs of N <= 32
+    //    take about 0.7 us to issue, whether A is read from shared memory or from TMEM
+    //    and whether they accumulate into one D or five: a per-instruction cost)
     __shared__ int ok_s;
     if (tid == 0) {
         bool ok = tc_wait(&w_full, 0, status);
@@ -540,6 +582,258 @@ up_mix_tc_kernel(const __grid_constant__ CUtensorMap tm_wu, const float* R, cons
     if (warp == 0) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, kTcTmemCols<TM>);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// decode_read_kernel - the whole read of up to 8 tokens as one kernel ("#2226
+// STRATA_HC_PERSIST=1 (opt-in, HIP): the verifier's hyper-connection read as one
+// persistent kernel", Summary: at 1-8 tokens the read is dominated by launches and
+// global dependencies; one kernel whose blocks split the down projection by column
+// slices, reduce, then run the up projection).
+//
+// The grid is the down kernel's: 20 clusters (row blocks) of 8 CTAs (K slices), two
+// CTAs per SM, all resident at once (checked at set-up). Each CTA
+//  1. issues its weight streams before the dependency wait: its W_down slice into
+//     registers (the down phase) and, by bulk copy, the 64 W_up rows of its 16 output
+//     columns (4 streams x 16 columns, bf16 as stored) into shared memory, one row
+//     per copy into rows padded to 656 bytes (conflict-free 16-byte reads below);
+//  2. reads the call count right after the wait (its latency hides behind the
+//     staging), then runs the down phase (down_phase): its 2 finished rows of lo go
+//     to global memory;
+//  3. publishes them: one release-add on its row block's counter. Every CTA then
+//     waits until all 20 row blocks' counters have reached 8 adds for this call, one
+//     lane per counter, bounded by %globaltimer (the context's wait limit), and reads
+//     lo through L2 into shared memory;
+//  4. runs the up projection on the CUDA cores: thread (segment q, row r) takes the
+//     dot of W_up row r with lo over K = 64q .. 64q+63 for every token (fp32 fused
+//     multiply-adds, even and odd groups of four in two chains added at the end), and
+//     the five segments are added in order;
+//  5. gates, mixes and writes its 16 columns x 4 streams of every token.
+//
+// The tensor cores are not used here: a kernel that touches tensor memory runs one CTA
+// per SM (measured with the occupancy API), too few for this grid, and at 1-8 tokens
+// the up projection is 64 T x 320 multiply-adds per CTA.
+//
+// Measured, this read is slower than the two kernels (8.6-9.0 against 7.2 us at T = 4
+// with P): a per-phase %globaltimer trace puts about 2 us between the last CTA's lo
+// stores and the pollers seeing them, against about 0.9 us for the two kernels'
+// hand-off through the end of the down grid; a tagged-word exchange (value and call
+// tag in one 64-bit store, the pollers reading the table itself) took as long.
+//
+// Counters: sync[0..19] count the publishing CTAs of each row block over all calls
+// (8 per call), sync[20] is the number of calls completed. Every CTA reads sync[20]
+// after the dependency wait and before it publishes; CTA 0 adds one to it after its
+// wait has seen every row block complete, when every CTA of the call has read it.
+// The next call reads it after its own dependency wait, when this grid has finished.
+// A wait that runs out records a timeout and the CTA writes NaN outputs;
+// hc_read_status, which reports the timeout, zeroes the counters.
+// ---------------------------------------------------------------------------
+constexpr int kRdCols = kWidth / (kDownSlices * kDownRowBlocks);   // 16 output columns a CTA
+constexpr int kRdRows = kStreams * kRdCols;                        // 64 W_up rows
+constexpr int kRdRowBytes = kRank * 2 + 16;                        // padded row: 656 B
+constexpr int kRdWBytes = kRdRows * kRdRowBytes;                   // 41 KB
+constexpr int kRdSegs = kDownThreads / kRdRows;                    // 5 K segments of 64
+constexpr int kRdSegLen = kRank / kRdSegs;                         // 64
+template <int T> constexpr int kRdSmem = kRdWBytes + kDownDynSmem<T>;
+static_assert(kRdSegs * kRdRows == kDownThreads && kRdSegLen % 8 == 0, "up mapping");
+static_assert(2 * (kRdSmem<kDecodeMaxT> + 12 * 1024) <= 228 * 1024, "two CTAs per SM");
+static_assert(kDownRowBlocks + 1 <= kSyncWords, "exchange counters");
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// The one-kernel read's hooks into the down phase: W_up rows requested before the
+// wait, the call count read after it, lo stored to global memory.
+struct CountedLo {
+    const uint16_t* W_up;
+    uint8_t* sW;
+    uint64_t* w_full;
+    int cbase;
+    int* status;
+    float* lo;
+    const unsigned* calls;
+    unsigned gen;
+    __device__ __forceinline__ void before_wait() {
+        if (threadIdx.x >= 32) return;
+        const int lane = threadIdx.x;
+        if (lane == 0) {
+            tc::mbar_init(w_full, 1);
+            tc::fence_barrier_init();
+            tc::mbar_arrive_expect_tx(w_full, kRdRows * kRank * 2);
+        }
+        __syncwarp();
+        // row r = stream * 16 + column; two row copies per lane
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = lane + 32 * h;
+            const size_t wi = (size_t)((r / kRdCols) * kWidth + cbase + r % kRdCols) * kRank;
+            const uint32_t dst = tc::smem_u32(sW + r * kRdRowBytes);
+            const uint32_t bar = tc::smem_u32(w_full);
+            if (HC_IN_RANGE(wi, kRank, (size_t)kCols * kRank, status)) {
+                asm volatile(
+                    "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                    "l"(W_up + wi), "r"((uint32_t)(kRank * 2)), "r"(bar)
+                    : "memory");
+            } else {
+                // the copy is skipped: its bytes still count, so the wait ends
+                asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar),
+                             "r"((uint32_t)(kRank * 2))
+                             : "memory");
+            }
+        }
+    }
+    __device__ __forceinline__ void after_wait() { gen = ld_acquire_u32(calls); }
+    __device__ __forceinline__ void store_lo(size_t i, float v) { lo[i] = v; }
+};
+
+template <int T>
+__global__ void __cluster_dims__(kDownSlices, 1, 1) __launch_bounds__(kDownThreads, 2)
+decode_read_kernel(const float* R, const float* P, const uint16_t* __restrict__ w_norm,
+                   const uint16_t* __restrict__ W_down, const uint16_t* __restrict__ W_up,
+                   const float* Rmix, float* out_f32, uint16_t* out_bf16, uint16_t* out_fp16,
+                   float* lo, unsigned* sync, float eps, int* status, uint64_t lo_wait_ns) {
+    extern __shared__ __align__(16) uint8_t rd_dyn[];
+    uint8_t* sW = rd_dyn;                                 // [64 rows][656 B]
+    // staged activations of the down phase, then lo [T][320] and the segment partials
+    float* lo_s = reinterpret_cast<float*>(rd_dyn + kRdWBytes);
+    float* part_s = lo_s + T * kRank;                     // [T][5 segments][64 rows]
+    __shared__ __align__(8) uint64_t w_full;
+    __shared__ int ok_s;
+    __shared__ __align__(16) float m_s[T][16];
+    __shared__ float g_s[T][kStreams][kRdCols];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cid = blockIdx.y * kDownSlices + blockIdx.x;
+    const int cbase = cid * kRdCols;                      // first output column of the CTA
+
+    // 1-2. weights, call count, the down phase
+    CountedLo hk{W_up, sW, &w_full, cbase, status, lo, &sync[kDownRowBlocks], 0u};
+    down_phase<T, false>(R, P, w_norm, W_down, eps, T, status, kRdWBytes, hk);
+
+    // R' of the gate elements (token t, W_up row r) and the mix, loaded while the other
+    // clusters finish: element e = t * 64 + r, at most two per thread
+    const size_t act_extent = (size_t)T * kCols;
+    (void)act_extent;
+    float rp[2] = {0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int e = tid + h * kDownThreads;
+        if (e >= T * kRdRows) continue;
+        const int t = e / kRdRows, r = e % kRdRows;
+        const size_t ri = (size_t)t * kCols + (r / kRdCols) * kWidth + cbase + r % kRdCols;
+        if (!HC_IN_RANGE(ri, 1, act_extent, status)) continue;
+        rp[h] = R[ri];
+        if (P != nullptr) rp[h] += P[ri];
+    }
+    for (int e = tid; e < T * 4; e += kDownThreads)
+        if (HC_IN_RANGE(4 * (size_t)e, 4, (size_t)T * 16, status))
+            reinterpret_cast<float4*>(&m_s[0][0])[e] = reinterpret_cast<const float4*>(Rmix)[e];
+
+    // 3. publish this CTA's rows (stored by warp 0's lanes), wait for every row block
+    if (warp == 0) {
+        __syncwarp();
+        if (lane == 0)
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&sync[blockIdx.y]) : "memory");
+        bool ok = true;
+        if (lane < kDownRowBlocks) {
+            const unsigned target = (hk.gen + 1) * (unsigned)kDownSlices;
+            if ((int)(ld_acquire_u32(&sync[lane]) - target) < 0) {
+                const uint64_t t0 = tc::globaltimer();
+                while ((int)(ld_acquire_u32(&sync[lane]) - target) < 0) {
+                    if (tc::globaltimer() - t0 > lo_wait_ns) {
+                        atomicOr(status, kStatusTimeout);
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (lane == 0) {
+            ok_s = ok;
+            if (ok && cid == 0) sync[kDownRowBlocks] = hk.gen + 1;
+        }
+    }
+    __syncthreads();
+    //    lo into shared memory (over the staging area: its last reads were before the
+    //    down phase's last barrier); then the W_up rows must have landed
+    const bool lo_ok = ok_s;
+    for (int e = tid; e < T * kRank / 4; e += kDownThreads) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lo_ok && HC_IN_RANGE(4 * (size_t)e, 4, (size_t)T * kRank, status))
+            v = __ldcg(reinterpret_cast<const float4*>(lo) + e);
+        reinterpret_cast<float4*>(lo_s)[e] = v;
+    }
+    if (tid == 0) {
+        // waited for even when lo is missing: no copy may still be in flight at exit
+        bool w_ok = tc_wait(&w_full, 0, status);
+        if (!w_ok) w_ok = tc_wait(&w_full, 0, status);
+        ok_s = lo_ok && w_ok;
+    }
+    __syncthreads();
+    const bool ok = ok_s;
+
+    // 4. the dots: thread (q, r) over K = 64q .. 64q+63, all tokens
+    {
+        const int r = tid % kRdRows, q = tid / kRdRows;
+        const uint4* wrow = reinterpret_cast<const uint4*>(sW + r * kRdRowBytes + q * kRdSegLen * 2);
+        float acc0[T], acc1[T];
+#pragma unroll
+        for (int t = 0; t < T; ++t) acc0[t] = acc1[t] = 0.f;
+#pragma unroll
+        for (int i = 0; i < kRdSegLen / 8; ++i) {
+            const uint4 w = wrow[i];
+            const float wf[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                 bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                const float4* l4 = reinterpret_cast<const float4*>(lo_s + t * kRank + q * kRdSegLen + 8 * i);
+                const float4 x0 = l4[0], x1 = l4[1];
+                float a = acc0[t], b = acc1[t];
+                a = fmaf(wf[0], x0.x, a);
+                b = fmaf(wf[4], x1.x, b);
+                a = fmaf(wf[1], x0.y, a);
+                b = fmaf(wf[5], x1.y, b);
+                a = fmaf(wf[2], x0.z, a);
+                b = fmaf(wf[6], x1.z, b);
+                a = fmaf(wf[3], x0.w, a);
+                b = fmaf(wf[7], x1.w, b);
+                acc0[t] = a;
+                acc1[t] = b;
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < T; ++t) part_s[(t * kRdSegs + q) * kRdRows + r] = acc0[t] + acc1[t];
+    }
+    __syncthreads();
+
+    // 5. u of (token, row): the segments added in order, then the gate; the four
+    //    streams of a column meet in shared memory; then the mix and the three images
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int e = tid + h * kDownThreads;
+        if (e >= T * kRdRows) continue;
+        const int t = e / kRdRows, r = e % kRdRows;
+        const float* p = part_s + t * kRdSegs * kRdRows + r;
+        float u = p[0];
+#pragma unroll
+        for (int q = 1; q < kRdSegs; ++q) u += p[q * kRdRows];
+        g_s[t][r / kRdCols][r % kRdCols] = gate_value(u, rp[h]);
+    }
+    __syncthreads();
+    for (int i = tid; i < T * kStreams * kRdCols; i += kDownThreads) {
+        const int l = i % kRdCols, o = (i / kRdCols) % kStreams, t = i / (kRdCols * kStreams);
+        const float m = ok ? mix_row(&m_s[t][o * 4], g_s[t][0][l], g_s[t][1][l], g_s[t][2][l],
+                                     g_s[t][3][l])
+                           : __int_as_float(0x7fc00000);
+        const size_t off = (size_t)t * kCols + o * kWidth + cbase + l;
+        if (!HC_IN_RANGE(off, 1, act_extent, status)) continue;
+        out_f32[off] = m;
+        out_bf16[off] = to_bf16_bits(m);
+        out_fp16[off] = to_fp16_bits(m);
     }
 }
 
@@ -639,7 +933,70 @@ cudaError_t launch_wide(const Ctx& ctx, const ReadArgs& a, int t0, int n, cudaSt
     return launch_wide_tc<64>(ctx, a, t0, n, tc, st);
 }
 
+// One-kernel read of a chunk of T <= 8 tokens starting at token t0.
+template <int T>
+cudaError_t launch_read_chunk(const Ctx& ctx, const ReadArgs& a, int t0, cudaStream_t st) {
+    const size_t off = (size_t)t0 * kCols;
+    return launch_pdl(decode_read_kernel<T>, dim3(kDownSlices, kDownRowBlocks), dim3(kDownThreads),
+                      (size_t)kRdSmem<T>, st, a.R + off, a.P ? a.P + off : nullptr, a.w_norm,
+                      a.W_down, a.W_up, a.Rmix + (size_t)t0 * 16, a.out_f32 + off,
+                      a.out_bf16 + off, a.out_fp16 + off, ctx.s.lo + (size_t)t0 * kRank, ctx.s.sync,
+                      ctx.eps, ctx.s.status, ctx.lo_wait_ns);
+}
+
+template <int T>
+cudaError_t allow_read_smem() {
+    return cudaFuncSetAttribute(decode_read_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kRdSmem<T>);
+}
+
 }  // namespace
+
+cudaError_t decode_fused_setup(bool* usable) {
+    *usable = false;
+    cudaError_t e = allow_read_smem<1>();
+    if (e == cudaSuccess) e = allow_read_smem<2>();
+    if (e == cudaSuccess) e = allow_read_smem<3>();
+    if (e == cudaSuccess) e = allow_read_smem<4>();
+    if (e == cudaSuccess) e = allow_read_smem<5>();
+    if (e == cudaSuccess) e = allow_read_smem<6>();
+    if (e == cudaSuccess) e = allow_read_smem<7>();
+    if (e == cudaSuccess) e = allow_read_smem<8>();
+    if (e != cudaSuccess) return e;
+    // every cluster of the grid must be resident at once (the CTAs wait on each other);
+    // otherwise the read keeps the two-kernel decode path
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kDownSlices, kDownRowBlocks);
+    cfg.blockDim = dim3(kDownThreads);
+    cfg.dynamicSmemBytes = kRdSmem<kDecodeMaxT>;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, decode_read_kernel<kDecodeMaxT>, &cfg);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cudaSuccess;
+    }
+    *usable = clusters >= kDownRowBlocks;
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode_fused(const Ctx& ctx, const ReadArgs& a, cudaStream_t st) {
+    for (int t0 = 0; t0 < a.T; t0 += kDecodeMaxT) {
+        const int n = a.T - t0 < kDecodeMaxT ? a.T - t0 : kDecodeMaxT;
+        cudaError_t e;
+        switch (n) {
+            case 1: e = launch_read_chunk<1>(ctx, a, t0, st); break;
+            case 2: e = launch_read_chunk<2>(ctx, a, t0, st); break;
+            case 3: e = launch_read_chunk<3>(ctx, a, t0, st); break;
+            case 4: e = launch_read_chunk<4>(ctx, a, t0, st); break;
+            case 5: e = launch_read_chunk<5>(ctx, a, t0, st); break;
+            case 6: e = launch_read_chunk<6>(ctx, a, t0, st); break;
+            case 7: e = launch_read_chunk<7>(ctx, a, t0, st); break;
+            default: e = launch_read_chunk<8>(ctx, a, t0, st); break;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
 const CUtensorMap* decode_w_up_map(const Ctx& ctx, const uint16_t* W_up) {
     WupMapCache& c = ctx.wu_maps;

@@ -44,9 +44,12 @@ struct Scratch {
     // tile-path schedulers: per kernel kind a pair {next tile, CTAs finished}; the
     // last CTA of a launch resets its pair to 0 for the next launch
     int* sched = nullptr;
-    unsigned* sync = nullptr;        // fused decode: [0] clusters that published lo,
-                                     // [1] CTAs that have read it (both reset per call)
+    // one-kernel decode read: [0..19] CTAs of each row block that published their lo
+    // rows, over all calls; [20] calls completed (zeroed with the status word after a
+    // timeout)
+    unsigned* sync = nullptr;
 };
+constexpr int kSyncWords = 32;
 
 // Tensor maps over the caller's W_up for the decode up kernel, by W_up's address (a
 // map depends on nothing else): encoding one costs host time on every call otherwise.
@@ -119,8 +122,9 @@ cudaError_t decode_setup(int device);
 // Decode kernels for any T: launched in chunks of kDecodeMaxT tokens.
 cudaError_t launch_decode(const Ctx& ctx, const ReadArgs& a, cudaStream_t st);
 
-// Decode read as one kernel per chunk of up to 8 tokens (needs s.lo and s.sync).
-// Sets kernel attributes; *usable tells whether all 20 clusters can be resident at once.
+// Decode read as one kernel per chunk of up to 8 tokens (needs s.lo and s.sync; in
+// hc_decode.cu). Sets kernel attributes; *usable tells whether all 20 clusters can be
+// resident at once.
 cudaError_t decode_fused_setup(bool* usable);
 cudaError_t launch_decode_fused(const Ctx& ctx, const ReadArgs& a, cudaStream_t st);
 
