@@ -498,7 +498,11 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
 // 32-byte sectors.
 // ---------------------------------------------------------------------------
 constexpr int kLoCols = 32;
-constexpr int kLoThreads = 512;    // 16 warps, two of the 32 columns each
+// 8 warps, four (token, column quad) pairs a thread: 8 CTAs fit on an SM, so an 8K
+// read's 640 CTAs run in one wave (with 512 threads a CTA, 1.05 waves: 8K read 0.381
+// -> 0.376 ms)
+constexpr int kLoThreads = 256;
+constexpr int kLoPairs = kTileM * (kLoCols / 4) / kLoThreads;
 
 __global__ void __launch_bounds__(kLoThreads)
 lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ssq,
@@ -534,9 +538,9 @@ lo_split_kernel(const float* __restrict__ partials, const float* __restrict__ ss
     }
     __syncthreads();
     // a thread takes (token, column quad) pairs: tokens across the lanes, so each load
-    // instruction of a warp reads 512 contiguous bytes; two pairs per thread
+    // instruction of a warp reads 512 contiguous bytes
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kLoPairs; ++i) {
         const int pidx = threadIdx.x + i * kLoThreads;
         const int tr = pidx & (kTileM - 1), jq = pidx >> 7;     // token, quad 0..7
         const float4* p = reinterpret_cast<const float4*>(partials) +
