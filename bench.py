@@ -47,8 +47,8 @@ EPS = float(np.float32(1e-6))
 # bytes. Capture (two reads, 48 rotated weight sets, so the weights come from DRAM):
 # down_slice_kernel<4, 0> 6,918,912 B, up_mix_tc_kernel<4> 6,910,848 B, both reads,
 # nothing written back to DRAM (the outputs stay in L2).
-NCU_TRAFFIC_T4_P = 13_829_760
-NCU_TRAFFIC_LAST = "13,829,760 B per T=4 read with P (13,783,296 algorithmic)"
+NCU_TRAFFIC_T4_P = 13_829_376
+NCU_TRAFFIC_LAST = "13,829,376 B per T=4 read with P (13,783,296 algorithmic)"
 
 
 def read_bytes(T: int, with_P: bool) -> int:

@@ -22,10 +22,11 @@ constexpr int kDownSlices = kCols / kDownSliceCols;   // 8
 constexpr int kDownRowsPerCta = 16;
 constexpr int kDownRowBlocks = kRank / kDownRowsPerCta;  // 20
 
-// Tokens at or below which HC_PATH_AUTO runs the decode kernels (in chunks of 8).
-// Measured on GB300 with one weight set and a pending write: decode 52.9 us vs tile
-// path 54.4 us at 32 tokens, 78.4 vs 57.8 at 48.
-constexpr int kAutoDecodeMaxT = 32;
+// Tokens at or below which HC_PATH_AUTO runs the decode kernels (up to 64 tokens in one
+// pass over the weights). Measured on GB300 with one weight set and a pending write,
+// us per read: decode 34.4 vs tile path 51.1 at 32 tokens, 52.1 vs 52.0 at 48, 66.6 vs
+// 53.3 at 64.
+constexpr int kAutoDecodeMaxT = 48;
 
 // Scheduler pairs in Scratch::sched.
 constexpr int kSchedUp = 0;

@@ -83,7 +83,7 @@ enum hc_status {
                               (status word; see hc_read_bounds_checked) */
 };
 
-/* Which kernels run. HC_PATH_AUTO picks the decode kernels for T <= 32 (the measured
+/* Which kernels run. HC_PATH_AUTO picks the decode kernels for T <= 48 (the measured
  * crossover) and the tensor-core tile path above that; the others force one path
  * (tests, bench). */
 enum hc_path {
