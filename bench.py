@@ -429,6 +429,17 @@ def gpu_arm(args) -> None:
             hc.hc_read(SWEEP[j][0], v["R"], v["P"], W["w_norm"], W["W_down"], W["W_up"],
                        v["Rmix"], f32, b16, h16, stream=stream)
 
+    stream_handle = stream.cuda_stream
+    e2e_args = {}
+    for g in range(n_groups):
+        for b in range(2):
+            rows = []
+            for j in range(len(SWEEP)):
+                v, f32, b16, h16 = e2e_views[b][j]
+                W = sets[g * len(SWEEP) + j]
+                rows.append((SWEEP[j][0], v["R"], v["P"], W["w_norm"], W["W_down"], W["W_up"],
+                             v["Rmix"], f32, b16, h16))
+            e2e_args[(g, b)] = rows
     e2e_graphs = {}
     with torch.cuda.stream(stream):
         for g in range(n_groups):
@@ -458,11 +469,14 @@ def gpu_arm(args) -> None:
         # the reads, once the inputs are over and buffer b's last outputs have left
         stream.wait_event(ev[("in", b)])
         stream.wait_event(ev[("out", b)])
-        with torch.cuda.stream(stream):   # a graph replays on the current stream
-            if graphed:
+        if graphed:
+            with torch.cuda.stream(stream):   # a graph replays on the current stream
                 e2e_graphs[(k % n_groups, b)].replay()
-            else:                          # the 16 public calls, launched one by one
-                enqueue_reads(k % n_groups, b)
+        else:
+            # the 16 public calls, launched one by one on the stream they name, with
+            # each read's arguments held as a caller holds its tensors
+            for args in e2e_args[(k % n_groups, b)]:
+                hc.hc_read(*args, stream=stream_handle)
         ev[("done", b)].record(stream)
         # the outputs back while the next step computes
         d2h_stream.wait_event(ev[("done", b)])

@@ -3,6 +3,12 @@
 Argument marshalling only. Tensors are passed by ``data_ptr()``; every step of the
 read runs in the library's CUDA kernels. There is no other implementation to fall
 back to: if the library is missing or a call fails, an exception says so.
+
+``hc_read`` and ``hc_read_path`` go through a small CPython module (``_hcpycall``,
+built with the library) that converts the arguments in C and calls the loaded
+library's own entry points: ctypes' per-call conversion of 11 arguments cost more
+host time than the read's two kernel launches. Where that module was not built, the
+calls go through ctypes.
 """
 from __future__ import annotations
 
@@ -67,6 +73,18 @@ class hc_check_report(ctypes.Structure):
 
 
 _lib = None
+_call = None        # the _hcpycall module, bound to _lib's entry points
+
+
+def _bind_call(lib: ctypes.CDLL) -> None:
+    global _call
+    try:
+        from . import _hcpycall
+    except ImportError:
+        return
+    addr = lambda f: ctypes.cast(f, ctypes.c_void_p).value  # noqa: E731
+    _hcpycall.bind(addr(lib.hc_read), addr(lib.hc_read_path))
+    _call = _hcpycall
 
 
 def load(path: str = LIB_PATH) -> ctypes.CDLL:
@@ -108,6 +126,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_read_bounds_checked.argtypes = []
     lib.hc_read_bounds_checked.restype = i32
     _lib = lib
+    _bind_call(lib)
     return lib
 
 
@@ -124,7 +143,7 @@ def _ptr(x) -> int | None:
 def _stream(stream) -> int | None:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
-    if isinstance(stream, int):
+    if type(stream) is int:
         return stream
     return stream.cuda_stream
 
@@ -155,17 +174,31 @@ def hc_read_init(device: int = 0, max_tokens: int = 8, eps: float = 1e-6) -> Non
 def hc_read(tokens, R, P, w_norm, W_down, W_up, Rmix, out_f32, out_bf16, out_fp16,
             stream=None) -> None:
     """Enqueues one read on ``stream`` (default: torch's current stream)."""
-    _check("hc_read", load().hc_read(
-        tokens, _ptr(R), _ptr(P), _ptr(w_norm), _ptr(W_down), _ptr(W_up), _ptr(Rmix),
-        _ptr(out_f32), _ptr(out_bf16), _ptr(out_fp16), _stream(stream)))
+    lib = _lib if _lib is not None else load()
+    if _call is not None:
+        code = _call.read(tokens, R, P, w_norm, W_down, W_up, Rmix, out_f32, out_bf16, out_fp16,
+                          _stream(stream))
+    else:
+        code = lib.hc_read(tokens, _ptr(R), _ptr(P), _ptr(w_norm), _ptr(W_down), _ptr(W_up),
+                           _ptr(Rmix), _ptr(out_f32), _ptr(out_bf16), _ptr(out_fp16),
+                           _stream(stream))
+    if code != HC_OK:
+        raise HcReadError("hc_read", code)
 
 
 def hc_read_path(path, tokens, R, P, w_norm, W_down, W_up, Rmix, out_f32, out_bf16,
                  out_fp16, stream=None) -> None:
     """``hc_read`` with an explicit kernel path (HC_PATH_*)."""
-    _check("hc_read_path", load().hc_read_path(
-        path, tokens, _ptr(R), _ptr(P), _ptr(w_norm), _ptr(W_down), _ptr(W_up), _ptr(Rmix),
-        _ptr(out_f32), _ptr(out_bf16), _ptr(out_fp16), _stream(stream)))
+    lib = _lib if _lib is not None else load()
+    if _call is not None:
+        code = _call.read_path(path, tokens, R, P, w_norm, W_down, W_up, Rmix, out_f32,
+                               out_bf16, out_fp16, _stream(stream))
+    else:
+        code = lib.hc_read_path(path, tokens, _ptr(R), _ptr(P), _ptr(w_norm), _ptr(W_down),
+                                _ptr(W_up), _ptr(Rmix), _ptr(out_f32), _ptr(out_bf16),
+                                _ptr(out_fp16), _stream(stream))
+    if code != HC_OK:
+        raise HcReadError("hc_read_path", code)
 
 
 def hc_read_noalloc(tokens, R, P, w_norm, W_down, W_up, Rmix, out_f32, out_bf16, out_fp16,

@@ -61,6 +61,31 @@ def build(verbose: bool = False, extra: list[str] | None = None, out: str = LIB)
     os.replace(tmp, out)
     if verbose:
         print(f"built {out} from {len(srcs)} sources")
+    if out == LIB:
+        build_pycall(verbose)
+    return out
+
+
+def build_pycall(verbose: bool = False) -> str | None:
+    """The CPython module behind the binding's hc_read / hc_read_path calls
+    (csrc/hc_pycall.c, marshalling only). Without a C compiler or Python headers it
+    is skipped and the binding calls the library through ctypes alone."""
+    import sysconfig
+    out = os.path.join(PKG, "_hcpycall" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+    inc = sysconfig.get_paths()["include"]
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None or not os.path.exists(os.path.join(inc, "Python.h")):
+        if verbose:
+            print("skipped the Python call module (no C compiler or Python headers)")
+        return None
+    tmp = out + ".tmp"
+    cmd = [cc, "-O2", "-shared", "-fPIC", "-I", inc, os.path.join(CSRC, "hc_pycall.c"), "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"building the Python call module failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, out)
+    if verbose:
+        print(f"built {out}")
     return out
 
 
