@@ -94,8 +94,11 @@ enum hc_path {
                                       activations as three bf16 terms, fp32-accurate over
                                       fp32's whole range, weights used as stored) */
     HC_PATH_PREFILL_UNFUSED = 3,   /* tile down, up GEMM writing gated, then the mix */
-    HC_PATH_DECODE_ONE_KERNEL = 4, /* per 8 tokens: one kernel with an in-kernel lo exchange
-                                      (HC_ERR_ARG where its 160 CTAs cannot all be resident) */
+    HC_PATH_DECODE_ONE_KERNEL = 4, /* per 8 tokens: one kernel, the decode down phase, an
+                                      in-kernel lo exchange, an up + gate + mix on the CUDA
+                                      cores (fp32 FMAs; within the tolerance of the others,
+                                      not bitwise equal to them); HC_ERR_ARG where its 160
+                                      CTAs cannot all be resident */
     HC_PATH_PREFILL_BF16_LO = 5    /* the pages' prefill numerics: tile down as in
                                       HC_PATH_PREFILL, then lo rounded once to bf16 and a
                                       single-term bf16 up GEMM on the caller's W_up with the
