@@ -385,6 +385,22 @@ def test_prefill_bitwise_repeatable_and_pending_write(weights):
     assert hc.hc_read_status() == 0
 
 
+@pytest.mark.parametrize("T,path", [(48, hc.HC_PATH_DECODE), (49, hc.HC_PATH_PREFILL)])
+def test_auto_path_switches_at_48_tokens(weights, T, path):
+    """HC_PATH_AUTO runs the decode kernels up to 48 tokens (the measured crossover of the
+    one-pass decode and the tile path) and the tile path above: its bits are those of
+    the path it picks, and both match the oracle."""
+    w, W = weights
+    a = synth.make_activations(60 + T, T, True)
+    R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+    auto = gpu_read(T, R, P, W, M)
+    forced = gpu_read(T, R, P, W, M, path)
+    for x, y in zip(auto, forced):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    want = O.hc_read(a["R"], a["P"], w["w_norm"], w["W_down"], w["W_up"], a["Rmix"], EPS)
+    assert_matches_oracle(auto, want)
+
+
 def test_decode_and_prefill_paths_agree(weights):
     w, W = weights
     for T in (1, 5, 8):
