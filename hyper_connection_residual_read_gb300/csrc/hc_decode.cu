@@ -1,7 +1,9 @@
-// Decode path of the hyper-connection read: 1-8 tokens per launch, bound by the
-// 13 MB of bf16 weights every read streams.
+// Decode path of the hyper-connection read: a few tokens per call (up to 64 in one pass
+// over the weights), latency-bound, with the 13 MB of bf16 weights every pass streams as
+// its floor.
 //
-// Two kernels per chunk of up to 8 tokens, chained by programmatic dependent
+// Two kernels per pass (1-8 tokens; 9-16 as two passes of up to 8; 17-64 in one pass
+// whose down kernel runs the tokens in chunks), chained by programmatic dependent
 // launch so that each kernel's weight stream starts while the previous kernel on
 // the stream is still running:
 //
@@ -17,7 +19,7 @@
 //      to finish; a cluster needs no global counter), so the result is bitwise
 //      repeatable.
 //
-//  up_mix_tc_kernel - the up projection of all the chunk's tokens at once on the
+//  up_mix_tc_kernel - the up projection of all the pass's tokens at once on the
 //      tcgen05 tensor cores (W_up rows as A, lo as three bf16 terms as B, D in
 //      TMEM), then the gate and the 4x4 mix in its epilogue ("#1370 prefill:
 //      opt-in STRATA_HC_UPMIX=1 on CUDA ...", "What it does": the mix fused into
