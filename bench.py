@@ -172,6 +172,48 @@ print(json.dumps({{"sweep_seconds": sweeps, "reads_per_sweep": len(cases)}}))
 """
 
 
+_CPU_PREFILL_SNIPPET = r"""
+import json, multiprocessing as mp, os, sys
+sys.path.insert(0, {root!r})
+from hyper_connection_residual_read_gb300 import synth
+from oracle.timing import timed_read
+
+if __name__ == "__main__":
+    n_tok = int(sys.argv[1])
+    w = synth.make_weights(0)
+    c = synth.make_prefill_chunk(100, n_tok)
+    # one thread: the whole sample in one call (tokens are independent, so the time
+    # scales linearly to a chunk)
+    single = min(timed_read((c["R"], c["Rmix"], w, {eps!r})) for _ in range(2))
+    # every core: the same sample split over one single-threaded process a core
+    cores = len(os.sched_getaffinity(0))
+    pieces = [(c["R"][i::cores].copy(), c["Rmix"][i::cores].copy(), w, {eps!r})
+              for i in range(cores)]
+    import time
+    with mp.get_context("spawn").Pool(cores) as pool:
+        pool.map_async(timed_read, pieces).get(timeout=300)   # warm-up: imports, first touch
+        t0 = time.perf_counter()
+        pool.map_async(timed_read, pieces).get(timeout=300)
+        wall = time.perf_counter() - t0
+    print(json.dumps({{"tokens": n_tok, "single_s": single, "all_cores_s": wall, "cores": cores}}))
+"""
+
+
+def run_oracle_prefill_sample(n_tok: int = 512) -> dict:
+    """The oracle on a sample of prefill tokens, one thread and then one single-threaded
+    process per host core, in a fresh process (started before nothing on the GPU)."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = _CPU_PREFILL_SNIPPET.format(root=ROOT, eps=EPS)
+    r = subprocess.run([sys.executable, "-c", code, str(n_tok)], capture_output=True, text=True,
+                       env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle prefill sample failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def run_oracle_sample(budget_s: float, min_sweeps: int) -> dict:
     """Runs the oracle, single-threaded, in a fresh process over whole sweeps until
     both ``min_sweeps`` sweeps and ``budget_s`` seconds are done."""
@@ -650,6 +692,19 @@ def gpu_arm(args) -> None:
                 "kind": "oracle", "cpu": cpu_model(),
                 "sample": f"{n} reads ({len(d['sweep_seconds'])} sweeps of T=1..8 x "
                           "{no P, P}, one weight set), float64 numpy, 1 thread"}
+            # the prefill chunks: a sample of tokens, extrapolated linearly
+            pf = run_oracle_prefill_sample(512)
+            per_tok_1, per_tok_n = pf["single_s"] / pf["tokens"], pf["all_cores_s"] / pf["tokens"]
+            line["cpu_baseline_prefill"] = {
+                "kind": "oracle", "cpu": cpu_model(), "unit": "ms per chunk",
+                "T8192": {"single_thread_ms": 1e3 * per_tok_1 * 8192,
+                          "all_cores_ms": 1e3 * per_tok_n * 8192},
+                "T32768": {"single_thread_ms": 1e3 * per_tok_1 * 32768,
+                           "all_cores_ms": 1e3 * per_tok_n * 32768},
+                "cores": pf["cores"],
+                "sample": f"{pf['tokens']} tokens of a prefill chunk (R ~ N(0,1), no P), float64 "
+                          "numpy, timed on one thread and on one single-threaded process per "
+                          "core, extrapolated linearly to the chunk (tokens are independent)"}
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
