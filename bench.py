@@ -47,6 +47,8 @@ EPS = float(np.float32(1e-6))
 # bytes. Capture (two reads, 48 rotated weight sets, so the weights come from DRAM):
 # down_slice_kernel<4, 0> 6,918,912 B, up_mix_tc_kernel<4> 6,910,848 B, both reads,
 # nothing written back to DRAM (the outputs stay in L2).
+# GB300's nominal HBM3e bandwidth, GB/s (context beside the measured copy peak)
+NOMINAL_HBM_GBS = 7900.0
 NCU_TRAFFIC_T4_P = 13_829_376
 NCU_TRAFFIC_LAST = "13,829,376 B per T=4 read with P (13,783,296 algorithmic)"
 
@@ -665,6 +667,8 @@ def gpu_arm(args) -> None:
                                        "null: the kernels changed after the last ncu capture; "
                                        "that capture: " + NCU_TRAFFIC_LAST),
                      "peak_source": peaks["source"],
+                     "nominal_peak": NOMINAL_HBM_GBS,
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                      "bytes_per_step": step_bytes},
         "clocks": clocks,
         "e2e": {"value": e2e_us, "unit": "us/read", "h2d_bytes_per_step": h2d,
