@@ -11,6 +11,7 @@
  */
 #define PY_SSIZE_T_CLEAN
 #include <Python.h>
+#include <limits.h>
 #include <stdint.h>
 
 typedef int (*read_fn)(int, void*, void*, void*, void*, void*, void*, void*, void*, void*,
@@ -39,6 +40,20 @@ static int to_ptr(PyObject* o, void** out) {
     return (*out == NULL && PyErr_Occurred()) ? -1 : 0;
 }
 
+/* An int argument of the entry point (token count, path): -1 with an exception set if
+ * it is not an int or does not fit in a C int (rather than truncating it into one that
+ * the library's range checks would accept). */
+static int to_int(PyObject* o, int* out) {
+    const long v = PyLong_AsLong(o);
+    if (v == -1 && PyErr_Occurred()) return -1;
+    if (v < INT_MIN || v > INT_MAX) {
+        PyErr_SetString(PyExc_OverflowError, "argument out of the range of a C int");
+        return -1;
+    }
+    *out = (int)v;
+    return 0;
+}
+
 /* bind(addr_hc_read, addr_hc_read_path) */
 static PyObject* py_bind(PyObject* self, PyObject* const* args, Py_ssize_t n) {
     (void)self;
@@ -65,12 +80,12 @@ static PyObject* py_read(PyObject* self, PyObject* const* args, Py_ssize_t n) {
         PyErr_SetString(PyExc_RuntimeError, "read: not bound to a library");
         return NULL;
     }
-    const long tokens = PyLong_AsLong(args[0]);
-    if (tokens == -1 && PyErr_Occurred()) return NULL;
+    int tokens;
+    if (to_int(args[0], &tokens) != 0) return NULL;
     void* p[10];
     for (int i = 0; i < 10; ++i)
         if (to_ptr(args[1 + i], &p[i]) != 0) return NULL;
-    const int rc = p_read((int)tokens, p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7], p[8], p[9]);
+    const int rc = p_read(tokens, p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7], p[8], p[9]);
     return PyLong_FromLong(rc);
 }
 
@@ -86,14 +101,13 @@ static PyObject* py_read_path(PyObject* self, PyObject* const* args, Py_ssize_t 
         PyErr_SetString(PyExc_RuntimeError, "read_path: not bound to a library");
         return NULL;
     }
-    const long path = PyLong_AsLong(args[0]);
-    const long tokens = PyLong_AsLong(args[1]);
-    if (PyErr_Occurred()) return NULL;
+    int path, tokens;
+    if (to_int(args[0], &path) != 0 || to_int(args[1], &tokens) != 0) return NULL;
     void* p[10];
     for (int i = 0; i < 10; ++i)
         if (to_ptr(args[2 + i], &p[i]) != 0) return NULL;
-    const int rc = p_read_path((int)path, (int)tokens, p[0], p[1], p[2], p[3], p[4], p[5], p[6],
-                               p[7], p[8], p[9]);
+    const int rc = p_read_path(path, tokens, p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7], p[8],
+                               p[9]);
     return PyLong_FromLong(rc);
 }
 

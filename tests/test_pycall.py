@@ -87,3 +87,7 @@ def test_bad_arguments_raise(stub):
         call.read(1, None)                      # wrong count
     with pytest.raises(AttributeError):
         call.read(1, "not a tensor", *([None] * 9))
+    with pytest.raises(OverflowError):               # not truncated into a small count
+        call.read(2 ** 32 + 4, *([None] * 10))
+    with pytest.raises(OverflowError):
+        call.read_path(1, -(2 ** 40), *([None] * 10))
