@@ -714,9 +714,10 @@ def gpu_arm(args) -> None:
         dist.destroy_process_group()
 
 
-def profile_decode(args) -> None:
+def profile_decode(args, path=None) -> None:
     """A small fixed decode workload for ncu: 48 rotated weight sets (larger than
-    L2), ``--steps`` reads of T=4 tokens with a pending write. No timing."""
+    L2), ``--steps`` reads of T=4 tokens with a pending write (``path``: a forced
+    HC_PATH_*, else the default choice). No timing."""
     import torch
     import hyper_connection_residual_read_gb300 as hc
     from hyper_connection_residual_read_gb300 import synth
@@ -730,7 +731,10 @@ def profile_decode(args) -> None:
          for dt in (torch.float32, torch.int16, torch.int16)]
     for i in range(args.steps):
         W = sets[i % N_SETS]
-        hc.hc_read(4, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o)
+        if path is None:
+            hc.hc_read(4, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o)
+        else:
+            hc.hc_read_path(path, 4, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o)
     torch.cuda.synchronize()
     rc = hc.hc_read_status()
     print(json.dumps({"profile": "decode", "reads": args.steps, "status": rc}))
@@ -767,11 +771,13 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "decode1", "prefill"], default=None,
                     help="run a small fixed workload for an ncu capture instead of timing")
     args = ap.parse_args()
     if args.profile == "decode":
         profile_decode(args)
+    elif args.profile == "decode1":      # the one-kernel decode read
+        profile_decode(args, path=4)
     elif args.profile == "prefill":
         profile_prefill(args)
     elif args.impl == "reference":
