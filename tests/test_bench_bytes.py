@@ -44,3 +44,15 @@ def test_sweep_is_the_verify_window():
     """Sixteen reads per step: T = 1..8, each with and without the pending write."""
     assert sorted(bench.SWEEP) == sorted((T, p) for T in range(1, 9) for p in (False, True))
     assert len(bench.SWEEP) == 16
+
+
+def test_prefill_cpu_baseline_worker_times_the_oracle_read():
+    """The worker the prefill CPU baseline runs in each spawned process times exactly
+    the oracle read of its tokens (here two, with the bench's weights)."""
+    import numpy as np
+    from hyper_connection_residual_read_gb300 import synth
+    from oracle.timing import timed_read
+    w = synth.make_weights(0)
+    c = synth.make_prefill_chunk(100, 2)
+    t = timed_read((c["R"], c["Rmix"], w, float(np.float32(1e-6))))
+    assert isinstance(t, float) and t > 0.0
