@@ -103,8 +103,9 @@ def assert_matches_oracle(got, want, tol=TOL_F32):
     delta = tol * float(np.max(np.abs(wf.astype(np.float64))))
     eq_b = assert_images_close(b16, wb, wf, "bf16", delta)
     eq_h = assert_images_close(h16, wh, wf, "fp16", delta)
-    # a wrong rounding mode or a wrong element would show as far more mismatches
-    assert eq_b > 0.99 and eq_h > 0.99, (eq_b, eq_h)
+    # a wrong rounding mode or a wrong element would show as far more mismatches; the
+    # fp16 floor sits lower because its 11 bits resolve the fp32 error on more elements
+    assert eq_b > 0.995 and eq_h > 0.99, (eq_b, eq_h)
     assert np.array_equal(b16, O.f32_to_bf16_bits(f32))
     assert np.array_equal(h16, O.f32_to_f16_bits(f32))
     return r
