@@ -79,6 +79,22 @@ __device__ __forceinline__ void split3_bf16(float x0, float x1, uint32_t& hi, ui
     low = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// The same split by truncation: hi = the top 16 bits of x (sign, exponent, 7 fraction
+// bits), mid = the top 16 bits of x - hi, low = the top 16 bits of x - hi - mid. Both
+// differences are exact, and each term takes the next 8 significant bits, so for a
+// normal x whose remainders stay normal the three terms sum to x exactly (24 bits);
+// masks and byte permutes replace split3_bf16's conversions. Packed as split3_bf16.
+__device__ __forceinline__ void split3_trunc(float x0, float x1, uint32_t& hi, uint32_t& mid,
+                                             uint32_t& low) {
+    const uint32_t a0 = __float_as_uint(x0) & 0xFFFF0000u, a1 = __float_as_uint(x1) & 0xFFFF0000u;
+    const float r0 = x0 - __uint_as_float(a0), r1 = x1 - __uint_as_float(a1);
+    const uint32_t b0 = __float_as_uint(r0) & 0xFFFF0000u, b1 = __float_as_uint(r1) & 0xFFFF0000u;
+    const float s0 = r0 - __uint_as_float(b0), s1 = r1 - __uint_as_float(b1);
+    hi = __byte_perm(a0, a1, 0x7632);
+    mid = __byte_perm(b0, b1, 0x7632);
+    low = __byte_perm(__float_as_uint(s0), __float_as_uint(s1), 0x7632);
+}
+
 // The gate: logistic sigmoid of the up projection times the residual value. expf is
 // the accurate one; the reciprocal is the fast one (within 2 ulp, and 0 when
 // expf(-u) overflows).

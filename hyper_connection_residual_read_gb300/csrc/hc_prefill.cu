@@ -20,10 +20,11 @@
 //                    `gated` instead, and mix_gated applies the same mix afterwards
 //                    (bitwise the same result).
 //
-// Three bf16 terms per activation (hi, mid, low; see split3_bf16) reproduce fp32
-// accuracy with fp32's exponent range, so the path takes any finite fp32 input; the
-// weights are used as the caller stores them (bf16, exact), each product of the MMA
-// is exact, and the sums are fp32 in TMEM.
+// Three bf16 terms per activation reproduce fp32 accuracy with fp32's exponent range,
+// so the path takes any finite fp32 input: the down tile's activations split by
+// truncation (split3_trunc, exact), lo by rounding (split3_bf16, whose hi term is lo's
+// bf16 image for the bf16-lo mode). The weights are used as the caller stores them
+// (bf16, exact), each product of the MMA is exact, and the sums are fp32 in TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -415,8 +416,10 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     sq = fmaf(r.w, r.w, sq);
                     ss[i] += sq;
                     uint32_t h0, m0, l0, h1, m1, l1;
-                    split3_bf16(r.x * w0, r.y * w1, h0, m0, l0);
-                    split3_bf16(r.z * w2, r.w * w3, h1, m1, l1);
+                    // by truncation: exact, and cheaper than rounding (its conversions
+                    // were part of what paces the converters; down stage 2.5% faster)
+                    split3_trunc(r.x * w0, r.y * w1, h0, m0, l0);
+                    split3_trunc(r.z * w2, r.w * w3, h1, m1, l1);
                     const uint32_t off = sw64_offset(row, kc);
                     *reinterpret_cast<uint2*>(ahi + off) = make_uint2(h0, h1);
                     *reinterpret_cast<uint2*>(amid + off) = make_uint2(m0, m1);
