@@ -44,13 +44,17 @@ constexpr int kTerms = 3;              // bf16 terms of an activation (split3_bf
 
 // down_tile
 constexpr int kDownN = kRank;          // 320 accumulator columns (two MMAs of N = 160)
-// K blocks of 32 (one 64-byte swizzle row): four stages of 44 KB (three 8 KB A terms
-// and 20 KB of W_down). With K blocks of 64, two stages of 88 KB were all that fit.
+// K blocks of 32. A stage holds the block's A operand (three 8 KB bf16 terms of 128
+// tokens x 32, 64-byte swizzled) and its W_down columns (20 KB: two 64-byte-swizzled
+// boxes of 160 rows); four stages. R comes through a ring of its own (128 tokens x 32
+// fp32, 16 KB a slot, 128-byte swizzled), read by the converter warps only.
 constexpr int kDownBK = 32;
 constexpr int kDownStages = 4;
+constexpr int kDownRSlots = 2;
 constexpr int kDownTileBytes = kTileM * kDownBK * 2;   // 8 KB: one 128 x 32 bf16 term
 constexpr int kDownBBytes = kDownN * kDownBK * 2;      // 20 KB
 constexpr int kDownStageBytes = kTerms * kDownTileBytes + kDownBBytes;
+constexpr int kDownRBytes = kTileM * kDownBK * 4;      // 16 KB
 constexpr int kDownKBlocks = kWidth / kDownBK;         // 80 per stream
 // Each stream's K is split into quarters with an accumulator (and a partial) each:
 // the tensor cores' fp32 accumulation rounds toward zero at every MMA, so the depth
@@ -76,7 +80,7 @@ constexpr int kDownTileQConsumers = 1 + 8 + 4;
 // half-buffer (at most kDownStages)
 constexpr int kDownAhead = 2;
 static_assert(kDownAhead >= 1 && kDownAhead <= kDownStages, "MMA issue order");
-constexpr int kDownSmem = kDownStages * kDownStageBytes + 1024;
+constexpr int kDownSmem = kDownStages * kDownStageBytes + kDownRSlots * kDownRBytes + 1024;
 
 // upmix_tile
 constexpr int kUpCols = 64;            // output columns per tile (x 4 streams = N 256)
@@ -127,13 +131,6 @@ constexpr int kUpSmem = kUpStages * kUpStageBytes + kRSlots * kRSlot + 1024;
 static_assert(kUpSmem <= 227 * 1024 - 1024, "up tile shared memory");
 static_assert(kDownSmem <= 227 * 1024 - 2048, "down tile shared memory");
 
-// Byte offset of 16-bit element (row r, k) in a K-major 64-byte-swizzled tile: rows of
-// 64 bytes, 8-row atoms of 512 bytes, the 16-byte chunk index XORed with bits 1-2 of r.
-__device__ __forceinline__ uint32_t sw64_offset(int r, int k) {
-    return static_cast<uint32_t>((r >> 3) * 512 + (r & 7) * 64 +
-                                 (((k >> 3) ^ ((r >> 1) & 3)) << 4) + (k & 7) * 2);
-}
-
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
@@ -157,31 +154,34 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // ---------------------------------------------------------------------------
 // down projection, one (128-token tile, stream, K quarter) per tile, persistent CTAs
 //
-// R reaches shared memory by TMA into the stage's A region, 16 KB of fp32 per K
-// block of 32 columns, laid out so that the 16 rows each converter warp owns occupy
-// exactly the bytes where that warp then writes the rows' first two bf16 terms (hi in
-// the first 8 KB, mid in the second, 64-byte swizzled; low goes to the third 8 KB):
-// the warp reads its rows into registers, scales and splits them, and overwrites them
-// in place, with no synchronisation beyond the warp. The view of R that gives this layout is
-// (column, stream, row r, half h, group g) with token = 16 g + 8 h + r; a tile's
-// two loads (h = 0, 1) each take 8 rows of 8 groups. A last tile with fewer than
-// 128 tokens is read by the converter warps from global memory instead.
+// Per K block of 32 columns, TMA brings R into a slot of the R ring (128-byte
+// swizzled; rows past T read as zero) and the W_down columns into a stage. The
+// converter warps take one token row a thread and half of the block's columns: a
+// thread reads its 16 R values (the swizzle spreads the 32 lanes' rows over all
+// banks), adds P, scales by w_norm, splits the products into three bf16 terms and
+// stores them as 16-byte pieces of its row of the stage's 64-byte-swizzled A tiles
+// (again on distinct banks). The shared-memory data pipe, which carries the tensor
+// cores' operand reads besides these, is what bounds the tile.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kDownThreads, 1)
-down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
-                 const uint16_t* __restrict__ w_norm, const __grid_constant__ CUtensorMap tm_wd,
-                 const __grid_constant__ CUtensorMap tm_r, float* __restrict__ partials,
-                 float* __restrict__ ssq, int T, int* __restrict__ status, int* __restrict__ sched) {
+down_tile_kernel(const float* __restrict__ P, const uint16_t* __restrict__ w_norm,
+                 const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_r,
+                 float* __restrict__ partials, float* __restrict__ ssq, int T,
+                 int* __restrict__ status, int* __restrict__ sched) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
+    // per stage: A written by every converter thread and B landed (full_bar), the
+    // stage's MMAs done (empty_bar); per R slot: landed (r_full), read by every
+    // converter thread (r_empty)
     __shared__ __align__(8) uint64_t full_bar[kDownStages], empty_bar[kDownStages];
-    __shared__ __align__(8) uint64_t r_full[kDownStages];
+    __shared__ __align__(8) uint64_t r_full[kDownRSlots], r_empty[kDownRSlots];
     __shared__ __align__(8) uint64_t tq_full[kDownTileQ], tq_empty[kDownTileQ];
     __shared__ int tile_q[kDownTileQ];
     __shared__ __align__(8) uint64_t acc_full, acc_empty[kDownHalfBufs], ss_full[2];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
-    __shared__ float ss_s[2][kTileM];   // per-row sums of squares, by tile parity
+    // per-row sums of squares by tile parity, one per K half of the row
+    __shared__ float ss_s[2][2][kTileM];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = ((T + kTileM - 1) / kTileM) * kStreams * kDownKSplit;
@@ -190,7 +190,10 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
         for (int i = 0; i < kDownStages; ++i) {
             mbar_init(&full_bar[i], 256 + 1);
             mbar_init(&empty_bar[i], 1);
+        }
+        for (int i = 0; i < kDownRSlots; ++i) {
             mbar_init(&r_full[i], 1);
+            mbar_init(&r_empty[i], 256);
         }
         mbar_init(&acc_full, 1);
         for (int i = 0; i < kDownHalfBufs; ++i) mbar_init(&acc_empty[i], 128);
@@ -211,6 +214,7 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
 
     auto sA = [&](int slot, int term) { return smem + slot * kDownStageBytes + term * kDownTileBytes; };
     auto sB = [&](int slot) { return smem + slot * kDownStageBytes + kTerms * kDownTileBytes; };
+    auto sR = [&](int rs) { return smem + kDownStages * kDownStageBytes + rs * kDownRBytes; };
     // the CTA's i-th tile from the queue (n_tiles: no more tiles, or the CTA gave up),
     // taken by a whole warp (its lane 0 releases the entry once every lane has read
     // it) or by one thread
@@ -224,8 +228,8 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
     };
 
     if (warp == 0) {
-        // producer: fetches the CTA's tiles; the stream's W_down columns (320 rows as
-        // two boxes of 160) and, for a full tile, the R block
+        // producer: fetches the CTA's tiles; per K block the R block (into the R ring)
+        // and the stream's W_down columns (320 rows as two boxes of 160, into a stage)
         if (lane == 0) {
             int it = 0;
             // the tile after the current one is fetched one tile early, so that its
@@ -241,21 +245,15 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                 next = (int)gridDim.x + atomicAdd(sched, 1);
                 const int tt = tile / (kStreams * kDownKSplit);
                 const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
-                const bool full = (tt + 1) * kTileM <= T;
                 const int ntt = next / (kStreams * kDownKSplit);
                 const int ns = (next / kDownKSplit) % kStreams, nkq = next % kDownKSplit;
-                const bool next_full = next < n_tiles && (ntt + 1) * kTileM <= T;
                 for (int kb = kq * kDownKBlocksPerTile; kb < (kq + 1) * kDownKBlocksPerTile; ++kb, ++it) {
+                    const int rs = it % kDownRSlots;
+                    if (!mbar_wait(&r_empty[rs], ((it / kDownRSlots) & 1) ^ 1, &abort_flag, status)) break;
+                    mbar_arrive_expect_tx(&r_full[rs], kDownRBytes);
+                    tma_load_3d(sR(rs), &tm_r, kb * kDownBK, s, tt * kTileM, &r_full[rs]);
                     const int slot = it % kDownStages;
-                    const uint32_t ph = (it / kDownStages) & 1;
-                    if (!mbar_wait(&empty_bar[slot], ph ^ 1, &abort_flag, status)) break;
-                    if (full) {
-                        mbar_arrive_expect_tx(&r_full[slot], 2 * kDownTileBytes);
-                        tma_load_5d(sA(slot, 0), &tm_r, kb * kDownBK, s, 0, 0, tt * 8, &r_full[slot]);
-                        tma_load_5d(sA(slot, 1), &tm_r, kb * kDownBK, s, 0, 1, tt * 8, &r_full[slot]);
-                    } else {
-                        mbar_arrive(&r_full[slot]);
-                    }
+                    if (!mbar_wait(&empty_bar[slot], ((it / kDownStages) & 1) ^ 1, &abort_flag, status)) break;
                     mbar_arrive_expect_tx(&full_bar[slot], kDownBBytes);
                     const int x = s * kWidth + kb * kDownBK;
                     tma_load_2d(sB(slot), &tm_wd, x, 0, &full_bar[slot]);
@@ -263,21 +261,18 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                     // R of the block kDownPrefetch stages ahead into L2: later in this
                     // tile, or at the start of the next one
                     const int pk = kb - kq * kDownKBlocksPerTile + kDownPrefetch;
-                    if (pk < kDownKBlocksPerTile) {
-                        if (full)
-                            for (int h = 0; h < 2; ++h)
-                                tma_prefetch_5d(&tm_r, (kb + kDownPrefetch) * kDownBK, s, 0, h, tt * 8);
-                    } else if (next_full) {
-                        const int nkb = nkq * kDownKBlocksPerTile + pk - kDownKBlocksPerTile;
-                        for (int h = 0; h < 2; ++h) tma_prefetch_5d(&tm_r, nkb * kDownBK, ns, 0, h, ntt * 8);
-                    }
+                    if (pk < kDownKBlocksPerTile)
+                        tma_prefetch_3d(&tm_r, (kb + kDownPrefetch) * kDownBK, s, tt * kTileM);
+                    else if (next < n_tiles)
+                        tma_prefetch_3d(&tm_r, (nkq * kDownKBlocksPerTile + pk - kDownKBlocksPerTile) * kDownBK,
+                                        ns, ntt * kTileM);
                 }
             }
         }
     } else if (warp == 1) {
         // MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kTileM, kDownN / 2);
+            const uint32_t idesc = idesc_bf16_f32(kTileM, kDownHalf);
             int it = 0;
             // waits until half-buffer use u may be written: its previous use drained
             auto half_free = [&](int u) {
@@ -304,12 +299,10 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
                                     (kl | term | kk) != 0);
                     }
                 };
-                // the first kDownAhead K blocks' first-half MMAs go before the wait for the
-                // second half-buffer, which the epilogue is usually still draining from the
-                // previous tile; each half still accumulates in (K block, term, K step)
-                // order. With one K block ahead the issuing thread waited about 1 us a tile
-                // there; two took the down stage 1.2% faster, four (the whole ring, whose
-                // refills then wait) 4% slower.
+                // the first kDownAhead K blocks' first-half MMAs go before the wait for
+                // the second half-buffer, which the epilogue is usually still draining
+                // from the previous tile; each half still accumulates in (K block, term,
+                // K step) order
                 for (int kl = 0; kl < kDownAhead; ++kl) {
                     const int slot = (it + kl) % kDownStages;
                     const uint32_t ph = ((it + kl) / kDownStages) & 1;
@@ -341,107 +334,116 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             }
         }
     } else if (warp < 10) {
-        // 8 converter warps produce A: warp cw owns rows 16*cw..16*cw+15 of the tile;
-        // eight lanes take a row, 4 columns each, four rows at a time
-        const int cw = warp - 2;
-        const int kc = 4 * (lane & 7);                  // this lane's 4 columns in a K block
-        const int jr = lane >> 3;                       // its row within a group of four
+        // 8 converter warps produce A: a thread takes token row m and half kh of each
+        // K block (16 columns); warps 2-5 take the first halves of rows 32 (w % 4) +
+        // lane, warps 6-9 the second
+        const int m = (warp & 3) * 32 + lane;
+        const int kh = (warp - 2) >> 2;
+        // this row's 16-byte pieces 2 kh and 2 kh + 1 in a 64-byte-swizzled tile
+        const uint32_t a_off = (m >> 3) * 512 + (m & 7) * 64;
+        const uint32_t a_c0 = ((2 * kh) ^ ((m >> 1) & 3)) << 4, a_c1 = ((2 * kh + 1) ^ ((m >> 1) & 3)) << 4;
         int it = 0;
         for (int lt = 0; !abort_flag; ++lt) {
             const int tile = take_tile(lt, true);
             if (tile >= n_tiles) break;
             const int tt = tile / (kStreams * kDownKSplit);
             const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
-            const bool full = (tt + 1) * kTileM <= T;
+            const int t = tt * kTileM + m;
+            const bool valid = t < T;
+            // sums of squares of the row's four column quads in this K half, each
+            // accumulated over the tile's K blocks
             float ss[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) ss[i] = 0.f;
-            // w_norm of this lane's 4 columns, loaded one K block ahead
-            const int wk0 = s * kWidth + kq * kDownKBlocksPerTile * kDownBK + kc;
-            uint2 wv_next = HC_IN_RANGE(wk0, 4, kCols, status)
-                                ? *reinterpret_cast<const uint2*>(w_norm + wk0)
-                                : make_uint2(0, 0);
+            for (int j = 0; j < 4; ++j) ss[j] = 0.f;
+            // w_norm of this thread's 16 columns, loaded one K block ahead
+            const int wk0 = s * kWidth + kq * kDownKBlocksPerTile * kDownBK + 16 * kh;
+            uint4 wv_next[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+            if (HC_IN_RANGE(wk0, 16, kCols, status)) {
+                wv_next[0] = *reinterpret_cast<const uint4*>(w_norm + wk0);
+                wv_next[1] = *reinterpret_cast<const uint4*>(w_norm + wk0 + 8);
+            }
+            bool ok = true;
             for (int kb = kq * kDownKBlocksPerTile; kb < (kq + 1) * kDownKBlocksPerTile; ++kb, ++it) {
-                const int slot = it % kDownStages;
-                const uint32_t ph = (it / kDownStages) & 1;
-                const int k = s * kWidth + kb * kDownBK + kc;
+                const int slot = it % kDownStages, rs = it % kDownRSlots;
+                const int k = s * kWidth + kb * kDownBK + 16 * kh;
+                // P straight from global memory, issued before the wait
+                float4 p[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) p[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (P != nullptr && valid && HC_IN_RANGE((size_t)t * kCols + k, 16, (size_t)T * kCols, status)) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        p[j] = *reinterpret_cast<const float4*>(P + (size_t)t * kCols + k + 4 * j);
+                }
+                const uint4 wv[2] = {wv_next[0], wv_next[1]};
+                if (kb + 1 < (kq + 1) * kDownKBlocksPerTile && HC_IN_RANGE(k + kDownBK, 16, kCols, status)) {
+                    wv_next[0] = *reinterpret_cast<const uint4*>(w_norm + k + kDownBK);
+                    wv_next[1] = *reinterpret_cast<const uint4*>(w_norm + k + kDownBK + 8);
+                }
+                if (!mbar_wait(&r_full[rs], (it / kDownRSlots) & 1, &abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                // this row's 16 R values: 16-byte chunks 4 kh .. 4 kh + 3 of its 128-byte
+                // row, each at its swizzled place
                 float4 x[4];
-                // P (and, in a last partial tile, R) straight from global memory,
-                // issued before the wait
+                const uint8_t* rrow = sR(rs) + m * 128;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int tr = tt * kTileM + 16 * cw + 4 * i + jr;
-                    x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (tr < T && HC_IN_RANGE((size_t)tr * kCols + k, 4, (size_t)T * kCols, status)) {
-                        if (P != nullptr) x[i] = *reinterpret_cast<const float4*>(P + (size_t)tr * kCols + k);
-                        if (!full) {
-                            const float4 r = *reinterpret_cast<const float4*>(R + (size_t)tr * kCols + k);
-                            x[i].x += r.x; x[i].y += r.y; x[i].z += r.z; x[i].w += r.w;
-                        }
+                for (int j = 0; j < 4; ++j)
+                    x[j] = *reinterpret_cast<const float4*>(rrow + (((4 * kh + j) ^ (m & 7)) << 4));
+                // R + P in that order: the pending write's single rounding
+                if (P != nullptr) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        x[j].x = x[j].x + p[j].x; x[j].y = x[j].y + p[j].y;
+                        x[j].z = x[j].z + p[j].z; x[j].w = x[j].w + p[j].w;
                     }
                 }
-                const uint2 wv = wv_next;
-                if (kb + 1 < (kq + 1) * kDownKBlocksPerTile && HC_IN_RANGE(k + kDownBK, 4, kCols, status))
-                    wv_next = *reinterpret_cast<const uint2*>(w_norm + k + kDownBK);
-                const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x), w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
-                if (!mbar_wait(&r_full[slot], ph, &abort_flag, status)) break;
-                uint8_t* ahi = sA(slot, 0);
-                uint8_t* amid = sA(slot, 1);
-                uint8_t* alow = sA(slot, 2);
-                if (full) {
-                    // R rows j = 4i + jr of this warp: half j >> 3, row j & 7, 128 bytes
-                    // a row; all of them are read before any term is written over them
+                uint32_t hi[8], mid[8], low[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int j = 4 * i + jr;
-                        const float4 r = *reinterpret_cast<const float4*>(
-                            sA(slot, j >> 3) + (cw * 8 + (j & 7)) * 128 + kc * 4);
-                        // R + P in that order: the pending write's single rounding
-                        if (P != nullptr) {
-                            x[i].x = r.x + x[i].x; x[i].y = r.y + x[i].y;
-                            x[i].z = r.z + x[i].z; x[i].w = r.w + x[i].w;
-                        } else {
-                            x[i] = r;
-                        }
-                    }
-                    __syncwarp();
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = 16 * cw + 4 * i + jr;
-                    const float4 r = x[i];
+                for (int j = 0; j < 4; ++j) {
+                    const float4 r = x[j];
                     float sq = r.x * r.x;
                     sq = fmaf(r.y, r.y, sq);
                     sq = fmaf(r.z, r.z, sq);
                     sq = fmaf(r.w, r.w, sq);
-                    ss[i] += sq;
-                    uint32_t h0, m0, l0, h1, m1, l1;
-                    // by truncation: exact, and cheaper than rounding (its conversions
-                    // were part of what paces the converters; down stage 2.5% faster)
-                    split3_trunc(r.x * w0, r.y * w1, h0, m0, l0);
-                    split3_trunc(r.z * w2, r.w * w3, h1, m1, l1);
-                    const uint32_t off = sw64_offset(row, kc);
-                    *reinterpret_cast<uint2*>(ahi + off) = make_uint2(h0, h1);
-                    *reinterpret_cast<uint2*>(amid + off) = make_uint2(m0, m1);
-                    *reinterpret_cast<uint2*>(alow + off) = make_uint2(l0, l1);
+                    ss[j] += sq;
+                    const uint32_t wa = j < 2 ? (j == 0 ? wv[0].x : wv[0].z) : (j == 2 ? wv[1].x : wv[1].z);
+                    const uint32_t wb = j < 2 ? (j == 0 ? wv[0].y : wv[0].w) : (j == 2 ? wv[1].y : wv[1].w);
+                    // by truncation: exact, and cheaper than rounding
+                    split3_trunc(r.x * bf16_lo(wa), r.y * bf16_hi(wa), hi[2 * j], mid[2 * j], low[2 * j]);
+                    split3_trunc(r.z * bf16_lo(wb), r.w * bf16_hi(wb), hi[2 * j + 1], mid[2 * j + 1],
+                                 low[2 * j + 1]);
                 }
+                // the R slot is handed back only now that its values have been used: the
+                // TMA refill (async proxy) must not overtake these shared loads, and the
+                // proxy fence orders them before it
+                fence_proxy_async_smem();
+                mbar_arrive(&r_empty[rs]);
+                // the stage's previous MMAs are done with its A tiles
+                if (!mbar_wait(&empty_bar[slot], ((it / kDownStages) & 1) ^ 1, &abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* ahi = sA(slot, 0) + a_off;
+                uint8_t* amid = sA(slot, 1) + a_off;
+                uint8_t* alow = sA(slot, 2) + a_off;
+                *reinterpret_cast<uint4*>(ahi + a_c0) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(ahi + a_c1) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+                *reinterpret_cast<uint4*>(amid + a_c0) = make_uint4(mid[0], mid[1], mid[2], mid[3]);
+                *reinterpret_cast<uint4*>(amid + a_c1) = make_uint4(mid[4], mid[5], mid[6], mid[7]);
+                *reinterpret_cast<uint4*>(alow + a_c0) = make_uint4(low[0], low[1], low[2], low[3]);
+                *reinterpret_cast<uint4*>(alow + a_c1) = make_uint4(low[4], low[5], low[6], low[7]);
                 fence_proxy_async_smem();
                 mbar_arrive(&full_bar[slot]);
             }
-            if (abort_flag) break;
-            // sums of squares per row: the 8 lanes that share a row, in a fixed order.
-            // The buffer of this parity was last read by the epilogue two tiles ago,
-            // before it released that tile's second half-buffer; this tile's MMAs,
-            // which the conversions run at most four stages (of a tile's twenty K
-            // blocks) ahead of, waited for that release.
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float v = ss[i];
-                v += __shfl_xor_sync(0xffffffffu, v, 1);
-                v += __shfl_xor_sync(0xffffffffu, v, 2);
-                v += __shfl_xor_sync(0xffffffffu, v, 4);
-                if ((lane & 7) == 0) ss_s[lt & 1][16 * cw + 4 * i + jr] = v;
-            }
+            if (!ok) break;
+            // the row's sum of squares over this K half, ((q0 + q1) + (q2 + q3)); the
+            // epilogue adds the two halves. The buffer of this parity was last read by
+            // the epilogue two tiles ago, before it released that tile's second
+            // half-buffer; this tile's MMAs, which the conversions run at most four
+            // stages (of a tile's twenty K blocks) ahead of, waited for that release.
+            ss_s[lt & 1][kh][m] = (ss[0] + ss[1]) + (ss[2] + ss[3]);
             mbar_arrive(&ss_full[lt & 1]);
         }
     } else {
@@ -456,15 +458,16 @@ down_tile_kernel(const float* __restrict__ R, const float* __restrict__ P,
             const int s = (tile / kDownKSplit) % kStreams, kq = tile % kDownKSplit;
             const int t = tt * kTileM + m;
             const bool valid = t < T;
-            if (!mbar_wait(&acc_full, lt & 1, &abort_flag, status)) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&acc_full, lt & 1, &abort_flag, status))) break;
             tc_fence_after();
             const size_t prow = ((size_t)tt * kStreams + s) * kDownKSplit + kq;
             // the sums of squares first: the converters finished them before the last
             // MMA of the tile, and their buffer is rewritten two tiles later, which
             // cannot start before this tile's second half is drained below
-            if (!mbar_wait(&ss_full[lt & 1], (lt >> 1) & 1, &abort_flag, status)) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(&ss_full[lt & 1], (lt >> 1) & 1, &abort_flag, status)))
+                break;
             if (valid && HC_IN_RANGE(prow * kTileM + m, 1, (size_t)n_tiles * kTileM, status))
-                ssq[prow * kTileM + m] = ss_s[lt & 1][m];
+                ssq[prow * kTileM + m] = ss_s[lt & 1][0][m] + ss_s[lt & 1][1][m];
             // column quads, token-minor: [tile][stream][quarter][column / 4][128 tokens]
             // [4 columns], so a lane stores 16 bytes and a warp 512 contiguous bytes;
             // each half-buffer is released as soon as it has been read
@@ -1043,18 +1046,15 @@ bool encode_act(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void*
     return encode_map(map, dt, base, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// R [T][4][2560] fp32 seen as (column, stream, row r, half h, group g), token =
-// 16 g + 8 h + r, in boxes of 64 columns x 1 stream x 8 rows x 1 half x 8 groups.
-// Only whole groups of 16 tokens are described; the kernel uses the map for full
-// 128-token tiles only.
+// R [T][4][2560] fp32 seen as (column, stream, token), in boxes of 32 columns x 1
+// stream x 128 tokens, 128-byte swizzled (a box row is 128 bytes); TMA zero-fills the
+// rows past T of a last partial tile.
 bool encode_down_r(CUtensorMap* map, const float* R, int T) {
-    const cuuint64_t groups = T / 16 > 0 ? (cuuint64_t)(T / 16) : 1;
-    const cuuint64_t dims[5] = {kWidth, kStreams, 8, 2, groups};
-    const cuuint64_t row = (cuuint64_t)kCols * 4;
-    const cuuint64_t strides[4] = {(cuuint64_t)kWidth * 4, row, 8 * row, 16 * row};
-    const cuuint32_t box[5] = {kDownBK, 1, 8, 1, 8};
-    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, R, 5, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_NONE);
+    const cuuint64_t dims[3] = {kWidth, kStreams, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)kWidth * 4, (cuuint64_t)kCols * 4};
+    const cuuint32_t box[3] = {kDownBK, 1, kTileM};
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, R, 3, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // The caller's W_down [kRank][kCols] bf16 in boxes of 32 K x 160 rows, 64-byte
@@ -1130,7 +1130,7 @@ cudaError_t launch_prefill_down(const Ctx& c, const ReadArgs& a, cudaStream_t st
     // an ordinary launch: the first kernel of the read reads R and P, which the kernel
     // before it on the stream may have written
     down_tile_kernel<<<down_grid, kDownThreads, kDownSmem, st>>>(
-        a.R, a.P, a.w_norm, tm_wd, tm_r, c.partials, c.ssq, a.T, c.s.status,
+        a.P, a.w_norm, tm_wd, tm_r, c.partials, c.ssq, a.T, c.s.status,
         c.s.sched + 2 * kSchedDown);
     const int rgrid = n_tt * (kRank / kLoCols);
     lo_split_kernel<<<rgrid, kLoThreads, 0, st>>>(c.partials, c.ssq, c.lo3, a.T, c.max_tokens,

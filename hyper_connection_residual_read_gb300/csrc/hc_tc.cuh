@@ -112,16 +112,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            int c3, int c4, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-        "r"(smem_u32(bar))
-        : "memory");
-}
-
 // L2 cache policy for the hinted copies below: evict_last, for operands that many
 // CTAs read again while other data streams through L2.
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
@@ -150,15 +140,13 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
-// Asks L2 to fetch a 5D tile of a tensor map (no shared memory, no completion):
+// Asks L2 to fetch a 3D tile of a tensor map (no shared memory, no completion):
 // a later TMA load of the same tile then finds it in L2.
-__device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap* map, int c0, int c1, int c2,
-                                                int c3, int c4) {
-    asm volatile(
-        "cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-        : "memory");
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
 }
 
 // TMA tile store from shared memory, tracked as a bulk async group of this thread.
