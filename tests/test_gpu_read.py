@@ -264,6 +264,36 @@ def test_prefill_chunk_sampled_tokens(weights, T, seed):
     assert hc.hc_read_status() == 0
 
 
+def test_prefill_several_tiles_per_cta_partial_last_tile(weights):
+    """T = 2000 with P: 16 token tiles (256 down tiles over at most 152 CTAs, so CTAs
+    take several, and the R and operand rings wrap across tiles), the last tile 80
+    tokens long (R's rows past T are read as zero). The first and last 128 tokens and
+    128 random ones against the oracle; the same bits from a second call."""
+    w, W = weights
+    T = 2000
+    a = synth.make_activations(2000, T, True)
+    R, P, M = dev_f32(a["R"]), dev_f32(a["P"]), dev_f32(a["Rmix"])
+    o = alloc_out(T)
+    hc.hc_read_path(hc.HC_PATH_PREFILL, T, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(o[0]).all())
+    rng = np.random.default_rng(2000)
+    idx = np.unique(np.concatenate([np.arange(128), np.arange(T - 128, T),
+                                    rng.choice(T, 128, replace=False)]))
+    want = O.hc_read_tokens(idx, a["R"], a["P"], w["w_norm"], w["W_down"], w["W_up"],
+                            a["Rmix"], EPS)
+    ti = torch.from_numpy(idx).cuda()
+    got = (o[0][ti].cpu().numpy(), o[1][ti].cpu().numpy().view(np.uint16),
+           o[2][ti].cpu().numpy().view(np.uint16))
+    assert_matches_oracle(got, want)
+    o2 = alloc_out(T)
+    hc.hc_read_path(hc.HC_PATH_PREFILL, T, R, P, W["w_norm"], W["W_down"], W["W_up"], M, *o2)
+    torch.cuda.synchronize()
+    for x, y in zip(o, o2):
+        assert bool(torch.equal(x, y))
+    assert hc.hc_read_status() == 0
+
+
 def test_self_check_passes(ctx):
     code, rep = hc.hc_read_check(8, 1234)
     assert code == 0, rep
