@@ -160,8 +160,8 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // thread reads its 16 R values (the swizzle spreads the 32 lanes' rows over all
 // banks), adds P, scales by w_norm, splits the products into three bf16 terms and
 // stores them as 16-byte pieces of its row of the stage's 64-byte-swizzled A tiles
-// (again on distinct banks). The shared-memory data pipe, which carries the tensor
-// cores' operand reads besides these, is what bounds the tile.
+// (again on distinct banks). The converters set the tile's pace: a K block's
+// conversion takes them longer than its 12 MMAs take the tensor core.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kDownThreads, 1)
 down_tile_kernel(const float* __restrict__ P, const uint16_t* __restrict__ w_norm,
