@@ -23,7 +23,7 @@ def main(path: str) -> None:
     hc.load(path)
     from _hc import EPS, alloc_out, assert_matches_oracle, dev_f32, dev_weights, gpu_read
     assert hc.hc_read_bounds_checked(), "not the bounds-checked build"
-    hc.hc_read_init(0, 512, EPS)
+    hc.hc_read_init(0, 2048, EPS)
     w = synth.make_weights(0)
     W = dev_weights(w)
 
@@ -37,7 +37,10 @@ def main(path: str) -> None:
              (hc.HC_PATH_DECODE, 8, True), (hc.HC_PATH_DECODE, 13, True),
              (hc.HC_PATH_DECODE, 40, True), (hc.HC_PATH_DECODE_ONE_KERNEL, 4, True),
              (hc.HC_PATH_PREFILL, 8, True), (hc.HC_PATH_PREFILL, 129, False),
-             (hc.HC_PATH_PREFILL, 300, True), (hc.HC_PATH_PREFILL_UNFUSED, 129, True)]
+             (hc.HC_PATH_PREFILL, 300, True), (hc.HC_PATH_PREFILL_UNFUSED, 129, True),
+             # several down tiles per CTA (the rings wrap across tiles), an 80-token
+             # last tile
+             (hc.HC_PATH_PREFILL, 2000, True)]
     for path, T, with_P in cases:
         a = synth.make_activations(600 + T, T, with_P)
         got = gpu_read(T, dev_f32(a["R"]), dev_f32(a["P"]), W, dev_f32(a["Rmix"]), path)
