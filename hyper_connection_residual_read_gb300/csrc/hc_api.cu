@@ -6,8 +6,11 @@
 // weights and inputs for 1..8 tokens, with and without the pending write, and
 // compares outputs bit for bit before trusting a kernel.
 #include <cuda_runtime.h>
+#include <errno.h>
+#include <limits.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "hc_common.cuh"
@@ -107,7 +110,7 @@ int run(int path, const ReadArgs& a, cudaStream_t st) {
     if (path < HC_PATH_AUTO || path > HC_PATH_PREFILL_BF16_LO) return HC_ERR_ARG;
     if (int e = validate(*c, a)) return e;
     if (a.T == 0) return HC_OK;
-    if (path == HC_PATH_AUTO) path = a.T <= kAutoDecodeMaxT ? HC_PATH_DECODE : HC_PATH_PREFILL;
+    if (path == HC_PATH_AUTO) path = a.T <= c->auto_decode_max_t ? HC_PATH_DECODE : HC_PATH_PREFILL;
     cudaError_t ce;
     switch (path) {
         case HC_PATH_DECODE:
@@ -247,6 +250,21 @@ extern "C" const char* hc_read_strerror(int code) {
     }
 }
 
+namespace {
+// The crossover of HC_PATH_AUTO from the environment: HC_READ_DECODE_MAX_T, a decimal
+// token count >= 0 (a debugging aid). Unset, empty or not such a number: the measured
+// default.
+int auto_decode_max_t_from_env() {
+    const char* v = getenv("HC_READ_DECODE_MAX_T");
+    if (v == nullptr || *v == '\0') return kAutoDecodeMaxT;
+    char* end = nullptr;
+    errno = 0;
+    const long t = strtol(v, &end, 10);
+    if (errno != 0 || end == v || *end != '\0' || t < 0 || t > INT_MAX) return kAutoDecodeMaxT;
+    return static_cast<int>(t);
+}
+}  // namespace
+
 extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     if (device < 0 || device >= kMaxDevices || max_tokens < 1) return HC_ERR_ARG;
     if (cudaSetDevice(device) != cudaSuccess) return HC_ERR_CUDA;
@@ -258,6 +276,7 @@ extern "C" int hc_read_init(int device, int max_tokens, float eps) {
     c.device = device;
     c.max_tokens = max_tokens;
     c.eps = eps > 0.f ? eps : 1e-6f;
+    c.auto_decode_max_t = auto_decode_max_t_from_env();
     c.sm_count = prop.multiProcessorCount;
     strncpy(c.name, prop.name, sizeof(c.name) - 1);
     bool ok = true;

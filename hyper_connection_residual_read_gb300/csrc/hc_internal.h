@@ -71,6 +71,10 @@ struct Ctx {
     // bound of the one-kernel decode read's wait for every CTA's lo (a test may shorten
     // it to make the wait run out; hc_read_set_wait_limit)
     uint64_t lo_wait_ns = kDefaultWaitNs;
+    // HC_PATH_AUTO runs the decode kernels at or below this many tokens:
+    // kAutoDecodeMaxT, or the HC_READ_DECODE_MAX_T environment variable as read by
+    // hc_read_init
+    int auto_decode_max_t = kAutoDecodeMaxT;
     char name[64] = {0};
     Scratch s;
     // prefill scratch

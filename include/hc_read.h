@@ -85,7 +85,9 @@ enum hc_status {
 
 /* Which kernels run. HC_PATH_AUTO picks the decode kernels for T <= 48 (the measured
  * crossover) and the tensor-core tile path above that; the others force one path
- * (tests, bench). */
+ * (tests, bench). The environment variable HC_READ_DECODE_MAX_T, a decimal token count
+ * >= 0 read by hc_read_init, moves the crossover for that context (a debugging aid;
+ * unset, empty or malformed keeps 48). Both paths are valid at every T. */
 enum hc_path {
     HC_PATH_AUTO = 0,
     HC_PATH_DECODE = 1,            /* per 8 tokens: sliced down kernel (CUDA cores, clusters),

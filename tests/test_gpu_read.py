@@ -7,6 +7,8 @@ that cross the 8-token launch chunks, a cold round of 48 weight sets, and long
 prefill chunks checked on sampled tokens. Plus determinism, the pending-write
 identity, argument errors and output guard bytes.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -415,6 +417,8 @@ def test_prefill_bitwise_repeatable_and_pending_write(weights):
     assert hc.hc_read_status() == 0
 
 
+@pytest.mark.skipif(bool(os.environ.get("HC_READ_DECODE_MAX_T")),
+                    reason="the environment moves HC_PATH_AUTO's crossover")
 @pytest.mark.parametrize("T,path", [(48, hc.HC_PATH_DECODE), (49, hc.HC_PATH_PREFILL)])
 def test_auto_path_switches_at_48_tokens(weights, T, path):
     """HC_PATH_AUTO runs the decode kernels up to 48 tokens (the measured crossover of the
