@@ -366,7 +366,7 @@ def _bf16_lo(T):
     return lo.cpu().numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("T,with_P,seed", [(300, True, 31), (8192, False, 100)])
+@pytest.mark.parametrize("T,with_P,seed", [(300, True, 31), (2000, True, 32), (8192, False, 100)])
 def test_bf16_lo_path_against_the_read_from_its_lo(weights, T, with_P, seed):
     """The pages' prefill numerics: lo rounded once to bf16 for a one-term bf16 up
     GEMM. Its output matches, to the fp32 tolerance, the oracle's read computed from
@@ -447,7 +447,7 @@ def test_decode_and_prefill_paths_agree(weights):
 
 
 @pytest.mark.parametrize("T,with_P,seed", [(1, True, 41), (129, True, 42), (300, False, 43),
-                                           (8192, False, 101)])
+                                           (2000, True, 44), (8192, False, 101)])
 def test_readout_y_against_oracle(weights, T, with_P, seed):
     """The 2560-wide read-out (y = sum of the gated streams, with its images) through
     hc_read_y, against the oracle's; long chunks on sampled tokens."""
